@@ -1,0 +1,419 @@
+#!/usr/bin/env python3
+"""Benchmark of the verify-and-graft step on one GB300 (or N independent replicas).
+
+One step = a1 prune + a2 graft + a3 mask + a4 tree attention + a5/a6 verify + a7 table
+update for every request of the workload, issued through the C ABI on one stream with no
+host synchronisation. The timed region replays a CUDA graph of K such steps; the inputs
+rotate over several device copies whose total size is a multiple of the 129 MB L2, so
+every step streams its K/V cache and logits from HBM.
+
+Prints ONE JSON line (rank 0). `--impl reference` times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workload import CONFIGS, make_scenario  # noqa: E402
+
+DEFAULT_CONFIG = 3   # the long-context workload (32K prefix) on which the HBM bar is stated
+METRIC = "verify-and-graft steps/s on 1 GB300; tree-attn HBM GB/s as % of ~8 TB/s roofline"
+KERNELS_PER_STEP = {True: 9, False: 8}  # with / without the graft launch
+L2_BYTES = 129 * 2 ** 20
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6800.0), "measured"
+    return 6800.0, "fallback"
+
+
+def attn_bytes(scn) -> int:
+    """Algorithmic bytes of one gt_tree_attn call: the K and V rows each request attends
+    (prefix + tree), Q read once, O written once."""
+    es = 2 if scn.dtype == "bf16" else 4
+    kv = sum(int(P) + scn.N for P in scn.prefix_len) * scn.Hkv * scn.d * es * 2
+    qo = 2 * scn.B * scn.N * scn.Hq * scn.d * es
+    return kv + qo
+
+
+def step_bytes(scn) -> int:
+    """Algorithmic bytes of the whole step: attention bytes + logits + the tree arrays, the
+    template, the table rows read by the graft and written by the update."""
+    B, N = scn.B, scn.N
+    logits = B * N * scn.V * 4
+    tree = B * scn.Nin * 12 + B * N * (4 * 6 + 8)          # prune in, tree out, mask, pos, depth
+    table = B * N * scn.k * 4 * 2 + len(scn.tpar) * 8       # graft reads + update writes
+    verify = B * N * scn.k * 8 + B * N * 16
+    return attn_bytes(scn) + logits + tree + table + verify
+
+
+def _clock_sampler():
+    cmd = ["nvidia-smi", "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,"
+           "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+           "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+           "clocks_event_reasons.sw_power_cap", "--format=csv,noheader,nounits", "-lms", "200"]
+    try:
+        return subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+    except OSError:
+        return None
+
+
+def _clock_summary(proc, gpu_index: int):
+    if proc is None:
+        return None
+    proc.terminate()
+    try:
+        out, _ = proc.communicate(timeout=5)
+    except subprocess.TimeoutExpired:
+        proc.kill()
+        out, _ = proc.communicate()
+    sm, mx, reasons = [], None, set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in out.strip().splitlines():
+        f = [x.strip() for x in line.split(",")]
+        if len(f) < 9 or not f[0].isdigit() or int(f[0]) != gpu_index:
+            continue
+        try:
+            sm.append(float(f[1]))
+            mx = float(f[2])
+        except ValueError:
+            continue
+        for nm, v in zip(names, f[5:9]):
+            if v.lower() == "active":
+                reasons.add(nm)
+    if not sm:
+        return None
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+            "samples": len(sm)}
+
+
+def _traffic_record(kernel_key: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source it was taken
+    on is unchanged (sha256 of the CUDA sources), else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f).get(kernel_key)
+    if not rec:
+        return None
+    return rec["bytes_per_launch"] if rec.get("src_sha256") == _src_hash() else None
+
+
+def _src_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "tree_speculative_decoding_parent_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()
+
+
+# --------------------------------------------------------------------------------------
+# CPU oracle timing (reference arm and cpu_baseline)
+# --------------------------------------------------------------------------------------
+
+
+def time_oracle(scn, steps: int, budget_s: float):
+    """Runs the oracle's whole step on the same workload; returns (steps/s, steps, seconds)."""
+    import oracle
+    tree = oracle.step_tree_phase(scn.parent_in, scn.tokens_in, scn.score_in,
+                                  [scn.Nin] * scn.B, scn.keep, scn.thresh, scn.tpar, scn.trank,
+                                  scn.R, scn.table, scn.prefix_len, scn.N)
+    logits = scn.logits(tree["parent"], tree["tokens"], tree["n_nodes"])
+    dec = oracle.bf16_to_f64 if scn.dtype == "bf16" else (lambda a: np.asarray(a, np.float64))
+    done, t0 = 0, time.perf_counter()
+    table = scn.table
+    while done < steps:
+        tree = oracle.step_tree_phase(scn.parent_in, scn.tokens_in, scn.score_in,
+                                      [scn.Nin] * scn.B, scn.keep, scn.thresh, scn.tpar,
+                                      scn.trank, scn.R, table, scn.prefix_len, scn.N)
+        for b in range(scn.B):
+            n, P = int(tree["n_nodes"][b]), int(scn.prefix_len[b])
+            oracle.tree_attn(dec(scn.Q[b]), dec(scn.K[b][:, :P + n]), dec(scn.Vc[b][:, :P + n]),
+                             tree["parent"][b], n, P, scn.scale)
+        res = oracle.step_verify_phase(tree, logits, table, scn.prefix_len, scn.k)
+        table = res["table"]
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return done / dt, done, dt
+
+
+def run_reference(args, rank: int, world: int):
+    if rank != 0:
+        return None
+    scn = make_scenario(args.config)
+    time_oracle(scn, 1, 0.0)  # one untimed warm-up step (the oracle has no caches to fill)
+    value, done, dt = time_oracle(scn, args.steps, args.ref_budget)
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s",
+        "n_gpus": world, "steps": done, "warmup": args.warmup, "ms_per_step": 1e3 * dt / done,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded generator; see DESIGN.md input recipe)",
+        "config": {"workload": CONFIGS[args.config]["name"], "config_id": args.config},
+        "cpu_baseline": {"value": value, "unit": "steps/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{done} whole steps of the same workload on the host CPU "
+                                   f"(numpy float64; BLAS may use all {cores} cores)"},
+        "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+# --------------------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------------------
+
+
+def run_gpu(args, rank: int, world: int, local_rank: int):
+    import torch
+    from tree_speculative_decoding_parent_gb300 import build, gt
+    from tree_speculative_decoding_parent_gb300.step import (StepBuffers, StepShape,
+                                                             run_step, run_tree_phase,
+                                                             run_verify_phase)
+    build.build()
+    gt.load()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    scn = make_scenario(args.config, seed=args.config + 1000 * rank)
+    shape = StepShape(B=scn.B, Nin=scn.Nin, N=scn.N, V=scn.V, k=scn.k, Hq=scn.Hq, Hkv=scn.Hkv,
+                      d=scn.d, Lcap=scn.Lcap, T=len(scn.tpar),
+                      dtype=gt.GT_BF16 if scn.dtype == "bf16" else gt.GT_F32)
+    bf16 = scn.dtype == "bf16"
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    def qkv(a):
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16) \
+            if bf16 else torch.from_numpy(np.ascontiguousarray(a))
+        return t.to(dev)
+
+    base = dict(score_in=to_dev(scn.score_in), parent_in=to_dev(scn.parent_in),
+                tokens_in=to_dev(scn.tokens_in), keep=to_dev(scn.keep), R=to_dev(scn.R),
+                table=to_dev(scn.table), prefix_len=to_dev(scn.prefix_len),
+                Q=qkv(scn.Q), K=qkv(scn.K), V=qkv(scn.Vc))
+    if scn.thresh is not None:
+        base["thresh"] = to_dev(scn.thresh)
+    if len(scn.tpar):
+        base["tpar"], base["trank"] = to_dev(scn.tpar), to_dev(scn.trank)
+    # plant the target logits on the tree this GPU path builds from the inputs
+    buf = StepBuffers(shape, dev)
+    run_tree_phase(buf, base)
+    torch.cuda.synchronize()
+    logits_np = scn.logits(buf.parent.cpu().numpy(), buf.tokens.cpu().numpy(),
+                           buf.n_nodes.cpu().numpy())
+    base["logits"] = to_dev(logits_np)
+    per_set = sum(base[k].numel() * base[k].element_size()
+                  for k in ("K", "V", "logits", "Q", "table"))
+    nsets = max(2, -(-4 * L2_BYTES // per_set))
+    sets = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(nsets - 1)]
+    stream = torch.cuda.current_stream(dev)
+
+    # eager warm-up (first calls set kernel attributes), then graphs
+    run_step(buf, sets[0], scale=scn.scale)
+    torch.cuda.synchronize()
+    if int(buf.err.item()) != 0:
+        raise RuntimeError(f"device error {gt.status_string(int(buf.err.item()))}")
+
+    def capture(nsteps: int, with_events: bool):
+        g = torch.cuda.CUDAGraph()
+        evs = []
+        with torch.cuda.graph(g):
+            s = torch.cuda.current_stream()
+            for i in range(nsteps):
+                inp = sets[i % nsets]
+                run_tree_phase(buf, inp, s)
+                if with_events:
+                    e0, e1 = ev_pool[2 * i], ev_pool[2 * i + 1]
+                    gt.gt_event_record_external(e0, s)
+                sh = buf.shape
+                gt.gt_tree_attn(inp["Q"], inp["K"], inp["V"], buf.mask, inp["prefix_len"],
+                                buf.n_nodes, sh.B, sh.N, sh.Hq, sh.Hkv, sh.d, sh.Lcap, sh.dtype,
+                                scn.scale, buf.O, buf.ws, buf.ws_bytes, buf.err, s)
+                if with_events:
+                    gt.gt_event_record_external(e1, s)
+                    evs.append((e0, e1))
+                gt.gt_verify_greedy(inp["logits"], buf.tokens, buf.parent, buf.n_nodes,
+                                    inp["prefix_len"], sh.B, sh.N, sh.V, sh.k, buf.topk_id,
+                                    buf.topk_val, buf.acc_len, buf.path, buf.out_tok,
+                                    buf.kv_src, buf.kv_dst, buf.err, s)
+                gt.gt_succ_update(inp["table"], sh.V, sh.k, buf.tokens, buf.topk_id,
+                                  buf.n_nodes, sh.B, sh.N, buf.err, s)
+        return g, evs
+
+    # torch creates CUDA events lazily: record each once before capture so it exists
+    ev_pool = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+    for e in ev_pool:
+        e.record(stream)
+    torch.cuda.synchronize()
+    g_warm, _ = capture(max(args.warmup, 1), False)
+    g_timed, evs = capture(args.steps, True)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    g_warm.replay()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = _clock_sampler() if rank == 0 else None
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t0.record(stream)
+    g_timed.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = _clock_summary(clk, torch.cuda.current_device()) if rank == 0 else None
+    ms = t0.elapsed_time(t1)
+    if dist:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    errc = int(buf.err.item())
+    if errc != 0:
+        raise RuntimeError(f"device error {gt.status_string(errc)}")
+    attn_ms = [a.elapsed_time(b) for a, b in evs]
+    attn_avg_ms = sum(attn_ms) / len(attn_ms)
+
+    # ---- end to end through host buffers: H2D of the step's inputs, D2H of its result
+    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+    h_tree = {k: pin(base[k]) for k in ("score_in", "parent_in", "tokens_in", "keep", "R")}
+    if "thresh" in base:
+        h_tree["thresh"] = pin(base["thresh"])
+    h_q = pin(base["Q"])
+    P = scn.prefix_len
+    h_kv = [(pin(base["K"][b, :, P[b]:P[b] + scn.N]), pin(base["V"][b, :, P[b]:P[b] + scn.N]))
+            for b in range(scn.B)]
+    h_logits = pin(base["logits"])
+    outs = ("acc_len", "out_tok", "path", "kv_src", "kv_dst")
+    h_out = {k: torch.empty(getattr(buf, k).shape, dtype=torch.int32).pin_memory() for k in outs}
+    h2d = sum(t.numel() * t.element_size() for t in list(h_tree.values()) + [h_q, h_logits]) + \
+        sum(a.numel() * a.element_size() * 2 for a, _ in h_kv)
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+    inp = sets[0]
+
+    def e2e_step():
+        for k, t in h_tree.items():
+            inp[k].copy_(t, non_blocking=True)
+        inp["Q"].copy_(h_q, non_blocking=True)
+        for b in range(scn.B):
+            inp["K"][b, :, P[b]:P[b] + scn.N].copy_(h_kv[b][0], non_blocking=True)
+            inp["V"][b, :, P[b]:P[b] + scn.N].copy_(h_kv[b][1], non_blocking=True)
+        inp["logits"].copy_(h_logits, non_blocking=True)
+        run_step(buf, inp, scale=scn.scale)
+        for k in outs:
+            h_out[k].copy_(getattr(buf, k), non_blocking=True)
+        torch.cuda.synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    ne = max(5, min(args.steps, 50))
+    if dist:
+        dist.barrier()
+    te = time.perf_counter()
+    for _ in range(ne):
+        e2e_step()
+    e2e_s = time.perf_counter() - te
+    if dist:
+        tt = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_s = float(tt.item())
+
+    if rank != 0:
+        return None
+    peak, peak_kind = _peaks()
+    ab = attn_bytes(scn)
+    achieved = ab / (attn_avg_ms * 1e-3) / 1e9
+    value = world * args.steps / (ms * 1e-3)
+    line = {
+        "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": scn.dtype,
+        "data": "synthetic (seeded generator; see DESIGN.md input recipe)",
+        "config": {"workload": scn.name, "config_id": args.config, "B": scn.B,
+                   "prefix_len": int(max(scn.prefix_len)), "slots": scn.N, "vocab": scn.V,
+                   "heads": f"{scn.Hq}/{scn.Hkv}x{scn.d}",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"inputs rotate over {nsets} device copies of {per_set / 1e6:.1f} MB "
+                         f"(> L2 of {L2_BYTES / 2**20:.0f} MiB)",
+                   "step_bytes": step_bytes(scn),
+                   "step_byte_roofline_frac": step_bytes(scn) / (ms / args.steps * 1e-3) / 1e9
+                   / peak},
+        "roofline": {"bound": "hbm", "kernel": "gt_tree_attn (sched + tcgen05/SIMT + combine)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": ab,
+                     "avg_launch_ms": attn_avg_ms,
+                     "traffic": _traffic_record(f"tree_attn/config{args.config}")},
+        "e2e": {"value": world * ne / e2e_s, "unit": "steps/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * KERNELS_PER_STEP[len(scn.tpar) > 0],
+        "clocks": clocks,
+        "accepted_len_mean": float(buf.acc_len.float().mean().item()),
+    }
+    if not args.no_cpu_baseline:
+        cv, cdone, cdt = time_oracle(scn, 1000, args.cpu_budget)
+        line["cpu_baseline"] = {
+            "value": cv, "unit": "steps/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{cdone} whole steps of the same workload (~{cdt:.0f} s, numpy float64; "
+                      "BLAS may use every core, the tree and top-k loops use one)"}
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=sorted(CONFIGS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--ref-budget", type=float, default=60.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        if world > 1:
+            import torch
+            import torch.distributed as dist
+            torch.cuda.set_device(local_rank)
+            dist.init_process_group("nccl")
+        line = run_gpu(args, rank, world, local_rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

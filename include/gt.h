@@ -1,0 +1,224 @@
+/*
+ * gt.h — C ABI of the GB300 (sm_103a) verify-and-graft step of tree speculative decoding.
+ *
+ * Sources, cited as page title + section:
+ *   [Graft]     "浙江大学、阿里巴巴联手破解AI推理瓶颈" — write-up of the Graft paper.
+ *               §二: calibrated prune at depths 0/1/5; the GPU-resident successor table
+ *               ("adjacency matrix": row = token, its k most likely successors by rank);
+ *               retrieval rooted at the current token and expanded by a stage-adaptive,
+ *               asymmetric template into the freed slots (8/24/40 draft + 52/36/20
+ *               retrieved of 60); flatten + tree position ids + mask + one parallel
+ *               verify; online update of the row of every verified position.
+ *               §四: batched serving keeps a fixed slot count per request and swaps
+ *               low-confidence draft nodes for retrieved ones. §六: accepted and rejected
+ *               positions both update the table.
+ *   [TreeGraft] "TreeGraft 精读：多起草器共嫁接一棵草稿树，让投机解码跨越快与好的单选题".
+ *               §一: accept the agreeing tokens, roll back at the first error.
+ *               §三: cumulative path score s(v) = product of edge scores root..v; global
+ *               prune to the verification budget Bver; tree-attention verification.
+ *               §四 How: non-destructive graft, then one global prune to Bver = 63.
+ *
+ * Conventions shared by every entry point
+ *   - Pointers named in the "device" list are caller-owned CUDA device pointers (or
+ *     managed memory); the library never allocates, frees or keeps them. Host helpers
+ *     at the end of the file take host pointers.
+ *   - Trees are flattened in topological order: node 0 is the root (the current token),
+ *     parent[0] = -1 and 0 <= parent[v] < v for v >= 1. Per-request arrays are
+ *     row-major [B][stride]; entries at or beyond a request's node count are padding.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default).
+ *     The return value reports what the host can see: bad arguments (GT_ERR_ARG), an
+ *     unsupported shape (GT_ERR_SHAPE) or a failed launch (GT_ERR_CUDA). Problems only
+ *     visible in device data (malformed tree, id out of range, non-monotone score, size
+ *     stored on the device that exceeds a buffer) are written as the matching negative
+ *     code into the device word *err with a compare-and-swap from 0, so the first error
+ *     wins; the caller zeroes *err beforehand and reads it after its own synchronisation.
+ *     err may be NULL (no device-side report). Requests with bad data get padded
+ *     outputs (count 0 or -1 entries) and do not corrupt other requests.
+ *   - Calls perform no host synchronisation and allocate nothing, so a sequence of them
+ *     can be captured into a CUDA graph.
+ */
+#ifndef GT_H
+#define GT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *gt_stream_t;
+
+typedef enum {
+  GT_OK = 0,
+  GT_ERR_ARG = -1,          /* null pointer, negative size, unsupported option          */
+  GT_ERR_SHAPE = -2,        /* size outside what the kernels support                    */
+  GT_ERR_CUDA = -3,         /* a CUDA launch or driver call failed                      */
+  GT_ERR_TREE = -4,         /* device: not a rooted topological tree, id out of range   */
+  GT_ERR_NONMONOTONE = -5,  /* device: a node's score exceeds its parent's, or is NaN   */
+  GT_ERR_TIMEOUT = -6,      /* device: a bounded wait gave up                           */
+  GT_ERR_RANGE = -7         /* device: a stored count exceeds its buffer                */
+} gt_status;
+
+typedef enum { GT_F32 = 0, GT_BF16 = 1 } gt_dtype;
+
+/* ---------------------------------------------------------------------------------------
+ * a1. Prune to the verification budget.  [TreeGraft] §三, §四 How; [Graft] §二, §四.
+ *
+ * Keeps, per request b, the root and the best nodes by (score desc, index asc), at most
+ * keep[b] nodes in total and, when thresh != NULL, only non-root nodes with
+ * score >= thresh[b]. Kept nodes are renumbered in ascending old index and their parents
+ * remapped, so the output is again a topological tree.
+ *   device in : score  f32 [B][Nin]  cumulative path scores (root's value is ignored)
+ *               parent i32 [B][Nin], tokens i32 [B][Nin]
+ *               n_in   i32 [B] nodes per request (NULL: every request has Nin)
+ *               keep   i32 [B] node budget incl. the root (>= 1)
+ *               thresh f32 [B] confidence threshold (NULL: none)
+ *   device out: out_parent, out_tokens i32 [B][Nout]; out_score f32 [B][Nout] (nullable);
+ *               out_old_idx i32 [B][Nout] old index of each kept node (nullable);
+ *               n_out i32 [B]. Entries >= n_out[b]: -1 (score 0).
+ * Limits: 1 <= Nin <= 1024, Nout >= 1. Device errors: GT_ERR_TREE (bad parent),
+ * GT_ERR_NONMONOTONE (score[v] > score[parent[v]] for a non-root parent, or NaN),
+ * GT_ERR_RANGE (min(keep, n_in) > Nout, keep < 1, n_in outside [1, Nin]).
+ * Output arrays must not alias the inputs.
+ * ------------------------------------------------------------------------------------- */
+int gt_prune_topB(const float *score, const int32_t *parent, const int32_t *tokens,
+                  const int32_t *n_in, int B, int Nin, const int32_t *keep,
+                  const float *thresh, int Nout, int32_t *out_parent, int32_t *out_tokens,
+                  float *out_score, int32_t *out_old_idx, int32_t *n_out, int32_t *err,
+                  gt_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * a2. Graft retrieved nodes into the freed slots.  [Graft] §二 (second gear), §四.
+ *
+ * In place on the kept trees. For request b with n = n_nodes[b] kept nodes, template
+ * nodes t = 0 .. R'-1, R' = min(R[b], Nmax - n, T), are tried in order: template parent
+ * tpar[t] (-1 = the tree root, else an earlier template node) and successor rank
+ * trank[t]; the node's token is table[token(parent)][trank[t]]. An empty entry (-1)
+ * drops the node and all its template descendants. Survivors are appended at n, n+1, ...
+ * in template order; slots from the new count to Nmax-1 are set to -1.
+ *   device in/out: parent, tokens i32 [B][Nmax]; n_nodes i32 [B] (in: kept, out: total)
+ *   device in    : tpar, trank i32 [T]; R i32 [B]; table i32 [V][k] (entries in [-1, V))
+ * Limits: 0 <= T <= 1024, k >= 1, V >= 1. Device errors: GT_ERR_TREE (template parent
+ * not earlier, rank >= k, a token or table entry outside its range), GT_ERR_RANGE
+ * (n_nodes outside [1, Nmax]).
+ * ------------------------------------------------------------------------------------- */
+int gt_graft_expand(int32_t *parent, int32_t *tokens, int32_t *n_nodes, int B, int Nmax,
+                    const int32_t *tpar, const int32_t *trank, int T, const int32_t *R,
+                    const int32_t *table, int V, int k, int32_t *err, gt_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * a3. Ancestor mask and tree position ids.  [Graft] §二 (third gear).
+ *
+ * depth[v] = number of edges from the root; pos[v] = prefix_len[b] + depth[v];
+ * bit u of mask row v (word u/64, bit u%64) is set iff u is v or an ancestor of v.
+ *   device in : parent i32 [B][N]; n_nodes i32 [B]; prefix_len i32 [B]
+ *   device out: depth, pos i32 [B][N]; mask u64 [B][N][ceil(N/64)]
+ *               Rows >= n_nodes[b]: depth = pos = -1, mask = 0.
+ * Limits: 1 <= N <= 1024. Device errors: GT_ERR_TREE, GT_ERR_RANGE (n outside [1, N]).
+ * ------------------------------------------------------------------------------------- */
+int gt_tree_mask(const int32_t *parent, const int32_t *n_nodes, const int32_t *prefix_len,
+                 int B, int N, int32_t *depth, int32_t *pos, uint64_t *mask, int32_t *err,
+                 gt_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * a4. Tree-masked GQA attention of the tree's queries.  [Graft] §二 (third gear);
+ *     [TreeGraft] §三 (tree-attention verification).
+ *
+ * O[b][i][h] = sum_j softmax_j(scale * Q[b][i][h] . K[b][h/g][j]) V[b][h/g][j], g = Hq/Hkv,
+ * over keys j in [0, P) (the committed prefix, P = prefix_len[b]) and j = P + u for every
+ * tree node u with bit u set in mask[b][i] (the tree's own K/V rows sit at P .. P+n-1).
+ *   device in : Q  [B][N][Hq][d]   (dtype)
+ *               K, V [B][Hkv][Lcap][d] (dtype) — the KV cache with the tree rows appended
+ *               mask u64 [B][N][1] from gt_tree_mask; prefix_len, n_nodes i32 [B]
+ *   device out: O [B][N][Hq][d] (dtype; fp32 accumulation, round to nearest even);
+ *               rows i >= n_nodes[b] are zero.
+ *   workspace : caller-owned device scratch of gt_tree_attn_workspace(...) bytes,
+ *               256-byte aligned; contents need no initialisation and are clobbered.
+ * dtype GT_BF16 runs on the tcgen05 tensor cores (bf16 operands, fp32 accumulators in
+ * tensor memory, K/V tiles staged by TMA); GT_F32 runs on FP32 FMA units.
+ * Limits: d = 128, 1 <= N <= 64, Hq % Hkv == 0, (Hq/Hkv)*N <= 512, Lcap >= 1; Q, K, V, O
+ * 16-byte aligned. Device errors: GT_ERR_RANGE (prefix_len + n_nodes > Lcap,
+ * n_nodes outside [1, N], prefix_len < 0). Keys past a request's length are never read
+ * into the result (cache rows there may hold anything, NaN included).
+ * ------------------------------------------------------------------------------------- */
+size_t gt_tree_attn_workspace(int B, int N, int Hq, int Hkv, int d, int Lcap);
+int gt_tree_attn(const void *Q, const void *K, const void *V, const uint64_t *mask,
+                 const int32_t *prefix_len, const int32_t *n_nodes, int B, int N, int Hq,
+                 int Hkv, int d, int Lcap, int dtype, float scale, void *O,
+                 void *workspace, size_t ws_bytes, int32_t *err, gt_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * a5. Vocab-wide top-k per row (argmax = column 0).  [Graft] §二 (table rows hold the
+ *     target's k most likely next tokens); [TreeGraft] §五 (greedy, temperature 0).
+ *
+ * Order: value descending, +0.0 equal to -0.0, NaN below -inf, ties to the lower index.
+ *   device in : logits f32 [rows][V]
+ *   device out: ids i32 [rows][k]; vals f32 [rows][k] (the logits' own bits)
+ * Limits: 1 <= k <= 16, k <= V, rows >= 0.
+ * ------------------------------------------------------------------------------------- */
+int gt_vocab_topk(const float *logits, int rows, int V, int k, int32_t *ids, float *vals,
+                  gt_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * a5 + a6. Greedy verification with commit indices.  [Graft] §二 (third gear);
+ *     [TreeGraft] §一, §三.
+ *
+ * Runs gt_vocab_topk over all B*N rows, then per request: node v is accepted iff every
+ * edge (p -> c) on its root path has tokens[c] == argmax[p]; v* = the deepest accepted
+ * node (ties: smaller index); L = depth(v*). Outputs path = root .. v*, the committed
+ * tokens (the path's draft tokens, then the bonus argmax[v*]) and the KV moves
+ * kv_src[j] = P + path[j] -> kv_dst[j] = P + j.
+ *   device in : logits f32 [B][N][V]; tokens, parent i32 [B][N]; n_nodes, prefix_len i32 [B]
+ *   device out: topk_id i32 [B][N][k]; topk_val f32 [B][N][k]; acc_len i32 [B];
+ *               path, kv_src, kv_dst i32 [B][N]; out_tok i32 [B][N+1]; entries past the
+ *               accepted length are -1.
+ * Limits: 1 <= N <= 1024, 1 <= k <= 16, k <= V. Device errors: GT_ERR_TREE, GT_ERR_RANGE.
+ * ------------------------------------------------------------------------------------- */
+int gt_verify_greedy(const float *logits, const int32_t *tokens, const int32_t *parent,
+                     const int32_t *n_nodes, const int32_t *prefix_len, int B, int N, int V,
+                     int k, int32_t *topk_id, float *topk_val, int32_t *acc_len,
+                     int32_t *path, int32_t *out_tok, int32_t *kv_src, int32_t *kv_dst,
+                     int32_t *err, gt_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * a7. Online successor-table update.  [Graft] §二 (third gear), §六.
+ *
+ * For every verified node (b, v), v < n_nodes[b], accepted or not: row tokens[b][v] of
+ * the table becomes topk_id[b][v][0..k). When several nodes share a token, the one with
+ * the largest linear index b*N + v wins (the result of applying the writes in order).
+ * Winners own distinct rows, so no atomics are used.
+ *   device in/out: table i32 [V][k]
+ *   device in    : tokens i32 [B][N]; topk_id i32 [B][N][k]; n_nodes i32 [B]
+ * Limits: B*N <= 16384. Device errors: GT_ERR_TREE (token outside [0, V)),
+ * GT_ERR_RANGE (n_nodes outside [0, N]).
+ * ------------------------------------------------------------------------------------- */
+int gt_succ_update(int32_t *table, int V, int k, const int32_t *tokens,
+                   const int32_t *topk_id, const int32_t *n_nodes, int B, int N,
+                   int32_t *err, gt_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Host helpers (host pointers, synchronous, no CUDA calls).
+ *
+ * gt_stage_budget: draft / retrieved split of `slots` for a prune at stage 0, 1 or 5
+ *   ([Graft] §二: 8/52, 24/36, 40/20 of 60; the same proportions for other slot counts
+ *   are not given by the pages, so slots must be 60). stage = -1: no prune, (slots, 0).
+ * gt_default_template: the asymmetric retrieval template of T nodes, k ranks, depth <=
+ *   max_depth (a reading of [Graft] §二: nodes chosen best-first by the integer weight
+ *   prod(rank_i + 2), ties by depth then rank path; every prefix is ancestor-closed).
+ * gt_status_string: a static description of a gt_status value.
+ * ------------------------------------------------------------------------------------- */
+int gt_stage_budget(int stage, int slots, int32_t *draft, int32_t *retrieved);
+int gt_default_template(int T, int k, int max_depth, int32_t *tpar, int32_t *trank);
+const char *gt_status_string(int status);
+
+/* Records `event` (a cudaEvent_t) on `stream` as an externally visible node when the
+ * stream is being captured into a CUDA graph (cudaEventRecordExternal), so a replayed
+ * graph can time the work between two such records. Not part of the step. */
+int gt_event_record_external(void *event, gt_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GT_H */

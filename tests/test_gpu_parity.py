@@ -1,0 +1,214 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle on the same seeded
+inputs. Indices, trees, masks, top-k, paths, commit indices and the table are compared
+bit for bit; attention to the max-abs tolerance of its input precision."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity_util import (TOL, attn_max_err, compare_tree, compare_verify, device_inputs, np_,
+                         oracle_tree, run_gpu_step, shape_of)
+from tree_speculative_decoding_parent_gb300 import gt
+from tree_speculative_decoding_parent_gb300.step import StepBuffers, run_step
+from workload import make_scenario
+
+pytestmark = pytest.mark.gpu
+
+# Reduced vocabularies and prefixes (several KV tiles plus a ragged tail; vocab sizes that
+# do and do not divide by 4), with the trees and budgets of each workload unchanged.
+SMALL = {
+    1: dict(),                                                   # config 1 is small already
+    2: dict(V=5000, P=700),
+    3: dict(V=4099, P=1333, stream_len=50000),
+    4: dict(V=4096, P=(200, 900), B=5, stream_len=50000),
+    5: dict(V=5003, P=611),
+}
+
+
+def _full_check(scn, reqs=None):
+    tree = oracle_tree(scn)
+    logits = scn.logits(tree["parent"], tree["tokens"], tree["n_nodes"])
+    buf, inp = run_gpu_step(scn, logits)
+    assert int(buf.err.item()) == 0
+    compare_tree(buf, tree)
+    res = oracle.step_verify_phase(tree, logits, scn.table, scn.prefix_len, scn.k)
+    compare_verify(buf, res, inp["table"])
+    err = attn_max_err(buf, scn, tree, reqs)
+    assert err <= TOL[scn.dtype], err
+    return buf, tree
+
+
+@pytest.mark.parametrize("cid", [1, 2, 3, 4, 5])
+def test_step_parity_small(cid):
+    _full_check(make_scenario(cid, **SMALL[cid]))
+
+
+def test_step_parity_nan_kv_tail_and_zero_prefix():
+    # cache rows past each request's length hold NaN: they must never reach the result
+    _full_check(make_scenario(2, V=5000, P=300, kv_fill="nan"))
+    _full_check(make_scenario(1, V=3000, P=0, kv_fill="nan"))
+    _full_check(make_scenario(4, V=4096, P=(0, 200), B=3, stream_len=20000, kv_fill="nan"))
+
+
+@pytest.mark.parametrize("cid", [2, 3, 5])
+def test_step_parity_full_size(cid):
+    _full_check(make_scenario(cid))
+
+
+def test_step_parity_full_size_batched():
+    scn = make_scenario(4)
+    _full_check(scn, reqs=[0, 7, 15])
+
+
+def test_repeated_steps_keep_parity():
+    """Three steps in a row on the evolving table (each graft reads the last update)."""
+    scn = make_scenario(3, V=4099, P=500, stream_len=30000)
+    buf = StepBuffers(shape_of(scn))
+    table = scn.table.copy()
+    for _ in range(3):
+        scn.table = table
+        tree = oracle_tree(scn)
+        logits = scn.logits(tree["parent"], tree["tokens"], tree["n_nodes"])
+        inp = device_inputs(scn, logits)
+        run_step(buf, inp, scale=scn.scale)
+        torch.cuda.synchronize()
+        compare_tree(buf, tree)
+        res = oracle.step_verify_phase(tree, logits, table, scn.prefix_len, scn.k)
+        compare_verify(buf, res, inp["table"])
+        table = res["table"]
+
+
+# ------------------------------------------------------------------------ single kernels
+
+
+def _t(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def test_vocab_topk_ties_zeros_nan():
+    rng = np.random.default_rng(0)
+    pool = np.float32([0.0, -0.0, 1.0, -1.0, 2.5, np.inf, -np.inf, np.nan, 1e-30, -1e-30])
+    for V, rows, k in ((37, 50, 8), (1000, 20, 16), (4096, 9, 5), (131, 70, 1), (8, 3, 8)):
+        x = pool[rng.integers(0, len(pool), size=(rows, V))]
+        ids = torch.empty((rows, k), dtype=torch.int32, device="cuda")
+        vals = torch.empty((rows, k), dtype=torch.float32, device="cuda")
+        gt.gt_vocab_topk(_t(x), rows, V, k, ids, vals)
+        torch.cuda.synchronize()
+        for r in range(rows):
+            ri, rv = oracle.vocab_topk(x[r], k)
+            assert np_(ids[r]).tolist() == ri.tolist()
+            assert np.array_equal(np_(vals[r]).view(np.uint32), rv.view(np.uint32))
+
+
+def test_vocab_topk_random_large():
+    rng = np.random.default_rng(1)
+    for V in (151936, 128256, 32000, 99991):
+        x = rng.standard_normal((6, V), dtype=np.float32)
+        x[2, 1000:1010] = 9.0  # ties at the top
+        ids = torch.empty((6, 8), dtype=torch.int32, device="cuda")
+        vals = torch.empty((6, 8), dtype=torch.float32, device="cuda")
+        gt.gt_vocab_topk(_t(x), 6, V, 8, ids, vals)
+        torch.cuda.synchronize()
+        for r in range(6):
+            assert np_(ids[r]).tolist() == oracle.vocab_topk(x[r], 8)[0].tolist()
+
+
+def test_succ_update_duplicates():
+    rng = np.random.default_rng(2)
+    V, k, B, N = 50, 8, 7, 60
+    table = rng.integers(0, V, size=(V, k)).astype(np.int32)
+    tokens = rng.integers(0, 12, size=(B, N)).astype(np.int32)   # many shared rows
+    topk = rng.integers(0, V, size=(B, N, k)).astype(np.int32)
+    n = rng.integers(0, N + 1, size=B).astype(np.int32)
+    dt = _t(table)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gt.gt_succ_update(dt, V, k, _t(tokens), _t(topk), _t(n), B, N, err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert np.array_equal(np_(dt), oracle.succ_update(table, tokens, topk, n))
+
+
+def test_graft_with_empty_entries():
+    rng = np.random.default_rng(3)
+    from workload import default_template
+    V, k, B, Nmax = 40, 8, 6, 60
+    tpar, trank = default_template(52, k)
+    for trial in range(5):
+        table = rng.integers(-1, V, size=(V, k)).astype(np.int32)
+        table[rng.random((V, k)) < 0.3] = -1
+        nk = rng.integers(1, 20, size=B).astype(np.int32)
+        parent = np.full((B, Nmax), -1, np.int32)
+        tokens = np.full((B, Nmax), -1, np.int32)
+        for b in range(B):
+            parent[b, 1:nk[b]] = [rng.integers(0, v) for v in range(1, nk[b])]
+            tokens[b, :nk[b]] = rng.integers(0, V, size=nk[b])
+        R = rng.integers(0, 60, size=B).astype(np.int32)
+        dp, dtk, dn = _t(parent), _t(tokens), _t(nk)
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        gt.gt_graft_expand(dp, dtk, dn, B, Nmax, _t(tpar), _t(trank), 52, _t(R), _t(table), V, k,
+                           err)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        for b in range(B):
+            p, t, n = oracle.graft_expand(parent[b], tokens[b], int(nk[b]), tpar, trank, int(R[b]),
+                                          table, Nmax)
+            assert np_(dn)[b] == n
+            assert np_(dp)[b].tolist() == p and np_(dtk)[b].tolist() == t
+
+
+def test_prune_ties_and_threshold():
+    rng = np.random.default_rng(4)
+    B, Nin, Nout = 9, 300, 64
+    parent = np.full((B, Nin), -1, np.int32)
+    score = np.zeros((B, Nin), np.float32)
+    for b in range(B):
+        parent[b, 1:] = [rng.integers(max(0, v - 20), v) for v in range(1, Nin)]
+        s = [1.0]
+        for v in range(1, Nin):
+            s.append(s[parent[b, v]] * rng.choice([0.25, 0.5, 0.75, 1.0]))
+        score[b] = s
+    tokens = rng.integers(0, 1000, size=(B, Nin)).astype(np.int32)
+    keep = rng.integers(1, Nout + 1, size=B).astype(np.int32)
+    thresh = np.float32(rng.choice([0.0, 0.01, 0.1, 0.5], size=B))
+    outs = [torch.empty((B, Nout), dtype=dt, device="cuda")
+            for dt in (torch.int32, torch.int32, torch.float32, torch.int32)]
+    n_out = torch.empty(B, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gt.gt_prune_topB(_t(score), _t(parent), _t(tokens), None, B, Nin, _t(keep), _t(thresh), Nout,
+                     *outs, n_out, err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    for b in range(B):
+        p, t, s, o = oracle.prune_topB(score[b], parent[b], tokens[b], Nin, int(keep[b]),
+                                       float(thresh[b]))
+        m = len(p)
+        assert np_(n_out)[b] == m
+        assert np_(outs[0])[b, :m].tolist() == p and np_(outs[3])[b, :m].tolist() == o
+        assert np_(outs[1])[b, :m].tolist() == t
+        assert (np_(outs[0])[b, m:] == -1).all()
+
+
+def test_device_errors_are_reported():
+    scn = make_scenario(1, V=3000, P=64)
+    tree = oracle_tree(scn)
+    logits = scn.logits(tree["parent"], tree["tokens"], tree["n_nodes"])
+    # a node whose score exceeds its parent's
+    bad = make_scenario(1, V=3000, P=64)
+    bad.score_in[0, 200] = 2.0
+    buf, _ = run_gpu_step(bad, logits)
+    assert buf.err.item() == gt.GT_ERR_NONMONOTONE
+    # a parent index that is not smaller than the child's
+    bad = make_scenario(1, V=3000, P=64)
+    bad.parent_in[0, 17] = 300
+    buf, _ = run_gpu_step(bad, logits)
+    assert buf.err.item() == gt.GT_ERR_TREE
+    # a prefix that does not fit in the cache
+    buf = StepBuffers(shape_of(scn))
+    inp = device_inputs(scn, logits)
+    inp["prefix_len"] = torch.tensor([scn.Lcap], dtype=torch.int32, device="cuda")
+    run_step(buf, inp, scale=scn.scale)
+    torch.cuda.synchronize()
+    assert buf.err.item() == gt.GT_ERR_RANGE
+    # host-visible errors raise without launching
+    with pytest.raises(gt.GTError):
+        gt.gt_vocab_topk(inp["logits"], 1, scn.V, 17, buf.topk_id, buf.topk_val)

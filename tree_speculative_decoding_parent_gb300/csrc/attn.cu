@@ -1,0 +1,399 @@
+// a4 tree-masked GQA attention: device-side split-KV scheduler, FP32 SIMT kernel,
+// LSE combine, and the C-ABI entry point (bf16 goes to the tcgen05 kernel).
+//
+// Sources: "浙江大学、阿里巴巴联手破解AI推理瓶颈" §二 third gear (the flattened tree is verified
+// in one parallel forward with tree position ids and an ancestor mask);
+// "TreeGraft 精读：多起草器共嫁接一棵草稿树，让投机解码跨越快与好的单选题" §三 (tree-attention
+// verification) and §七 (one target forward verifies the whole tree).
+//
+// Query rows of a segment (request b, KV head h) are ordered r = i*g + j for tree node i
+// and query head h*g + j, so the g heads that share a KV head are adjacent. Key j of the
+// segment is visible to node i when j < P (committed prefix) or when j = P + u and bit u
+// of mask[b][i] is set (u an ancestor of i, or i itself).
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "attn_common.cuh"
+#include "attn_tc.cuh"
+#include "gt_internal.cuh"
+#include "launch.cuh"
+
+namespace gt {
+
+// ------------------------------------------------------------------------------------
+// Scheduler: one CTA. tiles_s = ceil((P_b + n_b) / TK); tau = ceil(sum tiles / G);
+// segment s gets ceil(tiles_s / tau) pieces of near-equal tile counts. The piece count
+// is at most G + S, the size the workspace is laid out for.
+// ------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024)
+attn_sched_kernel(const int32_t *__restrict__ prefix_len, const int32_t *__restrict__ n_nodes,
+                  int B, int Hkv, int N, int Lcap, int TK, int G, AttnWs ws, int32_t *err) {
+  extern __shared__ int s_tiles[];  // [S]
+  __shared__ long long s_red[32];
+  __shared__ int s_wscan[32];
+  const int S = B * Hkv, tid = threadIdx.x, nt = blockDim.x;
+  const int lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
+  for (int s = tid; s < S; s += nt) {
+    const int b = s / Hkv;
+    const int n = n_nodes[b], P = prefix_len[b];
+    const bool ok = n >= 1 && n <= N && P >= 0 && (long long)P + n <= (long long)Lcap;
+    if (!ok && (s % Hkv) == 0) set_err(err, GT_ERR_RANGE);
+    s_tiles[s] = ok ? ceil_div(P + n, TK) : 0;
+  }
+  __syncthreads();
+  long long part = 0;
+  for (int s = tid; s < S; s += nt) part += s_tiles[s];
+#pragma unroll
+  for (int o = 16; o; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+  if (lane == 0) s_red[warp] = part;
+  __syncthreads();
+  long long T = 0;
+  for (int w = 0; w < nw; ++w) T += s_red[w];
+  const int tau = (int)max(1ll, (T + G - 1) / G);
+  const int chunk = (S + nt - 1) / nt;
+  const int c0 = min(S, tid * chunk), c1 = min(S, c0 + chunk);
+  int local = 0;
+  for (int s = c0; s < c1; ++s) local += ceil_div(s_tiles[s], tau);
+  // block exclusive scan of `local`
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_wscan[warp] = incl;
+  __syncthreads();
+  int woff = 0, total = 0;
+  for (int w = 0; w < nw; ++w) {
+    woff += (w < warp) ? s_wscan[w] : 0;
+    total += s_wscan[w];
+  }
+  int off = woff + incl - local;
+  for (int s = c0; s < c1; ++s) {
+    const int t = s_tiles[s];
+    const int cnt = ceil_div(t, tau);
+    ws.seg[s] = make_int2(off, cnt);
+    for (int j = 0; j < cnt; ++j)
+      ws.pieces[off + j] = make_int4(s, (int)((long long)t * j / cnt),
+                                     (int)((long long)t * (j + 1) / cnt), 0);
+    off += cnt;
+  }
+  if (tid == 0) ws.hdr[0] = total;
+}
+
+// ------------------------------------------------------------------------------------
+// FP32 SIMT kernel: CTA = (piece, group of 64 query rows); tiles of 64 keys in shared
+// memory; S = Q K^T by 4x4 register blocks, masked online softmax (expf), O by 4x8 blocks.
+// ------------------------------------------------------------------------------------
+constexpr int SIMT_ROWS = 64, SIMT_KEYS = 64, SIMT_LD = 68, SIMT_SLD = 65;
+constexpr size_t SIMT_SMEM =
+    sizeof(float) * (2 * (size_t)ATTN_D * SIMT_LD + (size_t)SIMT_KEYS * ATTN_D +
+                     (size_t)SIMT_ROWS * SIMT_SLD + 3 * SIMT_ROWS);
+
+template <typename T> __device__ __forceinline__ float to_f32(T x);
+template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
+  return __bfloat162float(x);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+attn_simt_kernel(const T *__restrict__ Q, const T *__restrict__ K, const T *__restrict__ V,
+                 const uint64_t *__restrict__ mask, const int32_t *__restrict__ prefix_len,
+                 const int32_t *__restrict__ n_nodes, int N, int Hq, int Hkv, int Lcap,
+                 float scale, AttnWs ws) {
+  extern __shared__ float sm[];
+  float *Qs = sm;                              // [d][SIMT_LD] (rows)
+  float *Ks = Qs + ATTN_D * SIMT_LD;           // [d][SIMT_LD] (keys)
+  float *Vs = Ks + ATTN_D * SIMT_LD;           // [keys][d]
+  float *Ss = Vs + SIMT_KEYS * ATTN_D;         // [rows][SIMT_SLD]
+  float *s_alpha = Ss + SIMT_ROWS * SIMT_SLD;  // [rows]
+  float *s_m = s_alpha + SIMT_ROWS, *s_l = s_m + SIMT_ROWS;
+  __shared__ uint64_t s_mask[SIMT_ROWS];
+
+  const int p = blockIdx.x;
+  if (p >= ws.hdr[0]) return;
+  const int4 pc = ws.pieces[p];
+  const int seg = pc.x, b = seg / Hkv, h = seg - b * Hkv;
+  const int g = Hq / Hkv;
+  const int n = n_nodes[b], P = prefix_len[b], keys = P + n;
+  const int r0 = blockIdx.y * SIMT_ROWS;
+  if (r0 >= g * n) return;
+  const int tid = threadIdx.x;
+
+  // Q rows (transposed into Qs), masks
+  for (int e = tid; e < SIMT_ROWS * ATTN_D; e += 256) {
+    const int rl = e / ATTN_D, dd = e - rl * ATTN_D, r = r0 + rl;
+    float q = 0.f;
+    if (r < g * n) {
+      const int i = r / g, hq = h * g + (r - i * g);
+      q = to_f32<T>(Q[(((size_t)b * N + i) * Hq + hq) * ATTN_D + dd]);
+    }
+    Qs[dd * SIMT_LD + rl] = q;
+  }
+  if (tid < SIMT_ROWS) {
+    const int r = r0 + tid;
+    s_mask[tid] = r < g * n ? mask[(size_t)b * N + r / g] : 0ull;
+  }
+
+  const int ty = tid >> 4, tx = tid & 15;   // S / PV blocking
+  const int srow = tid >> 2, spart = tid & 3;  // softmax: 4 threads per row
+  float m_run = -INFINITY, l_run = 0.f;
+  float acc[4][8];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int c = 0; c < 8; ++c) acc[a][c] = 0.f;
+  const size_t kv0 = ((size_t)b * Hkv + h) * Lcap;
+
+  for (int tile = pc.y; tile < pc.z; ++tile) {
+    const int kb = tile * SIMT_KEYS;
+    __syncthreads();
+    for (int e = tid; e < SIMT_KEYS * ATTN_D; e += 256) {
+      const int c = e / ATTN_D, dd = e - c * ATTN_D, j = kb + c;
+      float kx = 0.f, vx = 0.f;
+      if (j < keys) {
+        kx = to_f32<T>(K[(kv0 + j) * ATTN_D + dd]);
+        vx = to_f32<T>(V[(kv0 + j) * ATTN_D + dd]);
+      }
+      Ks[dd * SIMT_LD + c] = kx;
+      Vs[c * ATTN_D + dd] = vx;
+    }
+    __syncthreads();
+    float s[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) s[a][c] = 0.f;
+#pragma unroll 4
+    for (int dd = 0; dd < ATTN_D; ++dd) {
+      const float4 qv = *reinterpret_cast<const float4 *>(Qs + dd * SIMT_LD + ty * 4);
+      const float4 kv = *reinterpret_cast<const float4 *>(Ks + dd * SIMT_LD + tx * 4);
+      const float qa[4] = {qv.x, qv.y, qv.z, qv.w}, ka[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) s[a][c] = fmaf(qa[a], ka[c], s[a][c]);
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const int rl = ty * 4 + a;
+      const uint64_t mrow = s_mask[rl];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int j = kb + tx * 4 + c;
+        bool vis = j < P;
+        if (!vis && j < keys) vis = (mrow >> (j - P)) & 1ull;
+        Ss[rl * SIMT_SLD + tx * 4 + c] = vis ? s[a][c] * scale : -INFINITY;
+      }
+    }
+    __syncthreads();
+    {  // online softmax of row srow over this tile
+      float mx = -INFINITY;
+      float* srow_p = Ss + srow * SIMT_SLD + spart * 16;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) mx = fmaxf(mx, srow_p[c]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float m_new = fmaxf(m_run, mx);
+      const float alpha = (m_new == -INFINITY) ? 1.f : expf(m_run - m_new);
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const float pv = (m_new == -INFINITY) ? 0.f : expf(srow_p[c] - m_new);
+        srow_p[c] = pv;
+        sum += pv;
+      }
+      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+      l_run = l_run * alpha + sum;
+      m_run = m_new;
+      if (spart == 0) s_alpha[srow] = alpha;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const float al = s_alpha[ty * 4 + a];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) acc[a][c] *= al;
+    }
+    for (int c = 0; c < SIMT_KEYS; ++c) {
+      const float4 v0 = *reinterpret_cast<const float4 *>(Vs + c * ATTN_D + tx * 8);
+      const float4 v1 = *reinterpret_cast<const float4 *>(Vs + c * ATTN_D + tx * 8 + 4);
+      const float va[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        const float pv = Ss[(ty * 4 + a) * SIMT_SLD + c];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[a][q] = fmaf(pv, va[q], acc[a][q]);
+      }
+    }
+  }
+  if (spart == 0) {
+    s_m[srow] = m_run;
+    s_l[srow] = l_run;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int rl = ty * 4 + a, r = r0 + rl;
+    if (r >= g * n) continue;
+    const float l = s_l[rl];
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    float *dst = ws.opart + ((size_t)p * ws.rows_pad + r) * ATTN_D + tx * 8;
+    *reinterpret_cast<float4 *>(dst) =
+        make_float4(acc[a][0] * inv, acc[a][1] * inv, acc[a][2] * inv, acc[a][3] * inv);
+    *reinterpret_cast<float4 *>(dst + 4) =
+        make_float4(acc[a][4] * inv, acc[a][5] * inv, acc[a][6] * inv, acc[a][7] * inv);
+    if (tx == 0) ws.lse[(size_t)p * ws.rows_pad + r] = l > 0.f ? s_m[rl] + logf(l) : -INFINITY;
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// Combine: one warp per (b, i, query head); O = sum_p e^(lse_p - max) O_p / sum_p e^(...).
+// ------------------------------------------------------------------------------------
+template <typename T> __device__ __forceinline__ void store4(T *dst, float4 v);
+template <> __device__ __forceinline__ void store4<float>(float *dst, float4 v) {
+  *reinterpret_cast<float4 *>(dst) = v;
+}
+template <> __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16 *dst, float4 v) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), c = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t *>(&a);
+  u.y = *reinterpret_cast<uint32_t *>(&c);
+  *reinterpret_cast<uint2 *>(dst) = u;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+attn_combine_kernel(const int32_t *__restrict__ n_nodes, int B, int N, int Hq, int Hkv,
+                    AttnWs ws, T *__restrict__ O) {
+  const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (w >= B * N * Hq) return;
+  const int hq = w % Hq, i = (w / Hq) % N, b = w / (Hq * N);
+  const int g = Hq / Hkv, h = hq / g, r = i * g + (hq - h * g);
+  T *dst = O + (size_t)w * ATTN_D + lane * 4;
+  const int n = n_nodes[b];
+  const int2 sg = (i < n) ? ws.seg[b * Hkv + h] : make_int2(0, 0);
+  float mx = -INFINITY;
+  for (int j = 0; j < sg.y; ++j) mx = fmaxf(mx, ws.lse[(size_t)(sg.x + j) * ws.rows_pad + r]);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (mx != -INFINITY) {
+    float wsum = 0.f;
+    for (int j = 0; j < sg.y; ++j) {
+      const size_t pr = (size_t)(sg.x + j) * ws.rows_pad + r;
+      const float wt = expf(ws.lse[pr] - mx);
+      const float4 o = *reinterpret_cast<const float4 *>(ws.opart + pr * ATTN_D + lane * 4);
+      acc.x = fmaf(wt, o.x, acc.x);
+      acc.y = fmaf(wt, o.y, acc.y);
+      acc.z = fmaf(wt, o.z, acc.z);
+      acc.w = fmaf(wt, o.w, acc.w);
+      wsum += wt;
+    }
+    const float inv = 1.f / wsum;
+    acc = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  }
+  store4<T>(dst, acc);
+}
+
+// SM count of the current device, cached per device so that no device query runs while a
+// stream is being captured.
+static int device_sms() {
+  static int cache[64] = {0};
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 1024;  // conservative upper bound for the workspace size
+  }
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      sms <= 0) {
+    (void)cudaGetLastError();
+    return 1024;
+  }
+  if (dev >= 0 && dev < 64) cache[dev] = sms;
+  return sms;
+}
+
+static bool attn_args_ok(int B, int N, int Hq, int Hkv, int d, int Lcap) {
+  return B >= 0 && N >= 1 && Hq >= 1 && Hkv >= 1 && d >= 1 && Lcap >= 1;
+}
+static bool attn_shape_ok(int N, int Hq, int Hkv, int d) {
+  return d == ATTN_D && N <= ATTN_MAX_N && Hq % Hkv == 0 && (Hq / Hkv) * N <= 512;
+}
+
+}  // namespace gt
+
+using namespace gt;
+
+GT_API size_t gt_tree_attn_workspace(int B, int N, int Hq, int Hkv, int d, int Lcap) {
+  if (!attn_args_ok(B, N, Hq, Hkv, d, Lcap) || !attn_shape_ok(N, Hq, Hkv, d)) return 0;
+  const int S = B * Hkv;
+  const int rows_pad = ceil_div((Hq / Hkv) * N, ATTN_ROWS_PAD) * ATTN_ROWS_PAD;
+  return attn_ws_layout(nullptr, S, device_sms() + S, rows_pad, nullptr);
+}
+
+GT_API int gt_tree_attn(const void *Q, const void *K, const void *V, const uint64_t *mask,
+                        const int32_t *prefix_len, const int32_t *n_nodes, int B, int N, int Hq,
+                        int Hkv, int d, int Lcap, int dtype, float scale, void *O,
+                        void *workspace, size_t ws_bytes, int32_t *err, gt_stream_t stream) {
+  if (!attn_args_ok(B, N, Hq, Hkv, d, Lcap)) return GT_ERR_ARG;
+  if (dtype != GT_F32 && dtype != GT_BF16) return GT_ERR_ARG;
+  if (!attn_shape_ok(N, Hq, Hkv, d)) return GT_ERR_SHAPE;
+  if (B == 0) return GT_OK;
+  if (!Q || !K || !V || !mask || !prefix_len || !n_nodes || !O || !workspace) return GT_ERR_ARG;
+  if (((uintptr_t)Q | (uintptr_t)K | (uintptr_t)V | (uintptr_t)O) & 15) return GT_ERR_ARG;
+  if ((uintptr_t)workspace & 255) return GT_ERR_ARG;
+  const int S = B * Hkv;
+  if (S > 8192) return GT_ERR_SHAPE;
+  const int g = Hq / Hkv;
+  const int rows_pad = ceil_div(g * N, ATTN_ROWS_PAD) * ATTN_ROWS_PAD;
+  const int G = device_sms();
+  AttnWs ws;
+  const size_t need = attn_ws_layout(workspace, S, G + S, rows_pad, &ws);
+  if (ws_bytes < need) return GT_ERR_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+
+  const bool tc = (dtype == GT_BF16) && attn_tc_supported(g, N);
+  const int TK = tc ? ATTN_TC_KEYS : SIMT_KEYS;
+  int rc = launch(attn_sched_kernel, dim3(1), dim3(1024), sizeof(int) * (size_t)S, s, prefix_len,
+                  n_nodes, B, Hkv, N, Lcap, TK, G, ws, err);
+  if (rc != GT_OK) return rc;
+  if (tc) {
+    rc = attn_tc_launch(Q, K, V, mask, prefix_len, n_nodes, B, N, Hq, Hkv, Lcap, scale, ws, err,
+                        s);
+  } else if (dtype == GT_F32) {
+    static bool attr_f32 = false;
+    if (!attr_f32) {
+      if (cudaFuncSetAttribute(attn_simt_kernel<float>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)SIMT_SMEM) != cudaSuccess)
+        return launch_status(cudaErrorInvalidValue);
+      attr_f32 = true;
+    }
+    rc = launch(attn_simt_kernel<float>, dim3(ws.maxp, ceil_div(g * N, SIMT_ROWS)), dim3(256),
+                SIMT_SMEM, s, (const float *)Q, (const float *)K, (const float *)V, mask,
+                prefix_len, n_nodes, N, Hq, Hkv, Lcap, scale, ws);
+  } else {
+    static bool attr_bf16 = false;
+    if (!attr_bf16) {
+      if (cudaFuncSetAttribute(attn_simt_kernel<__nv_bfloat16>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)SIMT_SMEM) != cudaSuccess)
+        return launch_status(cudaErrorInvalidValue);
+      attr_bf16 = true;
+    }
+    rc = launch(attn_simt_kernel<__nv_bfloat16>, dim3(ws.maxp, ceil_div(g * N, SIMT_ROWS)),
+                dim3(256), SIMT_SMEM, s, (const __nv_bfloat16 *)Q, (const __nv_bfloat16 *)K,
+                (const __nv_bfloat16 *)V, mask, prefix_len, n_nodes, N, Hq, Hkv, Lcap, scale,
+                ws);
+  }
+  if (rc != GT_OK) return rc;
+  const int warps = B * N * Hq;
+  const dim3 cgrid(ceil_div(warps * 32, 256));
+  if (dtype == GT_F32)
+    return launch(attn_combine_kernel<float>, cgrid, dim3(256), 0, s, n_nodes, B, N, Hq, Hkv, ws,
+                  (float *)O);
+  return launch(attn_combine_kernel<__nv_bfloat16>, cgrid, dim3(256), 0, s, n_nodes, B, N, Hq,
+                Hkv, ws, (__nv_bfloat16 *)O);
+}

@@ -1,0 +1,23 @@
+// Interface of the tcgen05 (5th-generation tensor core) tree-attention kernel for bf16.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "attn_common.cuh"
+
+namespace gt {
+
+constexpr int ATTN_TC_KEYS = 128;  // keys per K/V tile
+
+// True when the tcgen05 kernel handles g query heads per KV head and N tree nodes.
+bool attn_tc_supported(int g, int N);
+
+// Runs the split-KV pieces listed in `ws` (already scheduled with tiles of ATTN_TC_KEYS)
+// and writes the partial O / LSE rows of every piece.
+int attn_tc_launch(const void *Q, const void *K, const void *V, const uint64_t *mask,
+                   const int32_t *prefix_len, const int32_t *n_nodes, int B, int N, int Hq,
+                   int Hkv, int Lcap, float scale, const AttnWs &ws, int32_t *err,
+                   cudaStream_t s);
+
+}  // namespace gt

@@ -1,0 +1,58 @@
+// Internal helpers shared by the sm_103a kernels of libgt.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gt.h"
+
+#define GT_API extern "C" __attribute__((visibility("default")))
+
+namespace gt {
+
+// First device-side error wins; later ones are dropped.
+__device__ __forceinline__ void set_err(int32_t *err, int code) {
+  if (err != nullptr) atomicCAS(reinterpret_cast<int *>(err), 0, code);
+}
+
+__host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+static inline int launch_status(cudaError_t e) {
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();  // clear a non-sticky launch error
+    return GT_ERR_CUDA;
+  }
+  return GT_OK;
+}
+
+// Exclusive prefix count of `flag` over the threads of a block (flags by thread index).
+// `warp_tot` is shared scratch of 32 ints. Returns the prefix; *total receives the sum.
+__device__ __forceinline__ int block_excl_count(bool flag, int *warp_tot, int *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  unsigned bal = __ballot_sync(0xffffffffu, flag);
+  int in_warp = __popc(bal & ((1u << lane) - 1u));
+  if (lane == 0) warp_tot[warp] = __popc(bal);
+  __syncthreads();
+  int off = 0, tot = 0;
+  for (int w = 0; w < nwarps; ++w) {
+    int c = warp_tot[w];
+    off += (w < warp) ? c : 0;
+    tot += c;
+  }
+  __syncthreads();
+  *total = tot;
+  return off + in_warp;
+}
+
+// Order-preserving 32-bit key of a float for "larger is better" comparisons:
+// +0.0 and -0.0 map to the same key, every NaN maps to 1 (below -inf), 0 is unused
+// by any float and marks an empty slot.
+__device__ __forceinline__ uint32_t order_key(float f) {
+  uint32_t b = __float_as_uint(f);
+  if ((b & 0x7fffffffu) > 0x7f800000u) return 1u;
+  if (b == 0x80000000u) b = 0u;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+}  // namespace gt

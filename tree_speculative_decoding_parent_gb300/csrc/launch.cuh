@@ -1,0 +1,42 @@
+// Kernel launch helper: cudaLaunchKernelEx with optional cluster shape, so every launch
+// returns its own error code and can carry launch attributes.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "gt_internal.cuh"
+
+namespace gt {
+
+template <typename... KArgs, typename... Args>
+static int launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                  Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = nullptr;
+  cfg.numAttrs = 0;
+  return launch_status(cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...));
+}
+
+template <typename... KArgs, typename... Args>
+static int launch_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, dim3 cluster,
+                          size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster.x;
+  attr[0].val.clusterDim.y = cluster.y;
+  attr[0].val.clusterDim.z = cluster.z;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return launch_status(cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...));
+}
+
+}  // namespace gt
