@@ -212,6 +212,11 @@ int gt_stage_budget(int stage, int slots, int32_t *draft, int32_t *retrieved);
 int gt_default_template(int T, int k, int max_depth, int32_t *tpar, int32_t *trank);
 const char *gt_status_string(int status);
 
+/* Host-side detail of the most recent GT_ERR_CUDA (or GT_ERR_ARG from a CUDA query) returned
+ * on the calling thread: the failing CUDA call and its error string. Empty if none. The
+ * pointer stays valid until the next libgt call on this thread. */
+const char *gt_last_error(void);
+
 /* Records `event` (a cudaEvent_t) on `stream` as an externally visible node when the
  * stream is being captured into a CUDA graph (cudaEventRecordExternal), so a replayed
  * graph can time the work between two such records. Not part of the step. */

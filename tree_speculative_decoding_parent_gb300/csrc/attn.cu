@@ -356,8 +356,11 @@ GT_API int gt_tree_attn(const void *Q, const void *K, const void *V, const uint6
 
   const bool tc = (dtype == GT_BF16) && attn_tc_supported(g, N);
   const int TK = tc ? ATTN_TC_KEYS : SIMT_KEYS;
+  // the tcgen05 kernel runs one CTA per SM and one CTA per 256 query rows of a piece:
+  // aim for one wave of CTAs
+  const int Gs = tc ? max(1, G / ceil_div(g * N, 256)) : G;
   int rc = launch(attn_sched_kernel, dim3(1), dim3(1024), sizeof(int) * (size_t)S, s, prefix_len,
-                  n_nodes, B, Hkv, N, Lcap, TK, G, ws, err);
+                  n_nodes, B, Hkv, N, Lcap, TK, Gs, ws, err);
   if (rc != GT_OK) return rc;
   if (tc) {
     rc = attn_tc_launch(Q, K, V, mask, prefix_len, n_nodes, B, N, Hq, Hkv, Lcap, scale, ws, err,
@@ -365,10 +368,9 @@ GT_API int gt_tree_attn(const void *Q, const void *K, const void *V, const uint6
   } else if (dtype == GT_F32) {
     static bool attr_f32 = false;
     if (!attr_f32) {
-      if (cudaFuncSetAttribute(attn_simt_kernel<float>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)SIMT_SMEM) != cudaSuccess)
-        return launch_status(cudaErrorInvalidValue);
+      const cudaError_t e = cudaFuncSetAttribute(
+          attn_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SIMT_SMEM);
+      if (e != cudaSuccess) return launch_status(e, "cudaFuncSetAttribute(attn_simt_kernel)");
       attr_f32 = true;
     }
     rc = launch(attn_simt_kernel<float>, dim3(ws.maxp, ceil_div(g * N, SIMT_ROWS)), dim3(256),
@@ -377,10 +379,10 @@ GT_API int gt_tree_attn(const void *Q, const void *K, const void *V, const uint6
   } else {
     static bool attr_bf16 = false;
     if (!attr_bf16) {
-      if (cudaFuncSetAttribute(attn_simt_kernel<__nv_bfloat16>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)SIMT_SMEM) != cudaSuccess)
-        return launch_status(cudaErrorInvalidValue);
+      const cudaError_t e =
+          cudaFuncSetAttribute(attn_simt_kernel<__nv_bfloat16>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SIMT_SMEM);
+      if (e != cudaSuccess) return launch_status(e, "cudaFuncSetAttribute(attn_simt_kernel)");
       attr_bf16 = true;
     }
     rc = launch(attn_simt_kernel<__nv_bfloat16>, dim3(ws.maxp, ceil_div(g * N, SIMT_ROWS)),

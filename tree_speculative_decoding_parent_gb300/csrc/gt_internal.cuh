@@ -17,8 +17,12 @@ __device__ __forceinline__ void set_err(int32_t *err, int code) {
 
 __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-static inline int launch_status(cudaError_t e) {
+// Records a host-side failure detail for gt_last_error() (thread-local).
+void note_error(const char *what, cudaError_t e);
+
+static inline int launch_status(cudaError_t e, const char *what = "kernel launch") {
   if (e != cudaSuccess) {
+    note_error(what, e);
     (void)cudaGetLastError();  // clear a non-sticky launch error
     return GT_ERR_CUDA;
   }

@@ -6,14 +6,16 @@
 // higher-ranked successors get more children and go deeper).
 #include <cuda_runtime.h>
 
+#include <stdio.h>
+
 #include <queue>
 #include <map>
 #include <tuple>
 #include <vector>
 
 #include "gt.h"
+#include "gt_internal.cuh"
 
-#define GT_API extern "C" __attribute__((visibility("default")))
 
 GT_API int gt_stage_budget(int stage, int slots, int32_t *draft, int32_t *retrieved) {
   if (!draft || !retrieved || slots < 1) return GT_ERR_ARG;
@@ -90,3 +92,13 @@ GT_API int gt_event_record_external(void *event, gt_stream_t stream) {
              ? GT_OK
              : GT_ERR_CUDA;
 }
+
+namespace gt {
+static thread_local char last_error[256];
+void note_error(const char *what, cudaError_t e) {
+  snprintf(last_error, sizeof(last_error), "%s: %s", what,
+           e == cudaSuccess ? "failed" : cudaGetErrorString(e));
+}
+}  // namespace gt
+
+GT_API const char *gt_last_error(void) { return gt::last_error; }

@@ -18,7 +18,7 @@ static int launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cu
   cfg.stream = s;
   cfg.attrs = nullptr;
   cfg.numAttrs = 0;
-  return launch_status(cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...));
+  return launch_status(cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...), "cudaLaunchKernelEx");
 }
 
 template <typename... KArgs, typename... Args>
@@ -36,7 +36,7 @@ static int launch_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, dim3 cl
   attr[0].val.clusterDim.z = cluster.z;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return launch_status(cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...));
+  return launch_status(cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...), "cudaLaunchKernelEx");
 }
 
 }  // namespace gt

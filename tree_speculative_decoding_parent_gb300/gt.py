@@ -33,6 +33,7 @@ _SIGS = {
     "gt_stage_budget": (_i, [_i, _i, _vp, _vp]),
     "gt_default_template": (_i, [_i, _i, _i, _vp, _vp]),
     "gt_status_string": (ctypes.c_char_p, [_i]),
+    "gt_last_error": (ctypes.c_char_p, []),
     "gt_event_record_external": (_i, [_vp, _vp]),
 }
 
@@ -41,7 +42,9 @@ _lib = None
 
 class GTError(RuntimeError):
     def __init__(self, name: str, status: int):
-        super().__init__(f"{name}: {status_string(status)} ({status})")
+        detail = last_error() if status == GT_ERR_CUDA else ""
+        super().__init__(f"{name}: {status_string(status)} ({status})"
+                         + (f" [{detail}]" if detail else ""))
         self.status = status
 
 
@@ -67,6 +70,10 @@ def exported_symbols():
 
 def status_string(status: int) -> str:
     return load().gt_status_string(int(status)).decode()
+
+
+def last_error() -> str:
+    return (load().gt_last_error() or b"").decode()
 
 
 def _p(x):
