@@ -16,7 +16,6 @@ import hashlib
 import json
 import os
 import statistics
-import subprocess
 import sys
 import time
 
@@ -62,44 +61,66 @@ def step_bytes(scn) -> int:
     return attn_bytes(scn) + logits + tree + table + verify
 
 
-def _clock_sampler():
-    cmd = ["nvidia-smi", "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,"
-           "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-           "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-           "clocks_event_reasons.sw_power_cap", "--format=csv,noheader,nounits", "-lms", "200"]
-    try:
-        return subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-    except OSError:
-        return None
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML (read-only queries) on a
+    background thread while the timed region runs; falls back to nvidia-smi polling."""
 
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-def _clock_summary(proc, gpu_index: int):
-    if proc is None:
-        return None
-    proc.terminate()
-    try:
-        out, _ = proc.communicate(timeout=5)
-    except subprocess.TimeoutExpired:
-        proc.kill()
-        out, _ = proc.communicate()
-    sm, mx, reasons = [], None, set()
-    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-    for line in out.strip().splitlines():
-        f = [x.strip() for x in line.split(",")]
-        if len(f) < 9 or not f[0].isdigit() or int(f[0]) != gpu_index:
-            continue
+    def __init__(self, gpu_index: int, period_s: float = 0.002):
+        import ctypes
+        import threading
+        self.samples, self.reasons, self.max_mhz = [], set(), None
+        self._stop = threading.Event()
+        self._thread = None
+        self._nvml = None
         try:
-            sm.append(float(f[1]))
-            mx = float(f[2])
-        except ValueError:
-            continue
-        for nm, v in zip(names, f[5:9]):
-            if v.lower() == "active":
-                reasons.add(nm)
-    if not sm:
-        return None
-    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-            "samples": len(sm)}
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit failed")
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(gpu_index), ctypes.byref(h)) != 0:
+                raise OSError("no NVML handle")
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            getr = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self._nvml = (nv, h, getr)
+        except (OSError, AttributeError):
+            self._nvml = None
+
+        def run():
+            nv, h, getr = self._nvml
+            clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+            while not self._stop.is_set():
+                if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                    self.samples.append(float(clk.value))
+                if getr(h, ctypes.byref(rs)) == 0:
+                    for bit, name in self.REASONS.items():
+                        if rs.value & bit:
+                            self.reasons.add(name)
+                time.sleep(period_s)
+
+        if self._nvml is not None:
+            self._thread = threading.Thread(target=run, daemon=True)
+
+    def start(self):
+        if self._thread is not None:
+            self._thread.start()
+        return self
+
+    def stop(self):
+        if self._thread is None:
+            return None
+        self._stop.set()
+        self._thread.join()
+        if not self.samples:
+            return None
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.samples),
+                "source": "nvml"}
 
 
 def _traffic_record(kernel_key: str):
@@ -274,19 +295,21 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    clk = _clock_sampler() if rank == 0 else None
+    clk = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
+    if clk:
+        clk.start()
     t0.record(stream)
     g_timed.replay()
     t1.record(stream)
     torch.cuda.synchronize()
+    clocks = clk.stop() if clk else None
     if dist:
         dist.barrier()
-    clocks = _clock_summary(clk, torch.cuda.current_device()) if rank == 0 else None
     ms = t0.elapsed_time(t1)
     if dist:
         tt = torch.tensor([ms], device=dev)
@@ -342,6 +365,10 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_s = float(tt.item())
 
+    breakdown = None
+    if args.breakdown and rank == 0:
+        breakdown = call_breakdown(torch, gt, buf, sets, scn, nsets)
+
     if rank != 0:
         return None
     peak, peak_kind = _peaks()
@@ -374,6 +401,8 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
         "clocks": clocks,
         "accepted_len_mean": float(buf.acc_len.float().mean().item()),
     }
+    if breakdown is not None:
+        line["breakdown_us"] = breakdown
     if not args.no_cpu_baseline:
         cv, cdone, cdt = time_oracle(scn, 1000, args.cpu_budget)
         line["cpu_baseline"] = {
@@ -381,6 +410,58 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
             "sample": f"{cdone} whole steps of the same workload (~{cdt:.0f} s, numpy float64; "
                       "BLAS may use every core, the tree and top-k loops use one)"}
     return line
+
+
+def call_breakdown(torch, gt, buf, sets, scn, nsets, reps: int = 50):
+    """Average device time of each C-ABI call of the step inside a CUDA graph: one graph
+    per input set with an externally visible event between consecutive calls."""
+    names = ["gt_prune_topB", "gt_graft_expand", "gt_tree_mask", "gt_tree_attn",
+             "gt_verify_greedy", "gt_succ_update"]
+    sh = buf.shape
+    graphs = []
+    for k in range(nsets):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+        for e in evs:
+            e.record()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        inp = sets[k]
+        with torch.cuda.graph(g):
+            s = torch.cuda.current_stream()
+            gt.gt_event_record_external(evs[0], s)
+            gt.gt_prune_topB(inp["score_in"], inp["parent_in"], inp["tokens_in"], None, sh.B, sh.Nin,
+                             inp["keep"], inp.get("thresh"), sh.N, buf.parent, buf.tokens, buf.score,
+                             buf.old_idx, buf.n_nodes, buf.err, s)
+            gt.gt_event_record_external(evs[1], s)
+            if sh.T > 0:
+                gt.gt_graft_expand(buf.parent, buf.tokens, buf.n_nodes, sh.B, sh.N, inp["tpar"],
+                                   inp["trank"], sh.T, inp["R"], inp["table"], sh.V, sh.k, buf.err,
+                                   s)
+            gt.gt_event_record_external(evs[2], s)
+            gt.gt_tree_mask(buf.parent, buf.n_nodes, inp["prefix_len"], sh.B, sh.N, buf.depth,
+                            buf.pos, buf.mask, buf.err, s)
+            gt.gt_event_record_external(evs[3], s)
+            gt.gt_tree_attn(inp["Q"], inp["K"], inp["V"], buf.mask, inp["prefix_len"],
+                            buf.n_nodes, sh.B, sh.N, sh.Hq, sh.Hkv, sh.d, sh.Lcap, sh.dtype,
+                            scn.scale, buf.O, buf.ws, buf.ws_bytes, buf.err, s)
+            gt.gt_event_record_external(evs[4], s)
+            gt.gt_verify_greedy(inp["logits"], buf.tokens, buf.parent, buf.n_nodes,
+                                inp["prefix_len"], sh.B, sh.N, sh.V, sh.k, buf.topk_id,
+                                buf.topk_val, buf.acc_len, buf.path, buf.out_tok, buf.kv_src,
+                                buf.kv_dst, buf.err, s)
+            gt.gt_event_record_external(evs[5], s)
+            gt.gt_succ_update(inp["table"], sh.V, sh.k, buf.tokens, buf.topk_id, buf.n_nodes,
+                              sh.B, sh.N, buf.err, s)
+            gt.gt_event_record_external(evs[6], s)
+        graphs.append((g, evs))
+    tot = [0.0] * len(names)
+    for r in range(reps):
+        g, evs = graphs[r % nsets]
+        g.replay()
+        torch.cuda.synchronize()
+        for i in range(len(names)):
+            tot[i] += evs[i].elapsed_time(evs[i + 1]) * 1e3
+    return {n: round(t / reps, 2) for n, t in zip(names, tot)}
 
 
 def main():
@@ -391,6 +472,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=sorted(CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--breakdown", action="store_true",
+                    help="also report the in-graph device time of each C-ABI call")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-budget", type=float, default=60.0)
     args = ap.parse_args()

@@ -137,8 +137,8 @@ int gt_tree_mask(const int32_t *parent, const int32_t *n_nodes, const int32_t *p
  *               256-byte aligned; contents need no initialisation and are clobbered.
  * dtype GT_BF16 runs on the tcgen05 tensor cores (bf16 operands, fp32 accumulators in
  * tensor memory, K/V tiles staged by TMA); GT_F32 runs on FP32 FMA units.
- * Limits: d = 128, 1 <= N <= 64, Hq % Hkv == 0, (Hq/Hkv)*N <= 512, Lcap >= 1; Q, K, V, O
- * 16-byte aligned. Device errors: GT_ERR_RANGE (prefix_len + n_nodes > Lcap,
+ * Limits: d = 128, 1 <= N <= 64, Hq % Hkv == 0, (Hq/Hkv)*N <= 512, Lcap >= 1, scale a
+ * finite value > 0 (else GT_ERR_ARG); Q, K, V, O 16-byte aligned. Device errors: GT_ERR_RANGE (prefix_len + n_nodes > Lcap,
  * n_nodes outside [1, N], prefix_len < 0). Keys past a request's length are never read
  * into the result (cache rows there may hold anything, NaN included).
  * ------------------------------------------------------------------------------------- */

@@ -21,67 +21,6 @@
 namespace gt {
 
 // ------------------------------------------------------------------------------------
-// Scheduler: one CTA. tiles_s = ceil((P_b + n_b) / TK); tau = ceil(sum tiles / G);
-// segment s gets ceil(tiles_s / tau) pieces of near-equal tile counts. The piece count
-// is at most G + S, the size the workspace is laid out for.
-// ------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(1024)
-attn_sched_kernel(const int32_t *__restrict__ prefix_len, const int32_t *__restrict__ n_nodes,
-                  int B, int Hkv, int N, int Lcap, int TK, int G, AttnWs ws, int32_t *err) {
-  extern __shared__ int s_tiles[];  // [S]
-  __shared__ long long s_red[32];
-  __shared__ int s_wscan[32];
-  const int S = B * Hkv, tid = threadIdx.x, nt = blockDim.x;
-  const int lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
-  for (int s = tid; s < S; s += nt) {
-    const int b = s / Hkv;
-    const int n = n_nodes[b], P = prefix_len[b];
-    const bool ok = n >= 1 && n <= N && P >= 0 && (long long)P + n <= (long long)Lcap;
-    if (!ok && (s % Hkv) == 0) set_err(err, GT_ERR_RANGE);
-    s_tiles[s] = ok ? ceil_div(P + n, TK) : 0;
-  }
-  __syncthreads();
-  long long part = 0;
-  for (int s = tid; s < S; s += nt) part += s_tiles[s];
-#pragma unroll
-  for (int o = 16; o; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-  if (lane == 0) s_red[warp] = part;
-  __syncthreads();
-  long long T = 0;
-  for (int w = 0; w < nw; ++w) T += s_red[w];
-  const int tau = (int)max(1ll, (T + G - 1) / G);
-  const int chunk = (S + nt - 1) / nt;
-  const int c0 = min(S, tid * chunk), c1 = min(S, c0 + chunk);
-  int local = 0;
-  for (int s = c0; s < c1; ++s) local += ceil_div(s_tiles[s], tau);
-  // block exclusive scan of `local`
-  int incl = local;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) s_wscan[warp] = incl;
-  __syncthreads();
-  int woff = 0, total = 0;
-  for (int w = 0; w < nw; ++w) {
-    woff += (w < warp) ? s_wscan[w] : 0;
-    total += s_wscan[w];
-  }
-  int off = woff + incl - local;
-  for (int s = c0; s < c1; ++s) {
-    const int t = s_tiles[s];
-    const int cnt = ceil_div(t, tau);
-    ws.seg[s] = make_int2(off, cnt);
-    for (int j = 0; j < cnt; ++j)
-      ws.pieces[off + j] = make_int4(s, (int)((long long)t * j / cnt),
-                                     (int)((long long)t * (j + 1) / cnt), 0);
-    off += cnt;
-  }
-  if (tid == 0) ws.hdr[0] = total;
-}
-
-// ------------------------------------------------------------------------------------
 // FP32 SIMT kernel: CTA = (piece, group of 64 query rows); tiles of 64 keys in shared
 // memory; S = Q K^T by 4x4 register blocks, masked online softmax (expf), O by 4x8 blocks.
 // ------------------------------------------------------------------------------------
@@ -101,7 +40,7 @@ __global__ void __launch_bounds__(256)
 attn_simt_kernel(const T *__restrict__ Q, const T *__restrict__ K, const T *__restrict__ V,
                  const uint64_t *__restrict__ mask, const int32_t *__restrict__ prefix_len,
                  const int32_t *__restrict__ n_nodes, int N, int Hq, int Hkv, int Lcap,
-                 float scale, AttnWs ws) {
+                 float scale, SchedArgs sa, AttnWs ws, int32_t *err) {
   extern __shared__ float sm[];
   float *Qs = sm;                              // [d][SIMT_LD] (rows)
   float *Ks = Qs + ATTN_D * SIMT_LD;           // [d][SIMT_LD] (keys)
@@ -112,8 +51,8 @@ attn_simt_kernel(const T *__restrict__ Q, const T *__restrict__ K, const T *__re
   __shared__ uint64_t s_mask[SIMT_ROWS];
 
   const int p = blockIdx.x;
-  if (p >= ws.hdr[0]) return;
-  const int4 pc = ws.pieces[p];
+  const int4 pc = schedule_piece(sa, p, ws, err);
+  if (pc.x < 0) return;
   const int seg = pc.x, b = seg / Hkv, h = seg - b * Hkv;
   const int g = Hq / Hkv;
   const int n = n_nodes[b], P = prefix_len[b], keys = P + n;
@@ -275,29 +214,39 @@ attn_combine_kernel(const int32_t *__restrict__ n_nodes, int B, int N, int Hq, i
   T *dst = O + (size_t)w * ATTN_D + lane * 4;
   const int n = n_nodes[b];
   const int2 sg = (i < n) ? ws.seg[b * Hkv + h] : make_int2(0, 0);
+  // the pieces' log-sum-exps are read in parallel across lanes (one round trip per 32)
   float mx = -INFINITY;
-  for (int j = 0; j < sg.y; ++j) mx = fmaxf(mx, ws.lse[(size_t)(sg.x + j) * ws.rows_pad + r]);
+  for (int j = lane; j < sg.y; j += 32) mx = fmaxf(mx, ws.lse[(size_t)(sg.x + j) * ws.rows_pad + r]);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (mx != -INFINITY) {
     float wsum = 0.f;
-    for (int j = 0; j < sg.y; ++j) {
-      const size_t pr = (size_t)(sg.x + j) * ws.rows_pad + r;
-      const float wt = expf(ws.lse[pr] - mx);
-      const float4 o = *reinterpret_cast<const float4 *>(ws.opart + pr * ATTN_D + lane * 4);
-      acc.x = fmaf(wt, o.x, acc.x);
-      acc.y = fmaf(wt, o.y, acc.y);
-      acc.z = fmaf(wt, o.z, acc.z);
-      acc.w = fmaf(wt, o.w, acc.w);
-      wsum += wt;
+    for (int j0 = 0; j0 < sg.y; j0 += 32) {
+      const int cnt = min(32, sg.y - j0);
+      const float myw =
+          lane < cnt ? expf(ws.lse[(size_t)(sg.x + j0 + lane) * ws.rows_pad + r] - mx) : 0.f;
+      wsum += myw;
+      const float *src = ws.opart + ((size_t)(sg.x + j0) * ws.rows_pad + r) * ATTN_D + lane * 4;
+      const size_t stride = (size_t)ws.rows_pad * ATTN_D;
+#pragma unroll 8
+      for (int j = 0; j < cnt; ++j) {  // independent loads: several partials in flight
+        const float wt = __shfl_sync(0xffffffffu, myw, j);
+        const float4 o = *reinterpret_cast<const float4 *>(src + j * stride);
+        acc.x = fmaf(wt, o.x, acc.x);
+        acc.y = fmaf(wt, o.y, acc.y);
+        acc.z = fmaf(wt, o.z, acc.z);
+        acc.w = fmaf(wt, o.w, acc.w);
+      }
     }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
     const float inv = 1.f / wsum;
     acc = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
   }
   store4<T>(dst, acc);
 }
 
-// SM count of the current device, cached per device so that no device query runs while a
-// stream is being captured.
 static int device_sms() {
   static int cache[64] = {0};
   int dev = 0, sms = 0;
@@ -339,6 +288,7 @@ GT_API int gt_tree_attn(const void *Q, const void *K, const void *V, const uint6
                         void *workspace, size_t ws_bytes, int32_t *err, gt_stream_t stream) {
   if (!attn_args_ok(B, N, Hq, Hkv, d, Lcap)) return GT_ERR_ARG;
   if (dtype != GT_F32 && dtype != GT_BF16) return GT_ERR_ARG;
+  if (!(scale > 0.f) || isinf(scale)) return GT_ERR_ARG;
   if (!attn_shape_ok(N, Hq, Hkv, d)) return GT_ERR_SHAPE;
   if (B == 0) return GT_OK;
   if (!Q || !K || !V || !mask || !prefix_len || !n_nodes || !O || !workspace) return GT_ERR_ARG;
@@ -359,12 +309,10 @@ GT_API int gt_tree_attn(const void *Q, const void *K, const void *V, const uint6
   // the tcgen05 kernel runs one CTA per SM and one CTA per 256 query rows of a piece:
   // aim for one wave of CTAs
   const int Gs = tc ? max(1, G / ceil_div(g * N, 256)) : G;
-  int rc = launch(attn_sched_kernel, dim3(1), dim3(1024), sizeof(int) * (size_t)S, s, prefix_len,
-                  n_nodes, B, Hkv, N, Lcap, TK, Gs, ws, err);
-  if (rc != GT_OK) return rc;
+  const SchedArgs sa{prefix_len, n_nodes, B, Hkv, N, Lcap, TK, Gs};
+  int rc;
   if (tc) {
-    rc = attn_tc_launch(Q, K, V, mask, prefix_len, n_nodes, B, N, Hq, Hkv, Lcap, scale, ws, err,
-                        s);
+    rc = attn_tc_launch(Q, K, V, mask, sa, B, N, Hq, Hkv, Lcap, scale, ws, err, s);
   } else if (dtype == GT_F32) {
     static bool attr_f32 = false;
     if (!attr_f32) {
@@ -375,7 +323,7 @@ GT_API int gt_tree_attn(const void *Q, const void *K, const void *V, const uint6
     }
     rc = launch(attn_simt_kernel<float>, dim3(ws.maxp, ceil_div(g * N, SIMT_ROWS)), dim3(256),
                 SIMT_SMEM, s, (const float *)Q, (const float *)K, (const float *)V, mask,
-                prefix_len, n_nodes, N, Hq, Hkv, Lcap, scale, ws);
+                prefix_len, n_nodes, N, Hq, Hkv, Lcap, scale, sa, ws, err);
   } else {
     static bool attr_bf16 = false;
     if (!attr_bf16) {
@@ -388,7 +336,7 @@ GT_API int gt_tree_attn(const void *Q, const void *K, const void *V, const uint6
     rc = launch(attn_simt_kernel<__nv_bfloat16>, dim3(ws.maxp, ceil_div(g * N, SIMT_ROWS)),
                 dim3(256), SIMT_SMEM, s, (const __nv_bfloat16 *)Q, (const __nv_bfloat16 *)K,
                 (const __nv_bfloat16 *)V, mask, prefix_len, n_nodes, N, Hq, Hkv, Lcap, scale,
-                ws);
+                sa, ws, err);
   }
   if (rc != GT_OK) return rc;
   const int warps = B * N * Hq;

@@ -10,6 +10,8 @@
 
 #include <stdint.h>
 
+#include "gt.h"
+
 namespace gt {
 
 constexpr int ATTN_D = 128;        // head dimension supported by the kernels
@@ -18,7 +20,6 @@ constexpr int ATTN_ROWS_PAD = 128; // partial rows are padded to a multiple of t
 
 struct AttnWs {
   int *hdr;          // [0] number of pieces
-  int4 *pieces;      // (segment, tile_begin, tile_end, 0)
   int2 *seg;         // (first piece, piece count) per segment
   float *lse;        // [maxp][rows_pad] natural-log LSE per partial row
   float *opart;      // [maxp][rows_pad][d] normalised partial O
@@ -33,8 +34,6 @@ static inline size_t attn_ws_layout(void *base, int S, int maxp, int rows_pad, A
   char *p = static_cast<char *>(base);
   const size_t o_hdr = off;
   off += align256(16 * sizeof(int));
-  const size_t o_pieces = off;
-  off += align256((size_t)maxp * sizeof(int4));
   const size_t o_seg = off;
   off += align256((size_t)S * sizeof(int2));
   const size_t o_lse = off;
@@ -43,7 +42,6 @@ static inline size_t attn_ws_layout(void *base, int S, int maxp, int rows_pad, A
   off += align256((size_t)maxp * rows_pad * ATTN_D * sizeof(float));
   if (ws) {
     ws->hdr = reinterpret_cast<int *>(p + o_hdr);
-    ws->pieces = reinterpret_cast<int4 *>(p + o_pieces);
     ws->seg = reinterpret_cast<int2 *>(p + o_seg);
     ws->lse = reinterpret_cast<float *>(p + o_lse);
     ws->opart = reinterpret_cast<float *>(p + o_opart);
@@ -52,5 +50,78 @@ static inline size_t attn_ws_layout(void *base, int S, int maxp, int rows_pad, A
   }
   return off;
 }
+
+// Arguments of the split-KV schedule (all device pointers are per-request arrays).
+struct SchedArgs {
+  const int32_t *prefix_len, *n_nodes;
+  int B, Hkv, N, Lcap, TK, G;
+};
+
+#ifdef __CUDACC__
+// The split-KV schedule, computed redundantly by every CTA of an attention launch so that
+// no separate scheduling kernel is needed. Segment s = (b, h) has
+// tiles_s = ceil((P_b + n_b) / TK) tiles (0 for an invalid request); with
+// tau = ceil(sum_s tiles_s / G) it gets cnt_s = ceil(tiles_s / tau) pieces of near-equal
+// tile counts, numbered consecutively over s. Returns piece p as (segment, tile_begin,
+// tile_end, 0), or segment -1 when p is past the last piece. The CTA at blockIdx (0,0)
+// also publishes (first piece, count) of every segment and the piece total into `ws`, and
+// reports invalid requests. Every thread of the CTA must call it (it synchronises).
+__device__ __forceinline__ int4 schedule_piece(const SchedArgs &a, int p, AttnWs ws,
+                                               int32_t *err) {
+  __shared__ long long s_red[32];
+  __shared__ int s_scan[32];
+  __shared__ int4 s_piece;
+  const int S = a.B * a.Hkv, tid = threadIdx.x, nt = blockDim.x;
+  const int lane = tid & 31, warp = tid >> 5, nw = (nt + 31) >> 5;
+  const bool publisher = blockIdx.x == 0 && blockIdx.y == 0;
+  const int chunk = (S + nt - 1) / nt;
+  const int c0 = min(S, tid * chunk), c1 = min(S, c0 + chunk);
+  auto tiles_of = [&](int s) {
+    const int b = s / a.Hkv;
+    const int n = a.n_nodes[b], P = a.prefix_len[b];
+    const bool ok = n >= 1 && n <= a.N && P >= 0 && (long long)P + n <= (long long)a.Lcap;
+    if (!ok && publisher && (s % a.Hkv) == 0 && err) atomicCAS(err, 0, GT_ERR_RANGE);
+    return ok ? (P + n + a.TK - 1) / a.TK : 0;
+  };
+  if (tid == 0) s_piece = make_int4(-1, 0, 0, 0);
+  long long local = 0;
+  for (int s = c0; s < c1; ++s) local += tiles_of(s);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) local += __shfl_xor_sync(0xffffffffu, local, o);
+  if (lane == 0) s_red[warp] = local;
+  __syncthreads();
+  long long T = 0;
+  for (int w = 0; w < nw; ++w) T += s_red[w];
+  const int tau = (int)max(1ll, (T + a.G - 1) / a.G);
+  int lp = 0;
+  for (int s = c0; s < c1; ++s) lp += (tiles_of(s) + tau - 1) / tau;
+  int incl = lp;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_scan[warp] = incl;
+  __syncthreads();
+  int off = incl - lp, total = 0;
+  for (int w = 0; w < nw; ++w) {
+    off += (w < warp) ? s_scan[w] : 0;
+    total += s_scan[w];
+  }
+  for (int s = c0; s < c1; ++s) {
+    const int t = tiles_of(s);
+    const int cnt = (t + tau - 1) / tau;
+    if (publisher) ws.seg[s] = make_int2(off, cnt);
+    if (p >= off && p < off + cnt) {
+      const int j = p - off;
+      s_piece = make_int4(s, (int)((long long)t * j / cnt), (int)((long long)t * (j + 1) / cnt), 0);
+    }
+    off += cnt;
+  }
+  if (publisher && tid == 0) ws.hdr[0] = total;
+  __syncthreads();
+  return s_piece;
+}
+#endif
 
 }  // namespace gt

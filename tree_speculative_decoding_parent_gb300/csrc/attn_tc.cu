@@ -6,14 +6,19 @@
 //
 // One CTA = one piece of a segment (request b, KV head h, a run of 128-key tiles) for up to
 // 256 query rows (two 128-row M-tiles; row r = node * g + head-in-group). Roles:
-//   warp 8      TMA producer: Q once, then K and V tiles into a 2-stage ring (evict-first);
+//   warp 8      TMA producer: Q once, then K(0), V(0), K(1), V(1), ... into one ring of
+//               5 slots of 32 KB (evict-first). A slot is reused in load order, so a K slot
+//               frees as soon as Q K^T has read it and the next V can stream in early;
 //   warp 9      MMA issuer (one thread) and TMEM owner: per tile and M-tile m,
+//               S_m = Q_m K^T (SMEM x SMEM), then O_m += P_m V (P from TMEM, V from SMEM),
+//               each MMA waiting only for the operands it reads;
 //   warps 10-11 idle (they complete the third warpgroup, which gives its registers away);
-//               S_m = Q_m K^T (SMEM x SMEM), then O_m += P_m V (P from TMEM, V from SMEM);
 //   warps 0-3   softmax of M-tile 0, warps 4-7 softmax of M-tile 1: each thread owns one
 //               query row, reads its S row from TMEM, applies the prefix/ancestor mask,
 //               keeps a running max and sum, writes P (bf16) back over its S row, and at
 //               the end writes the normalised partial O row and its log-sum-exp.
+// 128-key tiles keep every MMA at N = 128, where one tcgen05.mma of M=128, K=16 runs at
+// the tensor pipe's full rate (N = 64 loses about a third of it).
 // Tensor memory (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512);
 // P_m occupies the first 64 columns of S_m as bf16 pairs. MMAs issued by one thread run
 // in issue order, so S_m(j+1) overwrites P_m(j) only after O_m += P_m(j) V has read it,
@@ -43,42 +48,47 @@ constexpr int TC_THREADS = 384;     // 8 softmax warps + producer + MMA + 2 idle
 constexpr int TC_LAUNCH_REGS = 168, TC_LOW_REGS = 56, TC_HIGH_REGS = 224;
 static_assert(2 * 128 * TC_HIGH_REGS + 128 * TC_LOW_REGS == TC_THREADS * TC_LAUNCH_REGS,
               "register split must match the launch budget");
-constexpr int KST = 2, VST = 2;     // K and V ring stages
-constexpr int TILE_BYTES = 32768;   // 128 keys x 128 d x bf16
+constexpr int TK = ATTN_TC_KEYS;    // keys per tile (128)
+constexpr int SLOTS = 5;            // ring slots, each one K or one V tile
 constexpr int HALF_BYTES = 16384;   // 128 rows x 64 d x bf16 (one 128B-swizzled box)
+constexpr int SLOT_BYTES = 2 * HALF_BYTES;  // one tile: 128 keys x 128 d
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
+static_assert(TK == 128, "the tile shape above assumes 128-key tiles");
 
 struct Smem {
   // offsets from the 1024-aligned base
-  static constexpr int Q = 0;                         // [2 m][2 half] x 16 KB
-  static constexpr int K = Q + 4 * HALF_BYTES;        // [KST] x 32 KB
-  static constexpr int V = K + KST * TILE_BYTES;      // [VST] x 32 KB
-  static constexpr int BAR = V + VST * TILE_BYTES;    // mbarriers
-  static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 2 + 2 + 2 + 1;
+  static constexpr int Q = 0;                          // [2 m][2 half] x 16 KB
+  static constexpr int RING = Q + 4 * HALF_BYTES;      // [SLOTS] x 32 KB
+  static constexpr int BAR = RING + SLOTS * SLOT_BYTES;
+  static constexpr int NBAR = 1 + 2 * SLOTS + 2 + 2 + 2 + 1;
   static constexpr int END = BAR + NBAR * 8;
 };
 constexpr size_t TC_SMEM = Smem::END + 1024;  // + alignment slack
+static_assert(TC_SMEM <= 232448, "shared memory of one CTA");
 
 struct Bars {
-  uint64_t *q_full, *k_full, *k_empty, *v_full, *v_empty, *s_full, *p_full, *o_done, *drain;
+  uint64_t *q_full, *full, *empty, *s_full, *p_full, *o_done, *drain;
 };
 
 __device__ __forceinline__ Bars bars_at(uint8_t *base) {
   uint64_t *b = reinterpret_cast<uint64_t *>(base + Smem::BAR);
   Bars r;
   r.q_full = b;
-  r.k_full = b + 1;
-  r.k_empty = r.k_full + KST;
-  r.v_full = r.k_empty + KST;
-  r.v_empty = r.v_full + VST;
-  r.s_full = r.v_empty + VST;
+  r.full = b + 1;
+  r.empty = r.full + SLOTS;
+  r.s_full = r.empty + SLOTS;
   r.p_full = r.s_full + 2;
   r.o_done = r.p_full + 2;
   r.drain = r.o_done + 2;
   return r;
 }
+
+// Load sequence: item 2j is K(j), item 2j+1 is V(j); item q lives in slot q % SLOTS and is
+// that slot's use number q / SLOTS.
+__device__ __forceinline__ int slot_of(int q) { return q % SLOTS; }
+__device__ __forceinline__ uint32_t use_parity(int q) { return (uint32_t)((q / SLOTS) & 1); }
 
 // Bounded wait that ignores the abort flag (used only while draining in-flight work).
 __device__ __forceinline__ bool drain_wait(uint64_t *bar, uint32_t parity) {
@@ -90,14 +100,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
                const __grid_constant__ CUtensorMap mapV, const uint64_t *__restrict__ mask,
                const int32_t *__restrict__ prefix_len, const int32_t *__restrict__ n_nodes,
-               int N, int Hq, int Hkv, float scale, AttnWs ws, int32_t *err) {
+               int N, int Hq, int Hkv, float scale, SchedArgs sa, AttnWs ws, int32_t *err) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t tmem_sh;
   __shared__ int abort_sh;
 
   const int p = blockIdx.x;
-  if (p >= ws.hdr[0]) return;
-  const int4 pc = ws.pieces[p];
+  const int4 pc = schedule_piece(sa, p, ws, err);
+  if (pc.x < 0) return;
   const int seg = pc.x, b = seg / Hkv, h = seg - b * Hkv;
   const int g = Hq / Hkv;
   const int n = n_nodes[b], P = prefix_len[b], keys = P + n;
@@ -115,13 +125,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
   if (tid == 0) {
     abort_sh = 0;
     tc::mbar_init(bar.q_full, 1);
-    for (int s = 0; s < KST; ++s) {
-      tc::mbar_init(bar.k_full + s, 1);
-      tc::mbar_init(bar.k_empty + s, 1);
-    }
-    for (int s = 0; s < VST; ++s) {
-      tc::mbar_init(bar.v_full + s, 1);
-      tc::mbar_init(bar.v_empty + s, 1);
+    for (int s = 0; s < SLOTS; ++s) {
+      tc::mbar_init(bar.full + s, 1);
+      tc::mbar_init(bar.empty + s, 1);
     }
     for (int m = 0; m < 2; ++m) {
       tc::mbar_init(bar.s_full + m, 1);
@@ -158,39 +164,31 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
                           0, h, b * N + node0, pol_q);
       }
       const int plane = b * Hkv + h;
-      int last_k = -1, last_v = -1;
-      for (int j = 0; j < nt; ++j) {
-        const int kb = (t0 + j) * 128;
-        const int ks = j % KST, vs = j % VST;
-        if (j >= KST && !tc::mbar_wait(bar.k_empty + ks, ((j / KST) - 1) & 1, abort)) break;
-        tc::mbar_expect_tx(bar.k_full + ks, TILE_BYTES);
+      int last = -1;
+      for (int q = 0; q < 2 * nt; ++q) {
+        const int s = slot_of(q);
+        if (q >= SLOTS && !tc::mbar_wait(bar.empty + s, use_parity(q - SLOTS), abort)) break;
+        uint8_t *dst = base + Smem::RING + s * SLOT_BYTES;
+        const CUtensorMap *map = (q & 1) ? &mapV : &mapK;
+        const int kb = (t0 + (q >> 1)) * TK;
+        tc::mbar_expect_tx(bar.full + s, SLOT_BYTES);
         for (int hf = 0; hf < 2; ++hf)
-          tc::tma_load_3d(base + Smem::K + ks * TILE_BYTES + hf * HALF_BYTES, &mapK,
-                          bar.k_full + ks, hf * 64, kb, plane, pol_kv);
-        last_k = j;
-        if (j >= VST && !tc::mbar_wait(bar.v_empty + vs, ((j / VST) - 1) & 1, abort)) break;
-        tc::mbar_expect_tx(bar.v_full + vs, TILE_BYTES);
-        for (int hf = 0; hf < 2; ++hf)
-          tc::tma_load_3d(base + Smem::V + vs * TILE_BYTES + hf * HALF_BYTES, &mapV,
-                          bar.v_full + vs, hf * 64, kb, plane, pol_kv);
-        last_v = j;
+          tc::tma_load_3d(dst + hf * HALF_BYTES, map, bar.full + s, hf * 64, kb, plane, pol_kv);
+        last = q;
       }
       if (*abort) {  // let every issued copy land before the CTA's shared memory goes away
         drain_wait(bar.q_full, 0);
-        for (int j = (last_k - KST + 1 > 0 ? last_k - KST + 1 : 0); j <= last_k; ++j)
-          drain_wait(bar.k_full + j % KST, (j / KST) & 1);
-        for (int j = (last_v - VST + 1 > 0 ? last_v - VST + 1 : 0); j <= last_v; ++j)
-          drain_wait(bar.v_full + j % VST, (j / VST) & 1);
+        for (int q = (last - SLOTS + 1 > 0 ? last - SLOTS + 1 : 0); q <= last; ++q)
+          drain_wait(bar.full + slot_of(q), use_parity(q));
       }
     } else if (warp == 9 && lane == 0) {
       // -------------------------------------------------------------- MMA issuer
-      constexpr uint32_t idS = tc::idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idS = tc::idesc_bf16(128, TK, false, false);
       constexpr uint32_t idO = tc::idesc_bf16(128, 128, false, true);
       const uint32_t sQ = tc::smem_u32(base + Smem::Q);
-      const uint32_t sK = tc::smem_u32(base + Smem::K);
-      const uint32_t sV = tc::smem_u32(base + Smem::V);
-      auto issue_s = [&](int m, int ks) {
-        const uint32_t q0 = sQ + m * 2 * HALF_BYTES, k0 = sK + ks * TILE_BYTES;
+      const uint32_t ring = tc::smem_u32(base + Smem::RING);
+      auto issue_s = [&](int m, int s) {  // S_m = Q_m K^T over d = 128 (8 steps of 16)
+        const uint32_t q0 = sQ + m * 2 * HALF_BYTES, k0 = ring + s * SLOT_BYTES;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
@@ -198,40 +196,43 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
                      tc::sdesc_sw128(k0 + off, 16, 1024), idS, kk > 0);
         }
       };
-      bool ok = tc::mbar_wait(bar.q_full, 0, abort) && tc::mbar_wait(bar.k_full, 0, abort);
+      bool ok = tc::mbar_wait(bar.q_full, 0, abort) &&
+                tc::mbar_wait(bar.full + slot_of(0), use_parity(0), abort);
       if (ok) {
         tc::tc_fence_after();
         for (int m = 0; m < mtiles; ++m) {
-          issue_s(m, 0);
+          issue_s(m, slot_of(0));
           tc::mma_commit(bar.s_full + m);
         }
-        tc::mma_commit(bar.k_empty);
+        tc::mma_commit(bar.empty + slot_of(0));  // K(0) is free once both S_m(0) are done
       }
       for (int j = 0; ok && j < nt; ++j) {
-        const int vs = j % VST;
+        const int qv = 2 * j + 1, qk = 2 * j + 2;  // V(j), K(j+1)
         const bool next = j + 1 < nt;
-        const int ks = (j + 1) % KST;
-        if (!tc::mbar_wait(bar.v_full + vs, (j / VST) & 1, abort)) break;
-        if (next && !tc::mbar_wait(bar.k_full + ks, ((j + 1) / KST) & 1, abort)) break;
+        if (!tc::mbar_wait(bar.full + slot_of(qv), use_parity(qv), abort)) break;
+        const uint32_t v0 = ring + slot_of(qv) * SLOT_BYTES;
         for (int m = 0; m < mtiles; ++m) {
           if (!tc::mbar_wait(bar.p_full + m, j & 1, abort)) {
             ok = false;
             break;
           }
           tc::tc_fence_after();
-          const uint32_t v0 = sV + vs * TILE_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
+          for (int kk = 0; kk < 8; ++kk)  // O_m += P_m V over 128 keys (steps of 16)
             tc::mma_ts(tmem + 256 + m * 128, tmem + m * 128 + kk * 8,
                        tc::sdesc_sw128(v0 + kk * 2048, HALF_BYTES, 1024), idO, (j > 0) || (kk > 0));
           if (next) {
-            issue_s(m, ks);
+            if (m == 0 && !tc::mbar_wait(bar.full + slot_of(qk), use_parity(qk), abort)) {
+              ok = false;
+              break;
+            }
+            issue_s(m, slot_of(qk));
             tc::mma_commit(bar.s_full + m);
           }
         }
         if (!ok) break;
-        tc::mma_commit(bar.v_empty + vs);
-        if (next) tc::mma_commit(bar.k_empty + ks);
+        tc::mma_commit(bar.empty + slot_of(qv));            // V(j) read by both P V
+        if (next) tc::mma_commit(bar.empty + slot_of(qk));  // K(j+1) read by both S
       }
       if (ok)
         for (int m = 0; m < mtiles; ++m) tc::mma_commit(bar.o_done + m);
@@ -250,8 +251,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + m * 128;
     const uint32_t tO = tmem + lane_base + 256 + m * 128;
-    const float sl2 = scale * LOG2E;
-    float m_used = -INFINITY, l = 0.f;
+    const float sl2 = scale * LOG2E;  // scale > 0: the max of raw scores gives the max
+    float m_used = -INFINITY, l = 0.f;  // running max (log2 units) and sum of this row
     bool ok = active;
     for (int j = 0; ok && j < nt; ++j) {
       // wait results are made warp-uniform: the TMEM accesses below are warp-collective
@@ -264,27 +265,35 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
 #pragma unroll
       for (int c = 0; c < 4; ++c) tc::tmem_ld32(tS + c * 32, s[c]);
       tc::tmem_wait_ld();
-      const int kb = (t0 + j) * 128;
-      const bool all_vis = kb + 128 <= P;
-      float mx = -INFINITY;
+      const int kb = (t0 + j) * TK;
+      // 8 independent partial maxima of the raw scores keep the dependent chain short
+      float mxa[8];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int a = 0; a < 8; ++a) mxa[a] = -INFINITY;
+      if (kb + TK <= P) {  // whole tile inside the committed prefix: every key visible
 #pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          const int key = kb + c * 32 + q;
-          bool vis = true;
-          if (!all_vis) {
-            vis = key < P || (key < keys && ((mrow >> (unsigned)(key - P)) & 1ull));
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int q = 0; q < 32; ++q) mxa[q & 7] = fmaxf(mxa[q & 7], __uint_as_float(s[c][q]));
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int q = 0; q < 32; ++q) {
+            const int key = kb + c * 32 + q;
+            const bool vis =
+                key < P || (key < keys && ((mrow >> (unsigned)(key - P)) & 1ull));
+            if (!vis) s[c][q] = __float_as_uint(-INFINITY);
+            mxa[q & 7] = fmaxf(mxa[q & 7], __uint_as_float(s[c][q]));
           }
-          const float t = vis ? __uint_as_float(s[c][q]) * sl2 : -INFINITY;
-          s[c][q] = __float_as_uint(t);
-          mx = fmaxf(mx, t);
-        }
+      }
+      const float mx = sl2 * fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
+                                   fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
       // lazy rescale: move the reference max only when it grows by more than 8 (x256)
       const bool grow = mx > m_used + 8.f;
       float alpha = 1.f;
       if (grow) {
-        alpha = (m_used == -INFINITY) ? 0.f : exp2f(m_used - mx);
+        alpha = (m_used == -INFINITY) ? 0.f : tc::ex2_approx(m_used - mx);
         m_used = mx;
       }
       if (__any_sync(0xffffffffu, grow && j > 0)) {
@@ -306,37 +315,41 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
         tc::tmem_wait_st();
       }
       l *= alpha;
-      const bool live = m_used != -INFINITY;
+      // p = 2^(s * scale * log2 e - m); a row with no visible key so far has m = -inf and
+      // every s = -inf: its p are 0 (not NaN)
+      const float msub = m_used == -INFINITY ? 0.f : m_used;
+      float la[8];
+#pragma unroll
+      for (int a = 0; a < 8; ++a) la[a] = 0.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
-          const float t0v = __uint_as_float(s[c][2 * q]), t1v = __uint_as_float(s[c][2 * q + 1]);
-          const float p0 = live ? exp2f(t0v - m_used) : 0.f;
-          const float p1 = live ? exp2f(t1v - m_used) : 0.f;
-          l += p0 + p1;
+          const float p0 = tc::ex2_approx(fmaf(__uint_as_float(s[c][2 * q]), sl2, -msub));
+          const float p1 = tc::ex2_approx(fmaf(__uint_as_float(s[c][2 * q + 1]), sl2, -msub));
+          la[q & 7] += p0 + p1;
           pk[q] = tc::pack_bf16x2(p0, p1);
         }
         tc::tmem_st16(tS + c * 16, pk);
       }
+      l += ((la[0] + la[1]) + (la[2] + la[3])) + ((la[4] + la[5]) + (la[6] + la[7]));
       tc::tmem_wait_st();
-      if (m == 0 && kb + 128 > keys) {
+      if (m == 0 && kb + TK > keys) {
         // zero V rows past the request's length (they may hold NaN) before P V reads them
-        const int vs = j % VST;
-        if (!__all_sync(0xffffffffu, tc::mbar_wait(bar.v_full + vs, (j / VST) & 1, abort))) {
+        const int qv = 2 * j + 1;
+        if (!__all_sync(0xffffffffu, tc::mbar_wait(bar.full + slot_of(qv), use_parity(qv), abort))) {
           ok = false;
           break;
-        } else {
-          uint8_t *vt = base + Smem::V + vs * TILE_BYTES;
-          const int first = keys - kb > 0 ? keys - kb : 0;
-          for (int e = rl; e < (128 - first) * 16; e += 128) {
-            const int row = first + e / 16, chunk = e % 16;  // 2 halves x 8 chunks of 16 B
-            *reinterpret_cast<uint4 *>(vt + (chunk >> 3) * HALF_BYTES + row * 128 +
-                                       (chunk & 7) * 16) = make_uint4(0, 0, 0, 0);
-          }
-          tc::fence_proxy_async_smem();
         }
+        uint8_t *vt = base + Smem::RING + slot_of(qv) * SLOT_BYTES;
+        const int first = keys - kb > 0 ? keys - kb : 0;
+        for (int e = rl; e < (TK - first) * 16; e += 128) {
+          const int row = first + e / 16, chunk = e % 16;  // 2 halves x 8 chunks of 16 B
+          *reinterpret_cast<uint4 *>(vt + (chunk >> 3) * HALF_BYTES + row * 128 +
+                                     (chunk & 7) * 16) = make_uint4(0, 0, 0, 0);
+        }
+        tc::fence_proxy_async_smem();
       }
       tc::tc_fence_before();
       tc::mbar_arrive(bar.p_full + m);
@@ -403,9 +416,8 @@ bool attn_tc_supported(int g, int N) {
 }
 
 int attn_tc_launch(const void *Q, const void *K, const void *V, const uint64_t *mask,
-                   const int32_t *prefix_len, const int32_t *n_nodes, int B, int N, int Hq,
-                   int Hkv, int Lcap, float scale, const AttnWs &ws, int32_t *err,
-                   cudaStream_t s) {
+                   const SchedArgs &sa, int B, int N, int Hq, int Hkv, int Lcap, float scale,
+                   const AttnWs &ws, int32_t *err, cudaStream_t s) {
   const int g = Hq / Hkv;
   CUtensorMap mQ, mK, mV;
   const cuuint64_t qdims[4] = {(cuuint64_t)ATTN_D, (cuuint64_t)g, (cuuint64_t)Hkv,
@@ -415,7 +427,7 @@ int attn_tc_launch(const void *Q, const void *K, const void *V, const uint64_t *
   const cuuint32_t qbox[4] = {64, (cuuint32_t)g, 1, (cuuint32_t)(128 / g)};
   const cuuint64_t kdims[3] = {(cuuint64_t)ATTN_D, (cuuint64_t)Lcap, (cuuint64_t)B * Hkv};
   const cuuint64_t kstr[2] = {(cuuint64_t)ATTN_D * 2, (cuuint64_t)Lcap * ATTN_D * 2};
-  const cuuint32_t kbox[3] = {64, 128, 1};
+  const cuuint32_t kbox[3] = {64, (cuuint32_t)TK, 1};
   if (!encode_fn()) {
     note_error("cuTensorMapEncodeTiled entry point", cudaErrorNotSupported);
     return GT_ERR_CUDA;
@@ -446,7 +458,7 @@ int attn_tc_launch(const void *Q, const void *K, const void *V, const uint64_t *
   }
   const int row_groups = ceil_div(g * N, 256);
   return launch(attn_tc_kernel, dim3(ws.maxp, row_groups), dim3(TC_THREADS), TC_SMEM, s, mQ, mK,
-                mV, mask, prefix_len, n_nodes, N, Hq, Hkv, scale, ws, err);
+                mV, mask, sa.prefix_len, sa.n_nodes, N, Hq, Hkv, scale, sa, ws, err);
 }
 
 }  // namespace gt

@@ -13,11 +13,10 @@ constexpr int ATTN_TC_KEYS = 128;  // keys per K/V tile
 // True when the tcgen05 kernel handles g query heads per KV head and N tree nodes.
 bool attn_tc_supported(int g, int N);
 
-// Runs the split-KV pieces listed in `ws` (already scheduled with tiles of ATTN_TC_KEYS)
-// and writes the partial O / LSE rows of every piece.
+// Runs every split-KV piece of the schedule (tiles of ATTN_TC_KEYS keys, computed in the
+// kernel from `sa`) and writes the partial O / LSE rows of every piece.
 int attn_tc_launch(const void *Q, const void *K, const void *V, const uint64_t *mask,
-                   const int32_t *prefix_len, const int32_t *n_nodes, int B, int N, int Hq,
-                   int Hkv, int Lcap, float scale, const AttnWs &ws, int32_t *err,
-                   cudaStream_t s);
+                   const SchedArgs &sa, int B, int N, int Hq, int Hkv, int Lcap, float scale,
+                   const AttnWs &ws, int32_t *err, cudaStream_t s);
 
 }  // namespace gt
