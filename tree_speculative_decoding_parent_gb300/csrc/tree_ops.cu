@@ -28,8 +28,9 @@ prune_kernel(const float *__restrict__ score, const int32_t *__restrict__ parent
              int32_t *__restrict__ out_parent, int32_t *__restrict__ out_tokens,
              float *__restrict__ out_score, int32_t *__restrict__ out_old,
              int32_t *__restrict__ n_out, int32_t *err) {
-  extern __shared__ float s_score[];           // [Nin]
-  int *s_new = reinterpret_cast<int *>(s_score + Nin);  // [Nin]
+  extern __shared__ float s_score[];           // [Nin4] (NaN-padded), then s_new [Nin]
+  const int Nin4 = (Nin + 3) & ~3;
+  int *s_new = reinterpret_cast<int *>(s_score + Nin4);  // [Nin]
   __shared__ int warp_tot[32];
   __shared__ int s_bad;
   const int b = blockIdx.x, v = threadIdx.x;
@@ -75,14 +76,25 @@ prune_kernel(const float *__restrict__ score, const int32_t *__restrict__ parent
     return;
   }
   const float th = thresh ? thresh[b] : -INFINITY;
+  // the rank loop compares against every node: hide the root and the padding behind NaN
+  // (NaN fails every comparison), then read four scores per shared-memory load
+  if (v == 0) s_score[0] = __int_as_float(0x7fc00000);
+  for (int u = n + v; u < Nin4; u += blockDim.x) s_score[u] = __int_as_float(0x7fc00000);
+  __syncthreads();
   bool kept = (v == 0);
   if (v > 0 && v < n && s >= th) {
-    int rank = 0;
-    for (int u = 1; u < n; ++u) {
-      const float su = s_score[u];
-      rank += (su >= th) && (su > s || (su == s && u < v));
+    const float4 *s4 = reinterpret_cast<const float4 *>(s_score);
+    int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+#pragma unroll 4
+    for (int q = 0; q < (n + 3) >> 2; ++q) {
+      const float4 x = s4[q];
+      const int u = 4 * q;
+      r0 += (x.x >= th) & ((x.x > s) | ((x.x == s) & (u < v)));
+      r1 += (x.y >= th) & ((x.y > s) | ((x.y == s) & (u + 1 < v)));
+      r2 += (x.z >= th) & ((x.z > s) | ((x.z == s) & (u + 2 < v)));
+      r3 += (x.w >= th) & ((x.w > s) | ((x.w == s) & (u + 3 < v)));
     }
-    kept = rank < ke - 1;
+    kept = (r0 + r1) + (r2 + r3) < ke - 1;
   }
   int total;
   const int newi = block_excl_count(kept, warp_tot, &total);
@@ -255,7 +267,7 @@ GT_API int gt_prune_topB(const float *score, const int32_t *parent, const int32_
   if (B == 0) return GT_OK;
   if (!score || !parent || !tokens || !keep || !out_parent || !out_tokens || !n_out)
     return GT_ERR_ARG;
-  const size_t smem = 2 * sizeof(int) * (size_t)Nin;
+  const size_t smem = sizeof(int) * ((size_t)((Nin + 3) & ~3) + (size_t)Nin);
   return launch(prune_kernel, dim3(B), dim3(round32(Nin)), smem, (cudaStream_t)stream, score,
                 parent, tokens, n_in, Nin, keep, thresh, Nout, out_parent, out_tokens,
                 out_score, out_old_idx, n_out, err);

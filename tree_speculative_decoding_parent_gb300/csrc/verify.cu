@@ -8,14 +8,19 @@
 // prefix, roll back at the first error) and §五 (greedy decoding, temperature 0).
 //
 // Top-k design (HBM-bound: rows * V * 4 bytes, read once):
-//   - a thread-block cluster of CL CTAs shares one row; each CTA streams a contiguous
-//     1/CL of the row with 128-bit evict-first loads, so the 60-960 rows of a step fill
-//     all 152 SMs;
-//   - every thread keeps a sorted top-KK list in registers; an element enters only if its
-//     order key beats the list's last key (one compare on the common path);
-//   - lists merge warp -> CTA by KK rounds of a warp-wide max over 64-bit keys
-//     (order key, inverted index), then CTA -> cluster through distributed shared
-//     memory into the leader CTA, which writes the row's result.
+//   - a thread-block cluster of CL CTAs shares one row; each CTA takes a contiguous 1/CL of
+//     it, so the 60-960 rows of a step fill the GPU in one wave. Each thread streams its
+//     part in chunks of PER float4 with the next chunk's loads in flight (evict-first);
+//   - threshold: from the first chunk, the KK-th largest of the CTA's lane maxima (warp
+//     bitonic sorts); KK distinct elements lie at or above it, so nothing below reaches the
+//     CTA's top-KK. Elements not below it (ties and NaN included) are appended to a shared
+//     buffer; for ordinary logits that is a few dozen per CTA;
+//   - one warp merges the buffer by KK rounds of a warp argmax built from two redux.sync
+//     reductions (order key, then lowest index); the CTA results meet in the cluster
+//     leader's shared memory (DSMEM) for the same merge;
+//   - a buffer overflow (massive ties) redoes the CTA's part with exact per-thread sorted
+//     lists, so the threshold never decides correctness; rows whose length or alignment
+//     rules out 16-byte loads take that path too.
 #include <cooperative_groups.h>
 #include <math.h>
 
@@ -28,12 +33,21 @@ namespace gt {
 
 constexpr int TOPK_THREADS = 256;
 constexpr int TOPK_CLUSTER = 8;
+constexpr int TOPK_PER = 5;      // float4 per thread per chunk (a second chunk in flight)
+constexpr int TOPK_CAP = 512;    // candidate buffer per CTA
 
 __device__ __forceinline__ uint64_t pack_key(uint32_t key, int idx) {
   return ((uint64_t)key << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)idx);
 }
 __device__ __forceinline__ int unpack_idx(uint64_t p) {
   return (int)(0xFFFFFFFFu - (uint32_t)(p & 0xFFFFFFFFull));
+}
+
+// Inverse of order_key for keys of real numbers; keys 0 (empty) and 1 (NaN) give -inf,
+// which makes every element a candidate.
+__device__ __forceinline__ float key_floor(uint32_t k) {
+  if (k <= 1u) return -INFINITY;
+  return __uint_as_float((k & 0x80000000u) ? (k ^ 0x80000000u) : ~k);
 }
 
 // Insert (nk, ni) into a list sorted by key descending. Callers scan indices in
@@ -61,24 +75,63 @@ __device__ __forceinline__ void consider(uint32_t (&key)[KK], int (&idx)[KK], fl
   if (kx > key[KK - 1]) list_insert<KK>(key, idx, kx, i);
 }
 
-__device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
+// A bitonic sort of one key per lane across the warp, descending: lane r returns the
+// (r+1)-th largest.
+__device__ __forceinline__ uint32_t warp_sorted_desc(uint32_t v) {
+  const int lane = threadIdx.x & 31;
 #pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    const uint64_t w = __shfl_xor_sync(0xffffffffu, v, o);
-    v = w > v ? w : v;
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const uint32_t o = __shfl_xor_sync(0xffffffffu, v, stride);
+      const bool up = (lane & size) != 0;          // this block sorts ascending
+      const bool lower = (lane & stride) == 0;
+      v = (lower == up) ? min(v, o) : max(v, o);
+    }
   }
   return v;
 }
 
-// KK rounds of a warp-wide max over each lane's list head; lane r returns the r-th best.
+// Warp-wide max of packed (order key, inverted index) words: two single-instruction
+// reductions, the key first, then the lowest index among the lanes holding that key.
+__device__ __forceinline__ uint64_t warp_max_packed(uint64_t v) {
+  const uint32_t hi = (uint32_t)(v >> 32);
+  const uint32_t khi = __reduce_max_sync(0xffffffffu, hi);
+  const uint32_t klo = __reduce_max_sync(0xffffffffu, hi == khi ? (uint32_t)v : 0u);
+  return ((uint64_t)khi << 32) | klo;
+}
+
+// KK rounds over NC unsorted candidates per lane (0 = empty); lane r returns the r-th
+// best. Packed words are unique, so each round removes exactly one candidate.
+template <int KK, int NC>
+__device__ __forceinline__ uint64_t warp_select(uint64_t (&c)[NC]) {
+  const int lane = threadIdx.x & 31;
+  uint64_t out = 0;
+#pragma unroll
+  for (int r = 0; r < KK; ++r) {
+    uint64_t my = c[0];
+#pragma unroll
+    for (int j = 1; j < NC; ++j) my = c[j] > my ? c[j] : my;
+    const uint64_t best = warp_max_packed(my);
+    if (best != 0) {
+#pragma unroll
+      for (int j = 0; j < NC; ++j)
+        if (c[j] == best) c[j] = 0;
+    }
+    if (lane == r) out = best;
+  }
+  return out;
+}
+
+// KK rounds of a warp argmax over each lane's sorted list head; lane r gets the r-th best.
 template <int KK>
 __device__ __forceinline__ uint64_t warp_merge_lists(uint32_t (&key)[KK], int (&idx)[KK]) {
   const int lane = threadIdx.x & 31;
   uint64_t out = 0;
 #pragma unroll
   for (int r = 0; r < KK; ++r) {
-    const uint64_t my = pack_key(key[0], idx[0]);
-    const uint64_t best = warp_max_u64(my);
+    const uint64_t my = key[0] ? pack_key(key[0], idx[0]) : 0ull;
+    const uint64_t best = warp_max_packed(my);
     if (best != 0 && my == best) {
 #pragma unroll
       for (int j = 0; j < KK - 1; ++j) {
@@ -93,25 +146,33 @@ __device__ __forceinline__ uint64_t warp_merge_lists(uint32_t (&key)[KK], int (&
   return out;
 }
 
-// KK rounds over NC unsorted candidates per lane; lane r returns the r-th best.
-template <int KK, int NC>
-__device__ __forceinline__ uint64_t warp_merge_cands(uint64_t (&c)[NC]) {
-  const int lane = threadIdx.x & 31;
-  uint64_t out = 0;
+// Exact per-thread sorted lists over [b, e) of one row, merged to the CTA's top-KK in
+// s_top by warp 0 (rows without 16-byte alignment, and the overflow fallback).
+template <int KK>
+__device__ __forceinline__ void topk_exact(const float *x, int b, int e, uint64_t *s_stage,
+                                           uint64_t *s_top) {
+  constexpr int NW = TOPK_THREADS / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t key[KK];
+  int idx[KK];
 #pragma unroll
-  for (int r = 0; r < KK; ++r) {
-    uint64_t my = c[0];
+  for (int j = 0; j < KK; ++j) key[j] = 0u, idx[j] = -1;
+  for (int i = b + tid; i < e; i += TOPK_THREADS) consider<KK>(key, idx, __ldcs(x + i), i);
+  const uint64_t wb = warp_merge_lists<KK>(key, idx);
+  if (lane < KK) s_stage[warp * KK + lane] = wb;
+  __syncthreads();
+  if (warp == 0) {
+    constexpr int NC = (NW * KK + 31) / 32;
+    uint64_t c[NC];
 #pragma unroll
-    for (int j = 1; j < NC; ++j) my = c[j] > my ? c[j] : my;
-    const uint64_t best = warp_max_u64(my);
-    if (best != 0) {
-#pragma unroll
-      for (int j = 0; j < NC; ++j)
-        if (c[j] == best) c[j] = 0;
+    for (int j = 0; j < NC; ++j) {
+      const int q = lane + 32 * j;
+      c[j] = q < NW * KK ? s_stage[q] : 0ull;
     }
-    if (lane == r) out = best;
+    const uint64_t bb = warp_select<KK, NC>(c);
+    if (lane < KK) s_top[lane] = bb;
   }
-  return out;
+  __syncthreads();
 }
 
 template <int KK, int CL>
@@ -119,8 +180,13 @@ __global__ void __launch_bounds__(TOPK_THREADS)
 topk_cluster_kernel(const float *__restrict__ logits, int row0, int V, int k,
                     int32_t *__restrict__ ids, float *__restrict__ vals) {
   constexpr int NW = TOPK_THREADS / 32;
-  __shared__ uint64_t s_warp[NW * KK];
+  constexpr int CH = TOPK_PER * TOPK_THREADS;  // float4 per chunk of the CTA
+  __shared__ uint64_t s_cand[TOPK_CAP];        // candidates, then scratch of the merges
+  __shared__ uint64_t s_top[KK];               // the CTA's top-KK
   __shared__ uint64_t s_clus[CL * KK];
+  __shared__ uint32_t s_lmax[NW * KK];         // each warp's KK largest lane maxima
+  __shared__ uint32_t s_thr;
+  __shared__ int s_cnt;
   cg::cluster_group cluster = cg::this_cluster();
   // Every CTA of the cluster must be running before the leader's shared memory is
   // written remotely; arrive now, wait just before that write.
@@ -129,66 +195,108 @@ topk_cluster_kernel(const float *__restrict__ logits, int row0, int V, int k,
   const int crank = (int)cluster.block_rank();
   const int row = row0 + blockIdx.y;
   const float *x = logits + (size_t)row * V;
-  uint32_t key[KK];
-  int idx[KK];
-#pragma unroll
-  for (int j = 0; j < KK; ++j) {
-    key[j] = 0u;
-    idx[j] = -1;
-  }
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) s_cnt = 0;
+
   const bool vec = ((V & 3) == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15) == 0);
   if (vec) {
     const int V4 = V >> 2;
     const int b4 = (int)((long long)V4 * crank / CL), e4 = (int)((long long)V4 * (crank + 1) / CL);
     const float4 *x4 = reinterpret_cast<const float4 *>(x);
-    int i = b4 + tid;
-    for (; i + 3 * TOPK_THREADS < e4; i += 4 * TOPK_THREADS) {
-      const float4 a = __ldcs(x4 + i);
-      const float4 b = __ldcs(x4 + i + TOPK_THREADS);
-      const float4 c = __ldcs(x4 + i + 2 * TOPK_THREADS);
-      const float4 d = __ldcs(x4 + i + 3 * TOPK_THREADS);
-      int base = 4 * i;
-      consider<KK>(key, idx, a.x, base), consider<KK>(key, idx, a.y, base + 1);
-      consider<KK>(key, idx, a.z, base + 2), consider<KK>(key, idx, a.w, base + 3);
-      base += 4 * TOPK_THREADS;
-      consider<KK>(key, idx, b.x, base), consider<KK>(key, idx, b.y, base + 1);
-      consider<KK>(key, idx, b.z, base + 2), consider<KK>(key, idx, b.w, base + 3);
-      base += 4 * TOPK_THREADS;
-      consider<KK>(key, idx, c.x, base), consider<KK>(key, idx, c.y, base + 1);
-      consider<KK>(key, idx, c.z, base + 2), consider<KK>(key, idx, c.w, base + 3);
-      base += 4 * TOPK_THREADS;
-      consider<KK>(key, idx, d.x, base), consider<KK>(key, idx, d.y, base + 1);
-      consider<KK>(key, idx, d.z, base + 2), consider<KK>(key, idx, d.w, base + 3);
+    const float4 ninf = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    float4 a[TOPK_PER], nx[TOPK_PER];
+#pragma unroll
+    for (int u = 0; u < TOPK_PER; ++u) {
+      const int q = b4 + tid + u * TOPK_THREADS;
+      a[u] = q < e4 ? __ldcs(x4 + q) : ninf;
     }
-    for (; i < e4; i += TOPK_THREADS) {
-      const float4 a = __ldcs(x4 + i);
-      const int base = 4 * i;
-      consider<KK>(key, idx, a.x, base), consider<KK>(key, idx, a.y, base + 1);
-      consider<KK>(key, idx, a.z, base + 2), consider<KK>(key, idx, a.w, base + 3);
+    float thr = -INFINITY;
+    for (int c0 = b4; c0 < e4; c0 += CH) {
+      // the next chunk's loads are in flight while this chunk is examined
+#pragma unroll
+      for (int u = 0; u < TOPK_PER; ++u) {
+        const int q = c0 + CH + tid + u * TOPK_THREADS;
+        nx[u] = q < e4 ? __ldcs(x4 + q) : ninf;
+      }
+      if (c0 == b4) {
+        // threshold: the KK-th largest of the CTA's lane maxima over the first chunk; KK
+        // distinct elements lie at or above it, so nothing below reaches the CTA's top-KK
+        uint32_t km = 0u;
+#pragma unroll
+        for (int u = 0; u < TOPK_PER; ++u)
+          if (c0 + tid + u * TOPK_THREADS < e4)
+            km = max(km, max(max(order_key(a[u].x), order_key(a[u].y)),
+                             max(order_key(a[u].z), order_key(a[u].w))));
+        const uint32_t sorted = warp_sorted_desc(km);
+        if (lane < KK) s_lmax[warp * KK + lane] = sorted;
+        __syncthreads();
+        if (warp == 0) {
+          constexpr int NC = (NW * KK + 31) / 32;
+          uint32_t v = 0u;
+          // each lane keeps the max of its NC values, then the KK-th largest over lanes is a
+          // lower bound of the KK-th largest of all NW*KK values (each lane's max is one
+          // distinct value)
+#pragma unroll
+          for (int j = 0; j < NC; ++j) {
+            const int q = lane + 32 * j;
+            if (q < NW * KK) v = max(v, s_lmax[q]);
+          }
+          const uint32_t kth = __shfl_sync(0xffffffffu, warp_sorted_desc(v), KK - 1);
+          if (lane == 0) s_thr = kth;
+        }
+        __syncthreads();
+        thr = key_floor(s_thr);
+      }
+#pragma unroll
+      for (int u = 0; u < TOPK_PER; ++u) {
+        const int q = c0 + tid + u * TOPK_THREADS;
+        const float e[4] = {a[u].x, a[u].y, a[u].z, a[u].w};
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          if (q < e4 && !(e[c] < thr)) {
+            const int pos = atomicAdd(&s_cnt, 1);
+            if (pos < TOPK_CAP) s_cand[pos] = pack_key(order_key(e[c]), 4 * q + c);
+          }
+      }
+#pragma unroll
+      for (int u = 0; u < TOPK_PER; ++u) a[u] = nx[u];
+    }
+    __syncthreads();
+    const int cnt = s_cnt;
+    if (cnt > TOPK_CAP) {
+      __syncthreads();  // the buffer is reused as scratch
+      topk_exact<KK>(x, 4 * b4, 4 * e4, s_cand, s_top);
+    } else {
+      if (warp == 0) {
+        uint64_t bb;
+        if (cnt <= 64) {  // the usual case: a few dozen candidates
+          uint64_t c[2] = {lane < cnt ? s_cand[lane] : 0ull,
+                           lane + 32 < cnt ? s_cand[lane + 32] : 0ull};
+          bb = warp_select<KK, 2>(c);
+        } else {
+          constexpr int NC = TOPK_CAP / 32;
+          uint64_t c[NC];
+#pragma unroll
+          for (int j = 0; j < NC; ++j) {
+            const int q = lane + 32 * j;
+            c[j] = q < cnt ? s_cand[q] : 0ull;
+          }
+          bb = warp_select<KK, NC>(c);
+        }
+        if (lane < KK) s_top[lane] = bb;
+      }
+      __syncthreads();
     }
   } else {
     const int b = (int)((long long)V * crank / CL), e = (int)((long long)V * (crank + 1) / CL);
-    for (int i = b + tid; i < e; i += TOPK_THREADS) consider<KK>(key, idx, __ldcs(x + i), i);
+    topk_exact<KK>(x, b, e, s_cand, s_top);
   }
 
-  // warp -> CTA
-  const int lane = tid & 31, warp = tid >> 5;
-  const uint64_t wbest = warp_merge_lists<KK>(key, idx);
-  if (lane < KK) s_warp[warp * KK + lane] = wbest;
-  __syncthreads();
+  // CTA -> cluster leader
   asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
-  if (warp == 0) {
-    constexpr int NC = (NW * KK + 31) / 32;
-    uint64_t c[NC];
-#pragma unroll
-    for (int j = 0; j < NC; ++j) {
-      const int q = lane + 32 * j;
-      c[j] = q < NW * KK ? s_warp[q] : 0ull;
-    }
-    const uint64_t cbest = warp_merge_cands<KK, NC>(c);
+  if (warp == 0 && lane < KK) {
     uint64_t *leader = cluster.map_shared_rank(s_clus, 0);
-    if (lane < KK) leader[crank * KK + lane] = cbest;
+    leader[crank * KK + lane] = s_top[lane];
   }
   cluster.sync();
   if (crank == 0 && warp == 0) {
@@ -199,11 +307,15 @@ topk_cluster_kernel(const float *__restrict__ logits, int row0, int V, int k,
       const int q = lane + 32 * j;
       c[j] = q < CL * KK ? s_clus[q] : 0ull;
     }
-    const uint64_t best = warp_merge_cands<KK, NC>(c);
+    const uint64_t best = warp_select<KK, NC>(c);
     if (lane < k) {
       const int id = best ? unpack_idx(best) : -1;
+      const uint32_t kb = (uint32_t)(best >> 32);
       ids[(size_t)row * k + lane] = id;
-      vals[(size_t)row * k + lane] = id >= 0 ? x[id] : __int_as_float(0x7fc00000);
+      // the order key gives the value back exactly, except for the sign of a zero and the
+      // payload of a NaN: those few are read from the row
+      vals[(size_t)row * k + lane] = id < 0 ? __int_as_float(0x7fc00000)
+                                     : (kb == 0x80000000u || kb == 1u) ? x[id] : key_floor(kb);
     }
   }
 }
