@@ -28,7 +28,7 @@ from workload import CONFIGS, make_scenario  # noqa: E402
 
 DEFAULT_CONFIG = 3   # the long-context workload (32K prefix) on which the HBM bar is stated
 METRIC = "verify-and-graft steps/s on 1 GB300; tree-attn HBM GB/s as % of ~8 TB/s roofline"
-KERNELS_PER_STEP = {True: 9, False: 8}  # with / without the graft launch
+KERNELS_PER_STEP = 5  # tree build, attention + combine, top-k, walk + table update
 L2_BYTES = 129 * 2 ** 20
 
 
@@ -207,9 +207,9 @@ def run_reference(args, rank: int, world: int):
 def run_gpu(args, rank: int, world: int, local_rank: int):
     import torch
     from tree_speculative_decoding_parent_gb300 import build, gt
-    from tree_speculative_decoding_parent_gb300.step import (StepBuffers, StepShape,
-                                                             run_step, run_tree_phase,
-                                                             run_verify_phase)
+    from tree_speculative_decoding_parent_gb300.step import (StepBuffers, StepShape, run_attn,
+                                                             run_step, run_tree_build,
+                                                             run_tree_phase, run_verify_commit)
     build.build()
     gt.load()
     dev = torch.device("cuda", local_rank)
@@ -262,23 +262,15 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
             s = torch.cuda.current_stream()
             for i in range(nsteps):
                 inp = sets[i % nsets]
-                run_tree_phase(buf, inp, s)
+                run_tree_build(buf, inp, s)
                 if with_events:
                     e0, e1 = ev_pool[2 * i], ev_pool[2 * i + 1]
                     gt.gt_event_record_external(e0, s)
-                sh = buf.shape
-                gt.gt_tree_attn(inp["Q"], inp["K"], inp["V"], buf.mask, inp["prefix_len"],
-                                buf.n_nodes, sh.B, sh.N, sh.Hq, sh.Hkv, sh.d, sh.Lcap, sh.dtype,
-                                scn.scale, buf.O, buf.ws, buf.ws_bytes, buf.err, s)
+                run_attn(buf, inp, s, scn.scale)
                 if with_events:
                     gt.gt_event_record_external(e1, s)
                     evs.append((e0, e1))
-                gt.gt_verify_greedy(inp["logits"], buf.tokens, buf.parent, buf.n_nodes,
-                                    inp["prefix_len"], sh.B, sh.N, sh.V, sh.k, buf.topk_id,
-                                    buf.topk_val, buf.acc_len, buf.path, buf.out_tok,
-                                    buf.kv_src, buf.kv_dst, buf.err, s)
-                gt.gt_succ_update(inp["table"], sh.V, sh.k, buf.tokens, buf.topk_id,
-                                  buf.n_nodes, sh.B, sh.N, buf.err, s)
+                run_verify_commit(buf, inp, s)
         return g, evs
 
     # torch creates CUDA events lazily: record each once before capture so it exists
@@ -397,7 +389,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
                      "traffic": _traffic_record(f"tree_attn/config{args.config}")},
         "e2e": {"value": world * ne / e2e_s, "unit": "steps/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * KERNELS_PER_STEP[len(scn.tpar) > 0],
+        "gpu_launches": args.steps * KERNELS_PER_STEP,
         "clocks": clocks,
         "accepted_len_mean": float(buf.acc_len.float().mean().item()),
     }
@@ -414,10 +406,11 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
 
 def call_breakdown(torch, gt, buf, sets, scn, nsets, reps: int = 50):
     """Average device time of each C-ABI call of the step inside a CUDA graph: one graph
-    per input set with an externally visible event between consecutive calls."""
-    names = ["gt_prune_topB", "gt_graft_expand", "gt_tree_mask", "gt_tree_attn",
-             "gt_verify_greedy", "gt_succ_update"]
-    sh = buf.shape
+    per input set with an externally visible event between consecutive calls (the events
+    also end the programmatic overlap between the calls, so the sum exceeds the step)."""
+    from tree_speculative_decoding_parent_gb300.step import (run_attn, run_tree_build,
+                                                             run_verify_commit)
+    names = ["gt_tree_build", "gt_tree_attn", "gt_verify_commit"]
     graphs = []
     for k in range(nsets):
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
@@ -429,30 +422,12 @@ def call_breakdown(torch, gt, buf, sets, scn, nsets, reps: int = 50):
         with torch.cuda.graph(g):
             s = torch.cuda.current_stream()
             gt.gt_event_record_external(evs[0], s)
-            gt.gt_prune_topB(inp["score_in"], inp["parent_in"], inp["tokens_in"], None, sh.B, sh.Nin,
-                             inp["keep"], inp.get("thresh"), sh.N, buf.parent, buf.tokens, buf.score,
-                             buf.old_idx, buf.n_nodes, buf.err, s)
+            run_tree_build(buf, inp, s)
             gt.gt_event_record_external(evs[1], s)
-            if sh.T > 0:
-                gt.gt_graft_expand(buf.parent, buf.tokens, buf.n_nodes, sh.B, sh.N, inp["tpar"],
-                                   inp["trank"], sh.T, inp["R"], inp["table"], sh.V, sh.k, buf.err,
-                                   s)
+            run_attn(buf, inp, s, scn.scale)
             gt.gt_event_record_external(evs[2], s)
-            gt.gt_tree_mask(buf.parent, buf.n_nodes, inp["prefix_len"], sh.B, sh.N, buf.depth,
-                            buf.pos, buf.mask, buf.err, s)
+            run_verify_commit(buf, inp, s)
             gt.gt_event_record_external(evs[3], s)
-            gt.gt_tree_attn(inp["Q"], inp["K"], inp["V"], buf.mask, inp["prefix_len"],
-                            buf.n_nodes, sh.B, sh.N, sh.Hq, sh.Hkv, sh.d, sh.Lcap, sh.dtype,
-                            scn.scale, buf.O, buf.ws, buf.ws_bytes, buf.err, s)
-            gt.gt_event_record_external(evs[4], s)
-            gt.gt_verify_greedy(inp["logits"], buf.tokens, buf.parent, buf.n_nodes,
-                                inp["prefix_len"], sh.B, sh.N, sh.V, sh.k, buf.topk_id,
-                                buf.topk_val, buf.acc_len, buf.path, buf.out_tok, buf.kv_src,
-                                buf.kv_dst, buf.err, s)
-            gt.gt_event_record_external(evs[5], s)
-            gt.gt_succ_update(inp["table"], sh.V, sh.k, buf.tokens, buf.topk_id, buf.n_nodes,
-                              sh.B, sh.N, buf.err, s)
-            gt.gt_event_record_external(evs[6], s)
         graphs.append((g, evs))
     tot = [0.0] * len(names)
     for r in range(reps):

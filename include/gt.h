@@ -198,6 +198,33 @@ int gt_succ_update(int32_t *table, int V, int k, const int32_t *tokens,
                    int32_t *err, gt_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
+ * Fused forms of the step (same results and device error codes as the calls they stand
+ * for, fewer launches and global-memory round trips).
+ *
+ * gt_tree_build = gt_prune_topB (Nout = N) -> gt_graft_expand (Nmax = N) -> gt_tree_mask,
+ *   one CTA per request holding the tree in shared memory. [TreeGraft] §三, §四 How;
+ *   [Graft] §二, §四. Outputs: parent, tokens i32 [B][N] (final tree, -1 padded);
+ *   out_score f32 / out_old_idx i32 [B][N] (kept nodes, nullable); n_nodes i32 [B] (final
+ *   count); depth, pos i32 [B][N]; mask u64 [B][N][ceil(N/64)].
+ *   Limits: 1 <= Nin, N <= 1024, 0 <= T <= 1024.
+ * gt_verify_commit = gt_verify_greedy -> gt_succ_update on `table` i32 [V][k] (in place).
+ *   [Graft] §二 (third gear), §六; [TreeGraft] §一, §三. Limits: N <= 1024, k <= 16,
+ *   B*N <= 16384.
+ * ------------------------------------------------------------------------------------- */
+int gt_tree_build(const float *score, const int32_t *parent_in, const int32_t *tokens_in,
+                  const int32_t *n_in, int B, int Nin, const int32_t *keep, const float *thresh,
+                  const int32_t *tpar, const int32_t *trank, int T, const int32_t *R,
+                  const int32_t *table, int V, int k, const int32_t *prefix_len, int N,
+                  int32_t *parent, int32_t *tokens, float *out_score, int32_t *out_old_idx,
+                  int32_t *n_nodes, int32_t *depth, int32_t *pos, uint64_t *mask, int32_t *err,
+                  gt_stream_t stream);
+int gt_verify_commit(const float *logits, const int32_t *tokens, const int32_t *parent,
+                     const int32_t *n_nodes, const int32_t *prefix_len, int B, int N, int V,
+                     int k, int32_t *topk_id, float *topk_val, int32_t *acc_len, int32_t *path,
+                     int32_t *out_tok, int32_t *kv_src, int32_t *kv_dst, int32_t *table,
+                     int32_t *err, gt_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
  * Host helpers (host pointers, synchronous, no CUDA calls).
  *
  * gt_stage_budget: draft / retrieved split of `slots` for a prune at stage 0, 1 or 5

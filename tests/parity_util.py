@@ -56,10 +56,10 @@ def oracle_attn(scn, tree: dict, b: int) -> np.ndarray:
                             scn.scale)
 
 
-def run_gpu_step(scn, logits: np.ndarray):
+def run_gpu_step(scn, logits: np.ndarray, fused: bool = True):
     buf = StepBuffers(shape_of(scn))
     inp = device_inputs(scn, logits)
-    run_step(buf, inp, scale=scn.scale)
+    run_step(buf, inp, scale=scn.scale, fused=fused)
     torch.cuda.synchronize()
     return buf, inp
 

@@ -25,10 +25,10 @@ SMALL = {
 }
 
 
-def _full_check(scn, reqs=None):
+def _full_check(scn, reqs=None, fused=True):
     tree = oracle_tree(scn)
     logits = scn.logits(tree["parent"], tree["tokens"], tree["n_nodes"])
-    buf, inp = run_gpu_step(scn, logits)
+    buf, inp = run_gpu_step(scn, logits, fused=fused)
     assert int(buf.err.item()) == 0
     compare_tree(buf, tree)
     res = oracle.step_verify_phase(tree, logits, scn.table, scn.prefix_len, scn.k)
@@ -38,9 +38,10 @@ def _full_check(scn, reqs=None):
     return buf, tree
 
 
+@pytest.mark.parametrize("fused", [True, False], ids=["fused", "separate"])
 @pytest.mark.parametrize("cid", [1, 2, 3, 4, 5])
-def test_step_parity_small(cid):
-    _full_check(make_scenario(cid, **SMALL[cid]))
+def test_step_parity_small(cid, fused):
+    _full_check(make_scenario(cid, **SMALL[cid]), fused=fused)
 
 
 def test_step_parity_nan_kv_tail_and_zero_prefix():
@@ -192,16 +193,18 @@ def test_device_errors_are_reported():
     scn = make_scenario(1, V=3000, P=64)
     tree = oracle_tree(scn)
     logits = scn.logits(tree["parent"], tree["tokens"], tree["n_nodes"])
-    # a node whose score exceeds its parent's
-    bad = make_scenario(1, V=3000, P=64)
-    bad.score_in[0, 200] = 2.0
-    buf, _ = run_gpu_step(bad, logits)
-    assert buf.err.item() == gt.GT_ERR_NONMONOTONE
-    # a parent index that is not smaller than the child's
-    bad = make_scenario(1, V=3000, P=64)
-    bad.parent_in[0, 17] = 300
-    buf, _ = run_gpu_step(bad, logits)
-    assert buf.err.item() == gt.GT_ERR_TREE
+    for fused in (True, False):
+        # a node whose score exceeds its parent's
+        bad = make_scenario(1, V=3000, P=64)
+        bad.score_in[0, 200] = 2.0
+        buf, _ = run_gpu_step(bad, logits, fused=fused)
+        assert buf.err.item() == gt.GT_ERR_NONMONOTONE
+        assert buf.n_nodes.item() == 0 and (np_(buf.parent) == -1).all()
+        # a parent index that is not smaller than the child's
+        bad = make_scenario(1, V=3000, P=64)
+        bad.parent_in[0, 17] = 300
+        buf, _ = run_gpu_step(bad, logits, fused=fused)
+        assert buf.err.item() == gt.GT_ERR_TREE
     # a prefix that does not fit in the cache
     buf = StepBuffers(shape_of(scn))
     inp = device_inputs(scn, logits)

@@ -41,6 +41,7 @@ attn_simt_kernel(const T *__restrict__ Q, const T *__restrict__ K, const T *__re
                  const uint64_t *__restrict__ mask, const int32_t *__restrict__ prefix_len,
                  const int32_t *__restrict__ n_nodes, int N, int Hq, int Hkv, int Lcap,
                  float scale, SchedArgs sa, AttnWs ws, int32_t *err) {
+  pdl_enter();
   extern __shared__ float sm[];
   float *Qs = sm;                              // [d][SIMT_LD] (rows)
   float *Ks = Qs + ATTN_D * SIMT_LD;           // [d][SIMT_LD] (keys)
@@ -207,6 +208,7 @@ template <typename T>
 __global__ void __launch_bounds__(256)
 attn_combine_kernel(const int32_t *__restrict__ n_nodes, int B, int N, int Hq, int Hkv,
                     AttnWs ws, T *__restrict__ O) {
+  pdl_enter();
   const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (w >= B * N * Hq) return;
   const int hq = w % Hq, i = (w / Hq) % N, b = w / (Hq * N);

@@ -101,6 +101,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
                const __grid_constant__ CUtensorMap mapV, const uint64_t *__restrict__ mask,
                const int32_t *__restrict__ prefix_len, const int32_t *__restrict__ n_nodes,
                int N, int Hq, int Hkv, float scale, SchedArgs sa, AttnWs ws, int32_t *err) {
+  pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t tmem_sh;
   __shared__ int abort_sh;

@@ -17,6 +17,16 @@ __device__ __forceinline__ void set_err(int32_t *err, int code) {
 
 __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// Programmatic dependent launch. Every libgt kernel is launched with programmatic stream
+// serialisation: it lets the next kernel of the stream start launching at once, then waits
+// until all earlier work of the stream has completed and its memory is visible. Called
+// before a kernel's first global-memory access, it keeps stream order for every read and
+// write while the launch latency of consecutive kernels overlaps.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Records a host-side failure detail for gt_last_error() (thread-local).
 void note_error(const char *what, cudaError_t e);
 

@@ -1,5 +1,5 @@
-// Kernel launch helper: cudaLaunchKernelEx with optional cluster shape, so every launch
-// returns its own error code and can carry launch attributes.
+// Kernel launch helper: cudaLaunchKernelEx with programmatic stream serialisation (see
+// pdl_enter) and an optional cluster shape; every launch returns its own error code.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -16,8 +16,11 @@ static int launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cu
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cfg.attrs = nullptr;
-  cfg.numAttrs = 0;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   return launch_status(cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...), "cudaLaunchKernelEx");
 }
 
@@ -29,13 +32,15 @@ static int launch_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, dim3 cl
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cluster.x;
   attr[0].val.clusterDim.y = cluster.y;
   attr[0].val.clusterDim.z = cluster.z;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return launch_status(cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...), "cudaLaunchKernelEx");
 }
 

@@ -1,0 +1,242 @@
+// a1 + a2 + a3 fused: prune, graft and mask of one request in one CTA.
+//
+// The same computation as gt_prune_topB (with Nout = N) -> gt_graft_expand (Nmax = N) ->
+// gt_tree_mask, with identical outputs and error codes, but the tree stays in shared
+// memory between the three phases: one launch and one round trip to global memory for the
+// inputs instead of three launches and a chain of dependent reads and writes.
+//
+// Sources: "TreeGraft 精读：多起草器共嫁接一棵草稿树，让投机解码跨越快与好的单选题" §三, §四 How
+// (cumulative path score, global prune to Bver); "浙江大学、阿里巴巴联手破解AI推理瓶颈" §二
+// (successor-table retrieval by a template into the freed slots; flatten, tree position ids
+// and mask) and §四 (static slot count per request in batched serving).
+#include <math.h>
+
+#include "gt_internal.cuh"
+#include "launch.cuh"
+
+namespace gt {
+
+__global__ void __launch_bounds__(1024)
+tree_build_kernel(const float *__restrict__ score, const int32_t *__restrict__ parent_in,
+                  const int32_t *__restrict__ tokens_in, const int32_t *__restrict__ n_in,
+                  int Nin, const int32_t *__restrict__ keep, const float *__restrict__ thresh,
+                  const int32_t *__restrict__ tpar, const int32_t *__restrict__ trank, int T,
+                  const int32_t *__restrict__ R, const int32_t *__restrict__ table, int V, int k,
+                  const int32_t *__restrict__ prefix_len, int N, int W,
+                  int32_t *__restrict__ parent, int32_t *__restrict__ tokens,
+                  float *__restrict__ out_score, int32_t *__restrict__ out_old,
+                  int32_t *__restrict__ n_nodes, int32_t *__restrict__ depth,
+                  int32_t *__restrict__ pos, uint64_t *__restrict__ mask, int32_t *err) {
+  pdl_enter();
+  extern __shared__ int s_dyn[];
+  const int Nin4 = (Nin + 3) & ~3;
+  float *s_score = reinterpret_cast<float *>(s_dyn);  // [Nin4]
+  int *s_new = s_dyn + Nin4;                          // [Nin]
+  int *s_par = s_new + Nin;                           // [N] tree being built
+  int *s_tok = s_par + N;                             // [N]
+  const int Tb = T > 0 ? T : 1;
+  int *s_tpar = s_tok + N;                            // [Tb]
+  int *s_ttok = s_tpar + Tb;                          // [Tb]
+  int *s_tnew = s_ttok + Tb;                          // [Tb]
+  __shared__ int warp_tot[32];
+  __shared__ int s_bad, s_maxd, s_n;
+  const int b = blockIdx.x, t = threadIdx.x;
+  const size_t in0 = (size_t)b * Nin, row0 = (size_t)b * N;
+  const int n = n_in ? n_in[b] : Nin;
+  const int kb = keep[b];
+  const int P = prefix_len[b];
+  if (t == 0) {
+    s_bad = 0;
+    s_maxd = 0;
+  }
+
+  // ---------------------------------------------------------------- phase A: prune
+  int code = (n < 1 || n > Nin) ? GT_ERR_RANGE : 0;
+  int p = -1;
+  float s = 0.f;
+  if (!code && t < n) {
+    p = parent_in[in0 + t];
+    s = score[in0 + t];
+    s_score[t] = s;
+  }
+  __syncthreads();
+  if (!code && t < n) {
+    if (t == 0) {
+      if (p != -1) code = GT_ERR_TREE;
+    } else if (p < 0 || p >= t) {
+      code = GT_ERR_TREE;
+    } else {
+      const float ps = (p == 0) ? INFINITY : s_score[p];
+      if (!(s <= ps)) code = GT_ERR_NONMONOTONE;
+    }
+  }
+  const int ke = min(kb, n);
+  if (!code && (kb < 1 || ke > N)) code = GT_ERR_RANGE;
+  if (code) atomicCAS(&s_bad, 0, code);
+  __syncthreads();
+  const int bad = s_bad;
+  if (bad) {  // as the separate calls: nothing kept, every row padded
+    if (t == 0) {
+      set_err(err, bad);
+      n_nodes[b] = 0;
+    }
+    for (int j = t; j < N; j += blockDim.x) {
+      parent[row0 + j] = tokens[row0 + j] = -1;
+      if (out_score) out_score[row0 + j] = 0.f;
+      if (out_old) out_old[row0 + j] = -1;
+      depth[row0 + j] = pos[row0 + j] = -1;
+      for (int w = 0; w < W; ++w) mask[(row0 + j) * W + w] = 0ull;
+    }
+    return;
+  }
+  const float th = thresh ? thresh[b] : -INFINITY;
+  if (t == 0) s_score[0] = __int_as_float(0x7fc00000);  // the root never ranks
+  for (int u = n + t; u < Nin4; u += blockDim.x) s_score[u] = __int_as_float(0x7fc00000);
+  __syncthreads();
+  bool kept = (t == 0);
+  if (t > 0 && t < n && s >= th) {
+    const float4 *s4 = reinterpret_cast<const float4 *>(s_score);
+    int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+#pragma unroll 4
+    for (int q = 0; q < (n + 3) >> 2; ++q) {
+      const float4 x = s4[q];
+      const int u = 4 * q;
+      r0 += (x.x >= th) & ((x.x > s) | ((x.x == s) & (u < t)));
+      r1 += (x.y >= th) & ((x.y > s) | ((x.y == s) & (u + 1 < t)));
+      r2 += (x.z >= th) & ((x.z > s) | ((x.z == s) & (u + 2 < t)));
+      r3 += (x.w >= th) & ((x.w > s) | ((x.w == s) & (u + 3 < t)));
+    }
+    kept = (r0 + r1) + (r2 + r3) < ke - 1;
+  }
+  int nk;
+  const int newi = block_excl_count(kept, warp_tot, &nk);
+  if (t < n) s_new[t] = kept ? newi : -1;
+  __syncthreads();
+  if (kept) {
+    s_par[newi] = (t == 0) ? -1 : s_new[p];
+    s_tok[newi] = tokens_in[in0 + t];
+    if (out_score) out_score[row0 + newi] = s;
+    if (out_old) out_old[row0 + newi] = t;
+  }
+  for (int j = nk + t; j < N; j += blockDim.x) {
+    if (out_score) out_score[row0 + j] = 0.f;
+    if (out_old) out_old[row0 + j] = -1;
+  }
+  __syncthreads();
+
+  // ---------------------------------------------------------------- phase B: graft
+  const int root_tok = s_tok[0];
+  code = (root_tok < 0 || root_tok >= V) ? GT_ERR_TREE : 0;
+  const int r = code ? 0 : max(0, min(min(R[b], N - nk), T));
+  const bool active = t < r;
+  int tp = -1, rk = 0;
+  if (active) {
+    tp = tpar[t];
+    rk = trank[t];
+    if (tp < -1 || tp >= t || rk < 0 || rk >= k) code = GT_ERR_TREE;
+    s_tpar[t] = tp;
+  }
+  if (code) atomicCAS(&s_bad, 0, code);
+  __syncthreads();
+  int n_final = nk;
+  if (s_bad) {  // the kept tree stays; no graft
+    if (t == 0) set_err(err, s_bad);
+  } else {
+    int dep = 0;
+    if (active) {
+      for (int u = t; u != -1; u = s_tpar[u]) ++dep;
+      atomicMax(&s_maxd, dep);
+    }
+    __syncthreads();
+    const int maxd = s_maxd;
+    for (int L = 1; L <= maxd; ++L) {
+      if (active && dep == L) {
+        const int ptok = (tp == -1) ? root_tok : s_ttok[tp];
+        int tok = -1;
+        if (ptok >= 0) {
+          tok = table[(size_t)ptok * k + rk];
+          if (tok < -1 || tok >= V) {
+            set_err(err, GT_ERR_TREE);
+            tok = -1;
+          }
+        }
+        s_ttok[t] = tok;
+      }
+      __syncthreads();
+    }
+    const bool alive = active && s_ttok[t] >= 0;
+    int cnt;
+    const int gi = block_excl_count(alive, warp_tot, &cnt);
+    if (active) s_tnew[t] = gi;
+    __syncthreads();
+    if (alive) {
+      s_par[nk + gi] = (tp == -1) ? 0 : nk + s_tnew[tp];
+      s_tok[nk + gi] = s_ttok[t];
+    }
+    n_final = nk + cnt;
+  }
+  if (t == 0) s_n = n_final;
+  __syncthreads();
+
+  // ---------------------------------------------------------------- phase C: mask
+  const int nf = s_n;
+  for (int v = t; v < N; v += blockDim.x) {
+    const size_t o = row0 + v;
+    uint64_t *mrow = mask + o * W;
+    if (v >= nf) {
+      parent[o] = tokens[o] = -1;
+      depth[o] = pos[o] = -1;
+      for (int w = 0; w < W; ++w) mrow[w] = 0ull;
+      continue;
+    }
+    parent[o] = s_par[v];
+    tokens[o] = s_tok[v];
+    int d = 0, cur = v >> 6;
+    uint64_t word = 0ull;
+    for (int w = W - 1; w > cur; --w) mrow[w] = 0ull;
+    for (int u = v;; u = s_par[u]) {
+      const int wu = u >> 6;
+      while (wu < cur) {
+        mrow[cur] = word;
+        word = 0ull;
+        --cur;
+      }
+      word |= 1ull << (u & 63);
+      if (u == 0) break;
+      ++d;
+    }
+    mrow[cur] = word;
+    for (int w = cur - 1; w >= 0; --w) mrow[w] = 0ull;
+    depth[o] = d;
+    pos[o] = P + d;
+  }
+  if (t == 0) n_nodes[b] = nf;
+}
+
+}  // namespace gt
+
+using namespace gt;
+
+GT_API int gt_tree_build(const float *score, const int32_t *parent_in, const int32_t *tokens_in,
+                         const int32_t *n_in, int B, int Nin, const int32_t *keep,
+                         const float *thresh, const int32_t *tpar, const int32_t *trank, int T,
+                         const int32_t *R, const int32_t *table, int V, int k,
+                         const int32_t *prefix_len, int N, int32_t *parent, int32_t *tokens,
+                         float *out_score, int32_t *out_old_idx, int32_t *n_nodes,
+                         int32_t *depth, int32_t *pos, uint64_t *mask, int32_t *err,
+                         gt_stream_t stream) {
+  if (B < 0 || Nin < 1 || N < 1 || T < 0 || V < 1 || k < 1) return GT_ERR_ARG;
+  if (Nin > 1024 || N > 1024 || T > 1024) return GT_ERR_SHAPE;
+  if (B == 0) return GT_OK;
+  if (!score || !parent_in || !tokens_in || !keep || !R || !table || !prefix_len || !parent ||
+      !tokens || !n_nodes || !depth || !pos || !mask || (T > 0 && (!tpar || !trank)))
+    return GT_ERR_ARG;
+  const int W = (N + 63) / 64;
+  const int Tb = T > 0 ? T : 1;
+  const int threads = (max(max(Nin, N), Tb) + 31) / 32 * 32;
+  const size_t smem = sizeof(int) * ((size_t)((Nin + 3) & ~3) + Nin + 2 * (size_t)N + 3 * (size_t)Tb);
+  return launch(tree_build_kernel, dim3(B), dim3(threads), smem, (cudaStream_t)stream, score,
+                parent_in, tokens_in, n_in, Nin, keep, thresh, tpar, trank, T, R, table, V, k,
+                prefix_len, N, W, parent, tokens, out_score, out_old_idx, n_nodes, depth, pos,
+                mask, err);
+}

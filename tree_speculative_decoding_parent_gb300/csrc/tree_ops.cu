@@ -28,6 +28,7 @@ prune_kernel(const float *__restrict__ score, const int32_t *__restrict__ parent
              int32_t *__restrict__ out_parent, int32_t *__restrict__ out_tokens,
              float *__restrict__ out_score, int32_t *__restrict__ out_old,
              int32_t *__restrict__ n_out, int32_t *err) {
+  pdl_enter();
   extern __shared__ float s_score[];           // [Nin4] (NaN-padded), then s_new [Nin]
   const int Nin4 = (Nin + 3) & ~3;
   int *s_new = reinterpret_cast<int *>(s_score + Nin4);  // [Nin]
@@ -125,6 +126,7 @@ graft_kernel(int32_t *__restrict__ parent, int32_t *__restrict__ tokens,
              int32_t *__restrict__ n_nodes, int Nmax, const int32_t *__restrict__ tpar,
              const int32_t *__restrict__ trank, int T, const int32_t *__restrict__ R,
              const int32_t *__restrict__ table, int V, int k, int32_t *err) {
+  pdl_enter();
   extern __shared__ int s_i32[];
   int *s_par = s_i32;           // [T]
   int *s_tok = s_i32 + T;       // [T]
@@ -205,6 +207,7 @@ __global__ void __launch_bounds__(1024)
 mask_kernel(const int32_t *__restrict__ parent, const int32_t *__restrict__ n_nodes,
             const int32_t *__restrict__ prefix_len, int N, int W, int32_t *__restrict__ depth,
             int32_t *__restrict__ pos, uint64_t *__restrict__ mask, int32_t *err) {
+  pdl_enter();
   extern __shared__ int s_par[];  // [N]
   __shared__ int s_bad;
   const int b = blockIdx.x, v = threadIdx.x;

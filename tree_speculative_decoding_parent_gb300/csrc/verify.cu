@@ -179,6 +179,7 @@ template <int KK, int CL>
 __global__ void __launch_bounds__(TOPK_THREADS)
 topk_cluster_kernel(const float *__restrict__ logits, int row0, int V, int k,
                     int32_t *__restrict__ ids, float *__restrict__ vals) {
+  pdl_enter();
   constexpr int NW = TOPK_THREADS / 32;
   constexpr int CH = TOPK_PER * TOPK_THREADS;  // float4 per chunk of the CTA
   __shared__ uint64_t s_cand[TOPK_CAP];        // candidates, then scratch of the merges
@@ -349,6 +350,7 @@ walk_kernel(const int32_t *__restrict__ tokens, const int32_t *__restrict__ pare
             int k, const int32_t *__restrict__ topk_id, int32_t *__restrict__ acc_len,
             int32_t *__restrict__ path, int32_t *__restrict__ out_tok,
             int32_t *__restrict__ kv_src, int32_t *__restrict__ kv_dst, int32_t *err) {
+  pdl_enter();
   extern __shared__ int s_w[];
   int *s_par = s_w, *s_tok = s_w + N, *s_am = s_w + 2 * N, *s_path = s_w + 3 * N;
   __shared__ uint32_t s_best[32];
@@ -421,6 +423,7 @@ __global__ void __launch_bounds__(256)
 update_kernel(int32_t *__restrict__ table, int V, int k, const int32_t *__restrict__ tokens,
               const int32_t *__restrict__ topk_id, const int32_t *__restrict__ n_nodes, int N,
               int total, int32_t *err) {
+  pdl_enter();
   extern __shared__ int s_tok[];  // [total]
   for (int i = threadIdx.x; i < total; i += blockDim.x) {
     const int b = i / N, v = i - b * N;
@@ -447,6 +450,117 @@ update_kernel(int32_t *__restrict__ table, int V, int k, const int32_t *__restri
   const int32_t *src = topk_id + (size_t)i * k;
   int32_t *dst = table + (size_t)t * k;
   for (int c = 0; c < k; ++c) dst[c] = src[c];
+}
+
+// ------------------------------------------------------------------------------------
+// a6 + a7 fused: CTA b walks request b's tree (as walk_kernel) and then writes the table
+// rows its verified nodes win (as update_kernel: the largest linear index b*N + v of a
+// token wins). Every CTA stages the tokens of all requests in shared memory for that test.
+// ------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024)
+walk_update_kernel(const int32_t *__restrict__ tokens, const int32_t *__restrict__ parent,
+                   const int32_t *__restrict__ n_nodes, const int32_t *__restrict__ prefix_len,
+                   int B, int N, int k, const int32_t *__restrict__ topk_id,
+                   int32_t *__restrict__ acc_len, int32_t *__restrict__ path,
+                   int32_t *__restrict__ out_tok, int32_t *__restrict__ kv_src,
+                   int32_t *__restrict__ kv_dst, int32_t *__restrict__ table, int V,
+                   int32_t *err) {
+  pdl_enter();
+  extern __shared__ int s_w[];
+  int *s_par = s_w, *s_tok = s_w + N, *s_am = s_w + 2 * N, *s_path = s_w + 3 * N;
+  int *s_all = s_w + 4 * N;  // [B*N] verified tokens of every request (-1: none)
+  __shared__ uint32_t s_best[32];
+  __shared__ int s_bad;
+  const int b = blockIdx.x, v = threadIdx.x;
+  const int total = B * N;
+  const size_t row0 = (size_t)b * N;
+  const int n = n_nodes[b], P = prefix_len[b];
+  if (v == 0) s_bad = 0;
+  for (int i = v; i < total; i += blockDim.x) {
+    const int bb = i / N, vv = i - bb * N;
+    const int nn = n_nodes[bb];
+    int t = -1;
+    if (nn >= 0 && nn <= N && vv < nn) {
+      t = tokens[i];
+      if (t < 0 || t >= V) {
+        if (bb == b) set_err(err, GT_ERR_TREE);
+        t = -1;
+      }
+    } else if ((nn < 0 || nn > N) && vv == 0 && bb == b) {
+      set_err(err, GT_ERR_RANGE);
+    }
+    s_all[i] = t;
+  }
+  int code = (n < 1 || n > N) ? GT_ERR_RANGE : 0;
+  if (!code && v < n) {
+    const int p = parent[row0 + v];
+    s_par[v] = p;
+    s_tok[v] = tokens[row0 + v];
+    s_am[v] = topk_id[(row0 + v) * k];
+    if (v == 0 ? (p != -1) : (p < 0 || p >= v)) code = GT_ERR_TREE;
+  }
+  __syncthreads();
+  if (code) atomicCAS(&s_bad, 0, code);
+  __syncthreads();
+  const int bad = s_bad;
+  int L = 0, vstar = 0;
+  if (!bad) {
+    uint32_t key = 0u;
+    if (v < n) {
+      bool acc = true;
+      int d = 0;
+      for (int u = v; u != 0; u = s_par[u]) {
+        acc = acc && (s_tok[u] == s_am[s_par[u]]);
+        ++d;
+      }
+      if (acc) key = ((uint32_t)d << 16) | (0xFFFFu - (uint32_t)v);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) key = max(key, __shfl_xor_sync(0xffffffffu, key, o));
+    if ((v & 31) == 0) s_best[v >> 5] = key;
+    __syncthreads();
+    uint32_t best = 0u;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) best = max(best, s_best[w]);
+    L = (int)(best >> 16);
+    vstar = (int)(0xFFFFu - (best & 0xFFFFu));
+    if (v <= L) {
+      int u = vstar;
+      for (int s = 0; s < L - v; ++s) u = s_par[u];
+      s_path[v] = u;
+    }
+    __syncthreads();
+  } else if (v == 0) {
+    set_err(err, bad);
+  }
+  if (v < N) {
+    const bool on = !bad && v <= L;
+    path[row0 + v] = on ? s_path[v] : -1;
+    kv_src[row0 + v] = on ? P + s_path[v] : -1;
+    kv_dst[row0 + v] = on ? P + v : -1;
+  }
+  for (int j = v; j < N + 1; j += blockDim.x) {
+    int t = -1;
+    if (!bad && j < L) t = s_tok[s_path[j + 1]];
+    else if (!bad && j == L) t = s_am[vstar];
+    out_tok[(size_t)b * (N + 1) + j] = t;
+  }
+  if (v == 0) acc_len[b] = bad ? 0 : L;
+  // table rows won by this request's verified nodes
+  for (int vv = v; vv < N; vv += blockDim.x) {
+    const int i = b * N + vv;
+    const int t = s_all[i];
+    if (t < 0) continue;
+    bool last = true;
+    for (int j = i + 1; j < total; ++j)
+      if (s_all[j] == t) {
+        last = false;
+        break;
+      }
+    if (!last) continue;
+    const int32_t *src = topk_id + (size_t)i * k;
+    int32_t *dst = table + (size_t)t * k;
+    for (int c = 0; c < k; ++c) dst[c] = src[c];
+  }
 }
 
 }  // namespace gt
@@ -499,4 +613,30 @@ GT_API int gt_succ_update(int32_t *table, int V, int k, const int32_t *tokens,
   const int blocks = (int)((total + 255) / 256);
   return launch(update_kernel, dim3(blocks), dim3(256), smem, (cudaStream_t)stream, table, V, k,
                 tokens, topk_id, n_nodes, N, (int)total, err);
+}
+
+GT_API int gt_verify_commit(const float *logits, const int32_t *tokens, const int32_t *parent,
+                            const int32_t *n_nodes, const int32_t *prefix_len, int B, int N, int V,
+                            int k, int32_t *topk_id, float *topk_val, int32_t *acc_len,
+                            int32_t *path, int32_t *out_tok, int32_t *kv_src, int32_t *kv_dst,
+                            int32_t *table, int32_t *err, gt_stream_t stream) {
+  if (B < 0 || N < 1 || V < 1 || k < 1) return GT_ERR_ARG;
+  if (N > 1024 || k > 16 || k > V || (long long)B * N > 16384) return GT_ERR_SHAPE;
+  if (B == 0) return GT_OK;
+  if (!logits || !tokens || !parent || !n_nodes || !prefix_len || !topk_id || !topk_val ||
+      !acc_len || !path || !out_tok || !kv_src || !kv_dst || !table)
+    return GT_ERR_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  int rc = topk_launch(logits, B * N, V, k, topk_id, topk_val, s);
+  if (rc != GT_OK) return rc;
+  const int threads = (N + 31) / 32 * 32;
+  const size_t smem = sizeof(int) * (4 * (size_t)N + (size_t)B * N);
+  if (smem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        walk_update_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return launch_status(e, "cudaFuncSetAttribute(walk_update_kernel)");
+  }
+  return launch(walk_update_kernel, dim3(B), dim3(threads), smem, s, tokens, parent, n_nodes,
+                prefix_len, B, N, k, topk_id, acc_len, path, out_tok, kv_src, kv_dst, table, V,
+                err);
 }

@@ -30,6 +30,10 @@ _SIGS = {
     "gt_verify_greedy": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp,
                               _vp, _vp, _vp, _vp]),
     "gt_succ_update": (_i, [_vp, _i, _i, _vp, _vp, _vp, _i, _i, _vp, _vp]),
+    "gt_tree_build": (_i, [_vp, _vp, _vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _i,
+                           _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "gt_verify_commit": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp,
+                              _vp, _vp, _vp, _vp, _vp]),
     "gt_stage_budget": (_i, [_i, _i, _vp, _vp]),
     "gt_default_template": (_i, [_i, _i, _i, _vp, _vp]),
     "gt_status_string": (ctypes.c_char_p, [_i]),
@@ -152,6 +156,24 @@ def gt_verify_greedy(logits, tokens, parent, n_nodes, prefix_len, B, N, V, k, to
 def gt_succ_update(table, V, k, tokens, topk_id, n_nodes, B, N, err, stream=None):
     _check("gt_succ_update", load().gt_succ_update(
         _p(table), V, k, _p(tokens), _p(topk_id), _p(n_nodes), B, N, _p(err), _s(stream)))
+
+
+def gt_tree_build(score, parent_in, tokens_in, n_in, B, Nin, keep, thresh, tpar, trank, T, R,
+                  table, V, k, prefix_len, N, parent, tokens, out_score, out_old_idx, n_nodes,
+                  depth, pos, mask, err, stream=None):
+    _check("gt_tree_build", load().gt_tree_build(
+        _p(score), _p(parent_in), _p(tokens_in), _p(n_in), B, Nin, _p(keep), _p(thresh),
+        _p(tpar), _p(trank), T, _p(R), _p(table), V, k, _p(prefix_len), N, _p(parent),
+        _p(tokens), _p(out_score), _p(out_old_idx), _p(n_nodes), _p(depth), _p(pos), _p(mask),
+        _p(err), _s(stream)))
+
+
+def gt_verify_commit(logits, tokens, parent, n_nodes, prefix_len, B, N, V, k, topk_id, topk_val,
+                     acc_len, path, out_tok, kv_src, kv_dst, table, err, stream=None):
+    _check("gt_verify_commit", load().gt_verify_commit(
+        _p(logits), _p(tokens), _p(parent), _p(n_nodes), _p(prefix_len), B, N, V, k, _p(topk_id),
+        _p(topk_val), _p(acc_len), _p(path), _p(out_tok), _p(kv_src), _p(kv_dst), _p(table),
+        _p(err), _s(stream)))
 
 
 def gt_stage_budget(stage: int, slots: int = 60):

@@ -1,11 +1,14 @@
 """One verify-and-graft step through the C ABI, with its device buffers.
 
 ``StepBuffers`` owns (through torch) every output and scratch buffer of the step for a
-fixed shape; ``run_step`` issues, on one stream and without host synchronisation:
+fixed shape; ``run_step`` issues, on one stream and without host synchronisation, either
+the fused form (default: 5 kernel launches)
+  a1+a2+a3 gt_tree_build -> a4 gt_tree_attn -> a5+a6+a7 gt_verify_commit
+or the separate calls
   a1 gt_prune_topB -> a2 gt_graft_expand (when the template is non-empty)
   -> a3 gt_tree_mask -> a4 gt_tree_attn -> a5+a6 gt_verify_greedy -> a7 gt_succ_update.
-Every step of the computation runs in libgt's kernels; this module only allocates and
-passes pointers.
+Both give identical results. Every step of the computation runs in libgt's kernels; this
+module only allocates and passes pointers.
 """
 from __future__ import annotations
 
@@ -94,7 +97,40 @@ def run_verify_phase(buf: StepBuffers, inp: dict, stream=None, scale=None):
                       buf.err, stream)
 
 
-def run_step(buf: StepBuffers, inp: dict, stream=None, scale=None):
+def run_tree_build(buf: StepBuffers, inp: dict, stream=None):
+    """a1+a2+a3 in one launch."""
+    s = buf.shape
+    gt.gt_tree_build(inp["score_in"], inp["parent_in"], inp["tokens_in"], inp.get("n_in"), s.B,
+                     s.Nin, inp["keep"], inp.get("thresh"), inp.get("tpar"), inp.get("trank"),
+                     s.T, inp["R"], inp["table"], s.V, s.k, inp["prefix_len"], s.N, buf.parent,
+                     buf.tokens, buf.score, buf.old_idx, buf.n_nodes, buf.depth, buf.pos,
+                     buf.mask, buf.err, stream)
+
+
+def run_attn(buf: StepBuffers, inp: dict, stream=None, scale=None):
+    """a4."""
+    s = buf.shape
+    if scale is None:
+        scale = 1.0 / (s.d ** 0.5)
+    gt.gt_tree_attn(inp["Q"], inp["K"], inp["V"], buf.mask, inp["prefix_len"], buf.n_nodes, s.B,
+                    s.N, s.Hq, s.Hkv, s.d, s.Lcap, s.dtype, scale, buf.O, buf.ws, buf.ws_bytes,
+                    buf.err, stream)
+
+
+def run_verify_commit(buf: StepBuffers, inp: dict, stream=None):
+    """a5+a6+a7: top-k launch, then one walk + table-update launch."""
+    s = buf.shape
+    gt.gt_verify_commit(inp["logits"], buf.tokens, buf.parent, buf.n_nodes, inp["prefix_len"],
+                        s.B, s.N, s.V, s.k, buf.topk_id, buf.topk_val, buf.acc_len, buf.path,
+                        buf.out_tok, buf.kv_src, buf.kv_dst, inp["table"], buf.err, stream)
+
+
+def run_step(buf: StepBuffers, inp: dict, stream=None, scale=None, fused: bool = True):
     """The whole verify-and-graft step (a1..a7) on one stream, no host synchronisation."""
-    run_tree_phase(buf, inp, stream)
-    run_verify_phase(buf, inp, stream, scale)
+    if fused:
+        run_tree_build(buf, inp, stream)
+        run_attn(buf, inp, stream, scale)
+        run_verify_commit(buf, inp, stream)
+    else:
+        run_tree_phase(buf, inp, stream)
+        run_verify_phase(buf, inp, stream, scale)
