@@ -149,6 +149,37 @@ int gt_tree_attn(const void *Q, const void *K, const void *V, const uint64_t *ma
                  void *workspace, size_t ws_bytes, int32_t *err, gt_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
+ * a4 without caller scratch.  The pages have no counterpart: this is a convenience of
+ * this library, not a step of the method.
+ *
+ * Same arguments, limits, results and device errors as gt_tree_attn, minus workspace and
+ * ws_bytes. The scratch lives in one static device array of GT_ATTN_NOALLOC_SCRATCH_BYTES
+ * (32 MiB) inside libgt, one copy per device, so the caller allocates nothing.
+ * It is meant for callers that cannot hand over a workspace. One example is a C host
+ * without a device allocator of its own. Another is a serving loop whose memory pool has
+ * been given all of HBM, or that must not call cudaMalloc mid-step, because cudaMalloc
+ * can synchronise the device.
+ *   - Capacity: a shape whose gt_tree_attn_workspace(...) exceeds the array returns
+ *     GT_ERR_SHAPE before anything is launched, with the sizes in gt_last_error(). With
+ *     d = 128 the need is about 4*(SMs + B*Hkv)*ceil((Hq/Hkv)*N / 128)*128*128 bytes:
+ *     e.g. B = 1, Hkv = 8, Hq/Hkv = 4, N = 60 needs about 21 MB and fits.
+ *   - Set-up: the first call on each device (with that device current) looks up the
+ *     array's device address with cudaGetSymbolAddress, which may load the module, and
+ *     caches it. Make that first call before any stream capture. A failed look-up returns
+ *     GT_ERR_CUDA.
+ *   - Sharing: every call on a device uses the same array. Nothing in it needs to start at
+ *     zero; each call writes what it later reads. Calls ordered on one stream are
+ *     safe. Calls that can overlap race on the array and give wrong results: concurrent
+ *     streams, threads or processes sharing the context. Give such callers gt_tree_attn
+ *     with a workspace each.
+ * ------------------------------------------------------------------------------------- */
+#define GT_ATTN_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+int gt_tree_attn_noalloc(const void *Q, const void *K, const void *V, const uint64_t *mask,
+                         const int32_t *prefix_len, const int32_t *n_nodes, int B, int N,
+                         int Hq, int Hkv, int d, int Lcap, int dtype, float scale, void *O,
+                         int32_t *err, gt_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
  * a5. Vocab-wide top-k per row (argmax = column 0).  [Graft] §二 (table rows hold the
  *     target's k most likely next tokens); [TreeGraft] §五 (greedy, temperature 0).
  *

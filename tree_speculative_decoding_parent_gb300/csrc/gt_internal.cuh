@@ -29,6 +29,8 @@ __device__ __forceinline__ void pdl_enter() {
 
 // Records a host-side failure detail for gt_last_error() (thread-local).
 void note_error(const char *what, cudaError_t e);
+// Records a complete host-side message for gt_last_error() (thread-local).
+void note_message(const char *msg);
 
 static inline int launch_status(cudaError_t e, const char *what = "kernel launch") {
   if (e != cudaSuccess) {

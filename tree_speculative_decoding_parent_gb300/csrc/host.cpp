@@ -99,6 +99,7 @@ void note_error(const char *what, cudaError_t e) {
   snprintf(last_error, sizeof(last_error), "%s: %s", what,
            e == cudaSuccess ? "failed" : cudaGetErrorString(e));
 }
+void note_message(const char *msg) { snprintf(last_error, sizeof(last_error), "%s", msg); }
 }  // namespace gt
 
 GT_API const char *gt_last_error(void) { return gt::last_error; }

@@ -16,6 +16,7 @@ LIB_PATH = os.path.join(_HERE, "libgt.so")
 GT_OK, GT_ERR_ARG, GT_ERR_SHAPE, GT_ERR_CUDA = 0, -1, -2, -3
 GT_ERR_TREE, GT_ERR_NONMONOTONE, GT_ERR_TIMEOUT, GT_ERR_RANGE = -4, -5, -6, -7
 GT_F32, GT_BF16 = 0, 1
+GT_ATTN_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024  # size of the static scratch in libgt
 
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 _SIGS = {
@@ -26,6 +27,8 @@ _SIGS = {
     "gt_tree_attn_workspace": (_sz, [_i, _i, _i, _i, _i, _i]),
     "gt_tree_attn": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp,
                           _vp, _sz, _vp, _vp]),
+    "gt_tree_attn_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f,
+                                  _vp, _vp, _vp]),
     "gt_vocab_topk": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp]),
     "gt_verify_greedy": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp,
                               _vp, _vp, _vp, _vp]),
@@ -138,6 +141,13 @@ def gt_tree_attn(Q, K, V, mask, prefix_len, n_nodes, B, N, Hq, Hkv, d, Lcap, dty
     _check("gt_tree_attn", load().gt_tree_attn(
         _p(Q), _p(K), _p(V), _p(mask), _p(prefix_len), _p(n_nodes), B, N, Hq, Hkv, d, Lcap,
         dtype, float(scale), _p(O), _p(workspace), int(ws_bytes), _p(err), _s(stream)))
+
+
+def gt_tree_attn_noalloc(Q, K, V, mask, prefix_len, n_nodes, B, N, Hq, Hkv, d, Lcap, dtype,
+                         scale, O, err, stream=None):
+    _check("gt_tree_attn_noalloc", load().gt_tree_attn_noalloc(
+        _p(Q), _p(K), _p(V), _p(mask), _p(prefix_len), _p(n_nodes), B, N, Hq, Hkv, d, Lcap,
+        dtype, float(scale), _p(O), _p(err), _s(stream)))
 
 
 def gt_vocab_topk(logits, rows, V, k, ids, vals, stream=None):
