@@ -308,9 +308,8 @@ GT_API int gt_tree_attn(const void *Q, const void *K, const void *V, const uint6
 
   const bool tc = (dtype == GT_BF16) && attn_tc_supported(g, N);
   const int TK = tc ? ATTN_TC_KEYS : SIMT_KEYS;
-  // the tcgen05 kernel runs one CTA per SM and one CTA per 256 query rows of a piece:
-  // aim for one wave of CTAs
-  const int Gs = tc ? max(1, G / ceil_div(g * N, 256)) : G;
+  // the tcgen05 kernel runs one cluster per piece: aim for one wave of clusters
+  const int Gs = tc ? attn_tc_pieces(g, N) : G;
   const SchedArgs sa{prefix_len, n_nodes, B, Hkv, N, Lcap, TK, Gs};
   int rc;
   if (tc) {

@@ -60,9 +60,12 @@ struct SchedArgs {
 #ifdef __CUDACC__
 // The split-KV schedule, computed redundantly by every CTA of an attention launch so that
 // no separate scheduling kernel is needed. Segment s = (b, h) has
-// tiles_s = ceil((P_b + n_b) / TK) tiles (0 for an invalid request); with
-// tau = ceil(sum_s tiles_s / G) it gets cnt_s = ceil(tiles_s / tau) pieces of near-equal
-// tile counts, numbered consecutively over s. Returns piece p as (segment, tile_begin,
+// tiles_s = ceil((P_b + n_b) / TK) tiles (0 for an invalid request); with a piece length
+// tau it gets cnt_s = ceil(tiles_s / tau) pieces of near-equal tile counts, numbered
+// consecutively over s. tau starts at ceil(sum_s tiles_s / G); when G exceeds the number
+// of non-empty segments, tau is raised to the smallest value whose pieces all fit in one
+// wave of G (sum_s cnt_s <= G), so that no piece waits for a second wave. Returns piece p
+// as (segment, tile_begin,
 // tile_end, 0), or segment -1 when p is past the last piece. The CTA at blockIdx (0,0)
 // also publishes (first piece, count) of every segment and the piece total into `ws`, and
 // reports invalid requests. Every thread of the CTA must call it (it synchronises).
@@ -83,16 +86,42 @@ __device__ __forceinline__ int4 schedule_piece(const SchedArgs &a, int p, AttnWs
     if (!ok && publisher && (s % a.Hkv) == 0 && err) atomicCAS(err, 0, GT_ERR_RANGE);
     return ok ? (P + n + a.TK - 1) / a.TK : 0;
   };
-  if (tid == 0) s_piece = make_int4(-1, 0, 0, 0);
-  long long local = 0;
-  for (int s = c0; s < c1; ++s) local += tiles_of(s);
+  auto block_sum = [&](long long v) {
 #pragma unroll
-  for (int o = 16; o; o >>= 1) local += __shfl_xor_sync(0xffffffffu, local, o);
-  if (lane == 0) s_red[warp] = local;
-  __syncthreads();
-  long long T = 0;
-  for (int w = 0; w < nw; ++w) T += s_red[w];
-  const int tau = (int)max(1ll, (T + a.G - 1) / a.G);
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    __syncthreads();  // every thread has read s_red from the previous sum
+    if (lane == 0) s_red[warp] = v;
+    __syncthreads();
+    long long t = 0;
+    for (int w = 0; w < nw; ++w) t += s_red[w];
+    return t;
+  };
+  if (tid == 0) s_piece = make_int4(-1, 0, 0, 0);
+  // total tiles and (from bit 44 up) the number of non-empty segments in one sum
+  long long local = 0;
+  for (int s = c0; s < c1; ++s) {
+    const int t = tiles_of(s);
+    local += t + ((long long)(t > 0) << 44);
+  }
+  const long long both = block_sum(local);
+  const long long T = both & ((1ll << 44) - 1);
+  const long long Sn = both >> 44;
+  int tau = (int)max(1ll, (T + a.G - 1) / a.G);
+  if (Sn > 0 && a.G > Sn) {
+    // pieces(tau) does not grow with tau, and tau = ceil(T / (G - Sn)) always fits:
+    // sum_s ceil(t_s / tau) < T / tau + Sn <= G
+    int lo = tau, hi = (int)max((long long)tau, (T + (a.G - Sn) - 1) / (a.G - Sn));
+    while (lo < hi) {
+      const int mid = lo + (hi - lo) / 2;
+      long long cnt = 0;
+      for (int s = c0; s < c1; ++s) cnt += (tiles_of(s) + mid - 1) / mid;
+      if (block_sum(cnt) <= a.G)
+        hi = mid;
+      else
+        lo = mid + 1;
+    }
+    tau = lo;
+  }
   int lp = 0;
   for (int s = c0; s < c1; ++s) lp += (tiles_of(s) + tau - 1) / tau;
   int incl = lp;

@@ -4,29 +4,37 @@
 // the flattened tree with an ancestor mask); "TreeGraft 精读：多起草器共嫁接一棵草稿树，让投机解码
 // 跨越快与好的单选题" §三 (tree-attention verification).
 //
-// One CTA = one piece of a segment (request b, KV head h, a run of 128-key tiles) for up to
-// 256 query rows (two 128-row M-tiles; row r = node * g + head-in-group). Roles:
-//   warp 8      TMA producer: Q once, then K(0), V(0), K(1), V(1), ... into one ring of
-//               5 slots of 32 KB (evict-first). A slot is reused in load order, so a K slot
-//               frees as soon as Q K^T has read it and the next V can stream in early;
-//   warp 9      MMA issuer (one thread) and TMEM owner: per tile and M-tile m,
-//               S_m = Q_m K^T (SMEM x SMEM), then O_m += P_m V (P from TMEM, V from SMEM),
-//               each MMA waiting only for the operands it reads;
-//   warps 10-11 idle (they complete the third warpgroup, which gives its registers away);
-//   warps 0-3   softmax of M-tile 0, warps 4-7 softmax of M-tile 1: each thread owns one
-//               query row, reads its S row from TMEM, applies the prefix/ancestor mask,
-//               keeps a running max and sum, writes P (bf16) back over its S row, and at
-//               the end writes the normalised partial O row and its log-sum-exp.
-// 128-key tiles keep every MMA at N = 128, where one tcgen05.mma of M=128, K=16 runs at
-// the tensor pipe's full rate (N = 64 loses about a third of it).
-// Tensor memory (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512);
-// P_m occupies the first 64 columns of S_m as bf16 pairs. MMAs issued by one thread run
-// in issue order, so S_m(j+1) overwrites P_m(j) only after O_m += P_m(j) V has read it,
-// and the completion of S_m(j+1) implies O_m holds every tile up to j (used for lazy
-// rescaling: O is rescaled only when a row's max grows by more than 2^8).
+// Work split. A segment (request b, KV head h) has g*N query rows (row r = node * g +
+// head-in-group) and keys [0, P_b + n_b). The split-KV schedule cuts its 128-key tiles into
+// pieces; one thread-block cluster of C = ceil(g*N / 128) CTAs runs one piece, CTA rank c
+// owning query rows [128c, 128c + 128) as one 128-row M-tile. The CTAs of a cluster read
+// the same K/V tiles: the first L CTAs (L = C rounded down to a power of two) each load
+// 1/L of every tile with a cluster-multicast TMA, so every tile leaves L2 once and lands
+// in all C shared memories.
+//
+// Roles (192 threads, one CTA per SM):
+//   warp 4      TMA producer: the K/V items in consumption order, through a ring of 7
+//               slots of 32 KB: K(0), K(1), K(2), V(0), K(3), V(1), ... (K runs two tiles
+//               ahead of V). A slot is refilled once the MMA threads of all C CTAs released
+//               its previous item (multicast tcgen05.commit).
+//   warp 5      MMA issuer (one thread) and tensor-memory owner. S(t) = Q K(t)^T goes to one
+//               of two S buffers (Q from tensor memory, K from shared memory); S(j+2) is
+//               issued as soon as the softmax has read S(j) into registers, so Q K^T stays
+//               two tiles ahead. O += P(j) V(j) as soon as the softmax published P(j).
+//   warps 0-3   softmax: thread = query row = tensor-memory lane. First the thread copies
+//               its Q row into tensor memory. Per tile: read the S row (and free its
+//               buffer), mask, p = 2^(s*scale*log2e - m) with a lazily moved reference max
+//               m, write P (bf16) into the P buffer once O += P(j-1) V(j-1) has read the
+//               previous P, and at the end the normalised partial O row and its log-sum-exp.
+// Tensor memory (512 columns): S buffers at [0,128) and [128,256), O at [256,384), Q at
+// [384,448) and P at [448,512), both as bf16 pairs. Neither Q K^T nor the softmax ever
+// waits for the other's previous tile, and the tensor pipe always holds the next S. Keeping
+// Q out of shared memory leaves all of it to the ring and halves the shared-memory reads of
+// each Q K^T step.
 // Cache rows past a request's length may hold anything: their scores are masked by
 // predicate and their V rows are zeroed in shared memory before the P V product.
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -40,36 +48,35 @@ namespace gt {
 
 namespace {
 
-constexpr int TC_THREADS = 384;     // 8 softmax warps + producer + MMA + 2 idle warps
-// Register split: launched at TC_LAUNCH_REGS per thread (the most 12 warps can hold with 3
-// warps per SM sub-partition), then the producer/MMA warpgroup drops to TC_LOW_REGS and
-// the two softmax warpgroups rise to TC_HIGH_REGS. 2*128*224 + 128*56 = 384*168: the split
-// uses exactly the registers the CTA was launched with.
-constexpr int TC_LAUNCH_REGS = 168, TC_LOW_REGS = 56, TC_HIGH_REGS = 224;
-static_assert(2 * 128 * TC_HIGH_REGS + 128 * TC_LOW_REGS == TC_THREADS * TC_LAUNCH_REGS,
-              "register split must match the launch budget");
+constexpr int TC_THREADS = 192;     // 4 softmax warps + producer + MMA
 constexpr int TK = ATTN_TC_KEYS;    // keys per tile (128)
-constexpr int SLOTS = 5;            // ring slots, each one K or one V tile
+constexpr int SLOTS = 7;            // ring slots, each one K or one V tile
+constexpr int NSBUF = 2;            // S buffers in tensor memory
+constexpr int KLEAD = 2;            // K tiles loaded ahead of V (= NSBUF)
 constexpr int HALF_BYTES = 16384;   // 128 rows x 64 d x bf16 (one 128B-swizzled box)
 constexpr int SLOT_BYTES = 2 * HALF_BYTES;  // one tile: 128 keys x 128 d
+constexpr int MAX_CLUSTER = 4;
 constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t O_COL = 256;
+constexpr uint32_t Q_COL = 384;
+constexpr uint32_t P_COL = 448;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 static_assert(TK == 128, "the tile shape above assumes 128-key tiles");
+static_assert(KLEAD == NSBUF, "S(t + NSBUF) reuses the buffer of P(t)");
 
 struct Smem {
   // offsets from the 1024-aligned base
-  static constexpr int Q = 0;                          // [2 m][2 half] x 16 KB
-  static constexpr int RING = Q + 4 * HALF_BYTES;      // [SLOTS] x 32 KB
+  static constexpr int RING = 0;                       // [SLOTS] x 32 KB
   static constexpr int BAR = RING + SLOTS * SLOT_BYTES;
-  static constexpr int NBAR = 1 + 2 * SLOTS + 2 + 2 + 2 + 1;
+  static constexpr int NBAR = 1 + 2 * SLOTS + 2 * NSBUF + 1 + 1 + 1 + 1;
   static constexpr int END = BAR + NBAR * 8;
 };
 constexpr size_t TC_SMEM = Smem::END + 1024;  // + alignment slack
-static_assert(TC_SMEM <= 232448, "shared memory of one CTA");
+static_assert(TC_SMEM + 512 <= 232448, "shared memory of one CTA (dynamic + static)");
 
 struct Bars {
-  uint64_t *q_full, *full, *empty, *s_full, *p_full, *o_done, *drain;
+  uint64_t *q_full, *full, *empty, *s_full, *s_free, *p_full, *o_ready, *o_done, *drain;
 };
 
 __device__ __forceinline__ Bars bars_at(uint8_t *base) {
@@ -79,14 +86,42 @@ __device__ __forceinline__ Bars bars_at(uint8_t *base) {
   r.full = b + 1;
   r.empty = r.full + SLOTS;
   r.s_full = r.empty + SLOTS;
-  r.p_full = r.s_full + 2;
-  r.o_done = r.p_full + 2;
-  r.drain = r.o_done + 2;
+  r.s_free = r.s_full + NSBUF;
+  r.p_full = r.s_free + NSBUF;
+  r.o_ready = r.p_full + 1;
+  r.o_done = r.o_ready + 1;
+  r.drain = r.o_done + 1;
   return r;
 }
 
-// Load sequence: item 2j is K(j), item 2j+1 is V(j); item q lives in slot q % SLOTS and is
-// that slot's use number q / SLOTS.
+// Item sequence of a piece of nt tiles, the order in which the MMA thread consumes them:
+// K(0..P0-1) with P0 = min(KLEAD, nt), then for j = 0..nt-1: K(j+KLEAD) while
+// j+KLEAD < nt, followed by V(j). Item q sits in slot q % SLOTS as that slot's use number
+// q / SLOTS.
+__device__ __forceinline__ int pos_v(int j, int nt) {
+  const int p0 = min(KLEAD, nt), e = max(0, nt - KLEAD);
+  return p0 + j + min(j + 1, e);
+}
+__device__ __forceinline__ int pos_k(int t, int nt) {
+  const int p0 = min(KLEAD, nt);
+  return t < p0 ? t : p0 + 2 * (t - KLEAD);
+}
+__device__ __forceinline__ void item_at(int q, int nt, bool &is_v, int &tile) {
+  const int p0 = min(KLEAD, nt), e = max(0, nt - KLEAD);
+  if (q < p0) {
+    is_v = false;
+    tile = q;
+    return;
+  }
+  const int r = q - p0;
+  if (r < 2 * e) {
+    is_v = (r & 1) == 1;
+    tile = (r >> 1) + (is_v ? 0 : KLEAD);
+    return;
+  }
+  is_v = true;
+  tile = e + (r - 2 * e);
+}
 __device__ __forceinline__ int slot_of(int q) { return q % SLOTS; }
 __device__ __forceinline__ uint32_t use_parity(int q) { return (uint32_t)((q / SLOTS) & 1); }
 
@@ -97,26 +132,30 @@ __device__ __forceinline__ bool drain_wait(uint64_t *bar, uint32_t parity) {
 }
 
 __global__ void __launch_bounds__(TC_THREADS, 1)
-attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapK,
+attn_tc_kernel(const __nv_bfloat16 *__restrict__ Qg, const __grid_constant__ CUtensorMap mapK,
                const __grid_constant__ CUtensorMap mapV, const uint64_t *__restrict__ mask,
                const int32_t *__restrict__ prefix_len, const int32_t *__restrict__ n_nodes,
-               int N, int Hq, int Hkv, float scale, SchedArgs sa, AttnWs ws, int32_t *err) {
+               int N, int Hq, int Hkv, float scale, int C, int L, SchedArgs sa, AttnWs ws,
+               int32_t *err) {
   pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t tmem_sh;
   __shared__ int abort_sh;
 
-  const int p = blockIdx.x;
+  // every CTA of a cluster gets the same piece, so a cluster leaves here as a whole
+  const int p = blockIdx.x / C;
   const int4 pc = schedule_piece(sa, p, ws, err);
   if (pc.x < 0) return;
   const int seg = pc.x, b = seg / Hkv, h = seg - b * Hkv;
   const int g = Hq / Hkv;
   const int n = n_nodes[b], P = prefix_len[b], keys = P + n;
-  const int row0 = blockIdx.y * 256;          // first segment row of this CTA
-  const int rows_valid = g * n - row0;        // rows of this CTA holding real queries
-  if (rows_valid <= 0) return;
-  const int mtiles = rows_valid > 128 ? 2 : 1;
+  const int rank = (int)tc::cluster_ctarank();
+  const int row0 = rank * 128;  // first segment row of this CTA (may lie past g*n)
   const int t0 = pc.y, nt = pc.z - pc.y;
+  const int total = 2 * nt;
+  const uint16_t all_mask = (uint16_t)((1u << C) - 1u);
+  const bool multicast = C > 1;
+  const int box_rows = TK / L;  // keys of each tile this CTA loads when rank < L
 
   uint8_t *base = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -125,139 +164,177 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
 
   if (tid == 0) {
     abort_sh = 0;
-    tc::mbar_init(bar.q_full, 1);
+    tc::mbar_init(bar.q_full, 128);  // every softmax thread stored its Q row
     for (int s = 0; s < SLOTS; ++s) {
       tc::mbar_init(bar.full + s, 1);
-      tc::mbar_init(bar.empty + s, 1);
+      tc::mbar_init(bar.empty + s, C);  // one release from each CTA's MMA thread
     }
-    for (int m = 0; m < 2; ++m) {
-      tc::mbar_init(bar.s_full + m, 1);
-      tc::mbar_init(bar.p_full + m, 128);
-      tc::mbar_init(bar.o_done + m, 1);
+    for (int s = 0; s < NSBUF; ++s) {
+      tc::mbar_init(bar.s_full + s, 1);
+      tc::mbar_init(bar.s_free + s, 128);  // every softmax thread read its S row
     }
+    tc::mbar_init(bar.p_full, 128);
+    tc::mbar_init(bar.o_ready, 1);
+    tc::mbar_init(bar.o_done, 1);
     tc::mbar_init(bar.drain, 1);
     tc::fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == 5) {
     tc::tmem_alloc(&tmem_sh, TMEM_COLS);
     tc::tmem_relinquish();
   }
   tc::tc_fence_before();
   __syncthreads();
+  // no CTA may multicast into a peer before the peer's barriers exist
+  if (multicast) tc::cluster_sync_all();
   tc::tc_fence_after();
   const uint32_t tmem = tmem_sh;
   volatile int *abort = &abort_sh;
 
-  if (warp >= 8) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(TC_LOW_REGS));
-    if (warp == 8 && lane == 0) {
-      // ---------------------------------------------------------- TMA producer
-      tc::tma_prefetch_desc(&mapQ);
+  if (warp == 4) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer
       tc::tma_prefetch_desc(&mapK);
       tc::tma_prefetch_desc(&mapV);
       const uint64_t pol_kv = tc::policy_evict_first();
-      const uint64_t pol_q = tc::policy_evict_last();
-      tc::mbar_expect_tx(bar.q_full, mtiles * 2 * HALF_BYTES);
-      for (int m = 0; m < mtiles; ++m) {
-        const int node0 = (row0 + m * 128) / g;
-        for (int hf = 0; hf < 2; ++hf)
-          tc::tma_load_4d(base + Smem::Q + (m * 2 + hf) * HALF_BYTES, &mapQ, bar.q_full, hf * 64,
-                          0, h, b * N + node0, pol_q);
-      }
       const int plane = b * Hkv + h;
-      int last = -1;
-      for (int q = 0; q < 2 * nt; ++q) {
+      const bool loader = rank < L;
+      for (int q = 0; q < total; ++q) {
         const int s = slot_of(q);
         if (q >= SLOTS && !tc::mbar_wait(bar.empty + s, use_parity(q - SLOTS), abort)) break;
-        uint8_t *dst = base + Smem::RING + s * SLOT_BYTES;
-        const CUtensorMap *map = (q & 1) ? &mapV : &mapK;
-        const int kb = (t0 + (q >> 1)) * TK;
-        tc::mbar_expect_tx(bar.full + s, SLOT_BYTES);
-        for (int hf = 0; hf < 2; ++hf)
-          tc::tma_load_3d(dst + hf * HALF_BYTES, map, bar.full + s, hf * 64, kb, plane, pol_kv);
-        last = q;
+        if (*abort) break;
+        tc::mbar_expect_tx(bar.full + s, SLOT_BYTES);  // both halves of the whole tile
+        if (loader) {
+          bool is_v;
+          int tile;
+          item_at(q, nt, is_v, tile);
+          const CUtensorMap *map = is_v ? &mapV : &mapK;
+          const int kb = (t0 + tile) * TK + rank * box_rows;
+          uint8_t *dst = base + Smem::RING + s * SLOT_BYTES + rank * box_rows * 128;
+          for (int hf = 0; hf < 2; ++hf) {
+            if (multicast)
+              tc::tma_load_3d_mc(dst + hf * HALF_BYTES, map, bar.full + s, hf * 64, kb, plane,
+                                 all_mask, pol_kv);
+            else
+              tc::tma_load_3d(dst + hf * HALF_BYTES, map, bar.full + s, hf * 64, kb, plane,
+                              pol_kv);
+          }
+        }
       }
-      if (*abort) {  // let every issued copy land before the CTA's shared memory goes away
-        drain_wait(bar.q_full, 0);
-        for (int q = (last - SLOTS + 1 > 0 ? last - SLOTS + 1 : 0); q <= last; ++q)
-          drain_wait(bar.full + slot_of(q), use_parity(q));
-      }
-    } else if (warp == 9 && lane == 0) {
-      // -------------------------------------------------------------- MMA issuer
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {
+      // ------------------------------------------------------------- MMA issuer
       constexpr uint32_t idS = tc::idesc_bf16(128, TK, false, false);
       constexpr uint32_t idO = tc::idesc_bf16(128, 128, false, true);
-      const uint32_t sQ = tc::smem_u32(base + Smem::Q);
       const uint32_t ring = tc::smem_u32(base + Smem::RING);
-      auto issue_s = [&](int m, int s) {  // S_m = Q_m K^T over d = 128 (8 steps of 16)
-        const uint32_t q0 = sQ + m * 2 * HALF_BYTES, k0 = ring + s * SLOT_BYTES;
+      // Descriptors are built once; a K step moves the start address, which sits in the
+      // low 14 bits (address >> 4) and never carries out of them inside shared memory.
+      const uint64_t dK = tc::sdesc_sw128(ring, 16, 1024);
+      const uint64_t dV = tc::sdesc_sw128(ring, HALF_BYTES, 1024);
+      // a slot's release is only sent when a later item will refill it, so every release
+      // that reaches a peer is awaited by that peer's producer
+      auto release = [&](int q) {
+        if (q + SLOTS >= total) return;
+        if (multicast)
+          tc::mma_commit_mc(bar.empty + slot_of(q), all_mask);
+        else
+          tc::mma_commit(bar.empty + slot_of(q));
+      };
+      auto issue_s = [&](int t) {  // S(t) = Q K(t)^T over d = 128 (8 steps of 16)
+        const int q = pos_k(t, nt);
+        if (!tc::mbar_wait(bar.full + slot_of(q), use_parity(q), abort)) return false;
+        tc::tc_fence_after();
+        const uint64_t b0 = dK + ((slot_of(q) * SLOT_BYTES) >> 4);
+        const uint32_t dS = tmem + (uint32_t)((t % NSBUF) * 128);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
-          tc::mma_ss(tmem + m * 128, tc::sdesc_sw128(q0 + off, 16, 1024),
-                     tc::sdesc_sw128(k0 + off, 16, 1024), idS, kk > 0);
+          const uint32_t off = ((kk >> 2) * HALF_BYTES + (kk & 3) * 32) >> 4;
+          tc::mma_ts(dS, tmem + Q_COL + kk * 8, b0 + off, idS, kk > 0);
         }
+        tc::mma_commit(bar.s_full + t % NSBUF);
+        release(q);
+        return true;
       };
-      bool ok = tc::mbar_wait(bar.q_full, 0, abort) &&
-                tc::mbar_wait(bar.full + slot_of(0), use_parity(0), abort);
-      if (ok) {
-        tc::tc_fence_after();
-        for (int m = 0; m < mtiles; ++m) {
-          issue_s(m, slot_of(0));
-          tc::mma_commit(bar.s_full + m);
-        }
-        tc::mma_commit(bar.empty + slot_of(0));  // K(0) is free once both S_m(0) are done
-      }
+      bool ok = tc::mbar_wait(bar.q_full, 0, abort);
+      for (int t = 0; ok && t < min(KLEAD, nt); ++t) ok = issue_s(t);
       for (int j = 0; ok && j < nt; ++j) {
-        const int qv = 2 * j + 1, qk = 2 * j + 2;  // V(j), K(j+1)
-        const bool next = j + 1 < nt;
-        if (!tc::mbar_wait(bar.full + slot_of(qv), use_parity(qv), abort)) break;
-        const uint32_t v0 = ring + slot_of(qv) * SLOT_BYTES;
-        for (int m = 0; m < mtiles; ++m) {
-          if (!tc::mbar_wait(bar.p_full + m, j & 1, abort)) {
+        // S(j+2) into the buffer of S(j) once every softmax thread has read S(j)
+        if (j + KLEAD < nt) {
+          if (!tc::mbar_wait(bar.s_free + j % NSBUF, (uint32_t)((j / NSBUF) & 1), abort)) {
             ok = false;
             break;
           }
           tc::tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // O_m += P_m V over 128 keys (steps of 16)
-            tc::mma_ts(tmem + 256 + m * 128, tmem + m * 128 + kk * 8,
-                       tc::sdesc_sw128(v0 + kk * 2048, HALF_BYTES, 1024), idO, (j > 0) || (kk > 0));
-          if (next) {
-            if (m == 0 && !tc::mbar_wait(bar.full + slot_of(qk), use_parity(qk), abort)) {
-              ok = false;
-              break;
-            }
-            issue_s(m, slot_of(qk));
-            tc::mma_commit(bar.s_full + m);
-          }
+          if (!(ok = issue_s(j + KLEAD))) break;
         }
-        if (!ok) break;
-        tc::mma_commit(bar.empty + slot_of(qv));            // V(j) read by both P V
-        if (next) tc::mma_commit(bar.empty + slot_of(qk));  // K(j+1) read by both S
+        const int qv = pos_v(j, nt);
+        if (!tc::mbar_wait(bar.p_full, j & 1, abort) ||
+            !tc::mbar_wait(bar.full + slot_of(qv), use_parity(qv), abort)) {
+          ok = false;
+          break;
+        }
+        tc::tc_fence_after();
+        const uint64_t v0 = dV + ((slot_of(qv) * SLOT_BYTES) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)  // O += P V over 128 keys (steps of 16)
+          tc::mma_ts(tmem + O_COL, tmem + P_COL + kk * 8, v0 + ((kk * 2048) >> 4), idO,
+                     (j > 0) || (kk > 0));
+        tc::mma_commit(bar.o_ready);
+        release(qv);
       }
-      if (ok)
-        for (int m = 0; m < mtiles; ++m) tc::mma_commit(bar.o_done + m);
+      if (ok) tc::mma_commit(bar.o_done);
       tc::mma_commit(bar.drain);  // every MMA issued above completes before teardown
       drain_wait(bar.drain, 0);
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(TC_HIGH_REGS));
     // ------------------------------------------------------------------- softmax
-    const int m = warp >> 2;                       // M-tile of this warpgroup
-    const int rl = (warp & 3) * 32 + lane;          // row within the M-tile = TMEM lane
-    const int r = row0 + m * 128 + rl;              // row within the segment
-    const bool active = m < mtiles;
+    const int rl = warp * 32 + lane;                // row within the M-tile = TMEM lane
+    const int r = row0 + rl;                        // row within the segment
     const bool row_ok = r < g * n;
     const uint64_t mrow = row_ok ? mask[(size_t)b * N + r / g] : 0ull;
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + lane_base + m * 128;
-    const uint32_t tO = tmem + lane_base + 256 + m * 128;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t tO = tmem + lane_base + O_COL;
     const float sl2 = scale * LOG2E;  // scale > 0: the max of raw scores gives the max
-    float m_used = -INFINITY, l = 0.f;  // running max (log2 units) and sum of this row
-    bool ok = active;
+    float m_used = -INFINITY, l = 0.f;  // reference max (log2 units) and sum of this row
+    {
+      // Q row r = node * g + head-in-group, as 64 bf16 pairs (low half = even element),
+      // the tensor-memory layout of an M-tile operand; rows past the tree are zero
+      const int node = r / g;
+      uint32_t qw[64];
+      if (node < N) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(
+            Qg + (((size_t)b * N + node) * Hq + (size_t)h * g + (r - node * g)) * ATTN_D);
+#pragma unroll
+        for (int v = 0; v < 16; ++v) {
+          const uint4 x = __ldg(src + v);
+          qw[4 * v] = x.x;
+          qw[4 * v + 1] = x.y;
+          qw[4 * v + 2] = x.z;
+          qw[4 * v + 3] = x.w;
+        }
+      } else {
+#pragma unroll
+        for (int v = 0; v < 64; ++v) qw[v] = 0u;
+      }
+      const uint32_t tQ = tmem + lane_base + Q_COL;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t w[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) w[q] = qw[c * 16 + q];
+        tc::tmem_st16(tQ + c * 16, w);
+      }
+      tc::tmem_wait_st();
+      tc::tc_fence_before();
+      tc::mbar_arrive(bar.q_full);
+    }
+    bool ok = true;
     for (int j = 0; ok && j < nt; ++j) {
+      const uint32_t tS = tmem + lane_base + (uint32_t)((j % NSBUF) * 128);
       // wait results are made warp-uniform: the TMEM accesses below are warp-collective
-      if (!__all_sync(0xffffffffu, tc::mbar_wait(bar.s_full + m, j & 1, abort))) {
+      if (!__all_sync(0xffffffffu,
+                      tc::mbar_wait(bar.s_full + j % NSBUF, (uint32_t)((j / NSBUF) & 1), abort))) {
         ok = false;
         break;
       }
@@ -266,39 +343,92 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
 #pragma unroll
       for (int c = 0; c < 4; ++c) tc::tmem_ld32(tS + c * 32, s[c]);
       tc::tmem_wait_ld();
+      tc::tc_fence_before();
+      tc::mbar_arrive(bar.s_free + j % NSBUF);  // S(j) is in registers: S(j+2) may follow
       const int kb = (t0 + j) * TK;
-      // 8 independent partial maxima of the raw scores keep the dependent chain short
-      float mxa[8];
-#pragma unroll
-      for (int a = 0; a < 8; ++a) mxa[a] = -INFINITY;
-      if (kb + TK <= P) {  // whole tile inside the committed prefix: every key visible
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int q = 0; q < 32; ++q) mxa[q & 7] = fmaxf(mxa[q & 7], __uint_as_float(s[c][q]));
-      } else {
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int q = 0; q < 32; ++q) {
-            const int key = kb + c * 32 + q;
-            const bool vis =
-                key < P || (key < keys && ((mrow >> (unsigned)(key - P)) & 1ull));
-            if (!vis) s[c][q] = __float_as_uint(-INFINITY);
-            mxa[q & 7] = fmaxf(mxa[q & 7], __uint_as_float(s[c][q]));
-          }
-      }
-      const float mx = sl2 * fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
-                                   fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
-      // lazy rescale: move the reference max only when it grows by more than 8 (x256)
-      const bool grow = mx > m_used + 8.f;
       float alpha = 1.f;
-      if (grow) {
-        alpha = (m_used == -INFINITY) ? 0.f : tc::ex2_approx(m_used - mx);
-        m_used = mx;
+      uint32_t pk[4][16];  // P(j) as bf16 pairs, stored once the previous P is consumed
+      // Fast path, for a tile wholly inside the committed prefix once the row has a finite
+      // reference max: no max pass. p = 2^(s*scale*log2e - m_used) straight away, with the
+      // tile's sum as the overflow test: sum <= 2^15 = 128 * 2^8 means no p exceeded the
+      // lazy-rescale bound 2^8, so the result is what the general path below computes
+      // (up to summation order). Otherwise (rare: the row's max grew by more than 8 in
+      // log2 units) the warp falls back to the general path, which recomputes every P word
+      // of this tile with a rescaled reference.
+      bool done = false;
+      if (__all_sync(0xffffffffu, kb + TK <= P && j > 0 && m_used > -INFINITY)) {
+        const uint64_t a2 = tc::f32x2_pack(sl2, sl2), c2 = tc::f32x2_pack(-m_used, -m_used);
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            float p0, p1;
+            tc::ex2_fma_x2(__uint_as_float(s[c][2 * q]), __uint_as_float(s[c][2 * q + 1]), a2,
+                           c2, p0, p1);
+            tc::add_x2(acc[q & 3], p0, p1);
+            pk[c][q] = tc::pack_bf16x2(p0, p1);
+          }
+        const float lt = (tc::f32x2_sum(acc[0]) + tc::f32x2_sum(acc[1])) +
+                         (tc::f32x2_sum(acc[2]) + tc::f32x2_sum(acc[3]));
+        done = __all_sync(0xffffffffu, lt <= 32768.f);  // false for inf and NaN too
+        if (done) l += lt;
       }
-      if (__any_sync(0xffffffffu, grow && j > 0)) {
-        // O holds every earlier tile (S_m(j) completed after O_m += P_m(j-1) V)
+      if (!done) {
+        // 8 independent partial maxima of the raw scores keep the dependent chain short
+        float mxa[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) mxa[a] = -INFINITY;
+        if (kb + TK <= P) {  // whole tile inside the committed prefix: every key visible
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int q = 0; q < 32; ++q) mxa[q & 7] = fmaxf(mxa[q & 7], __uint_as_float(s[c][q]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+              const int key = kb + c * 32 + q;
+              const bool vis =
+                  key < P || (key < keys && ((mrow >> (unsigned)(key - P)) & 1ull));
+              if (!vis) s[c][q] = __float_as_uint(-INFINITY);
+              mxa[q & 7] = fmaxf(mxa[q & 7], __uint_as_float(s[c][q]));
+            }
+        }
+        const float mx = sl2 * fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
+                                     fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
+        // lazy rescale: move the reference max only when it grows by more than 8 (x256)
+        if (mx > m_used + 8.f) {
+          alpha = (m_used == -INFINITY) ? 0.f : tc::ex2_approx(m_used - mx);
+          m_used = mx;
+        }
+        l *= alpha;
+        // p = 2^(s * scale * log2 e - m); a row with no visible key so far has m = -inf
+        // and every s = -inf: its p are 0 (not NaN)
+        const float msub = m_used == -INFINITY ? 0.f : m_used;
+        float la[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) la[a] = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const float p0 = tc::ex2_approx(fmaf(__uint_as_float(s[c][2 * q]), sl2, -msub));
+            const float p1 = tc::ex2_approx(fmaf(__uint_as_float(s[c][2 * q + 1]), sl2, -msub));
+            la[q & 7] += p0 + p1;
+            pk[c][q] = tc::pack_bf16x2(p0, p1);
+          }
+        l += ((la[0] + la[1]) + (la[2] + la[3])) + ((la[4] + la[5]) + (la[6] + la[7]));
+      }
+      // O += P(j-1) V(j-1) must have completed before O is rescaled here and before P(j)
+      // overwrites P(j-1)
+      if (j > 0 && !__all_sync(0xffffffffu, tc::mbar_wait(bar.o_ready, (uint32_t)((j - 1) & 1), abort))) {
+        ok = false;
+        break;
+      }
+      if (__any_sync(0xffffffffu, alpha != 1.f && j > 0)) {
+        tc::tc_fence_after();
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t o[32];
@@ -313,32 +443,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
             tc::tmem_st16(tO + c * 32 + half * 16, w);
           }
         }
-        tc::tmem_wait_st();
       }
-      l *= alpha;
-      // p = 2^(s * scale * log2 e - m); a row with no visible key so far has m = -inf and
-      // every s = -inf: its p are 0 (not NaN)
-      const float msub = m_used == -INFINITY ? 0.f : m_used;
-      float la[8];
+      const uint32_t tP = tmem + lane_base + P_COL;
 #pragma unroll
-      for (int a = 0; a < 8; ++a) la[a] = 0.f;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const float p0 = tc::ex2_approx(fmaf(__uint_as_float(s[c][2 * q]), sl2, -msub));
-          const float p1 = tc::ex2_approx(fmaf(__uint_as_float(s[c][2 * q + 1]), sl2, -msub));
-          la[q & 7] += p0 + p1;
-          pk[q] = tc::pack_bf16x2(p0, p1);
-        }
-        tc::tmem_st16(tS + c * 16, pk);
-      }
-      l += ((la[0] + la[1]) + (la[2] + la[3])) + ((la[4] + la[5]) + (la[6] + la[7]));
+      for (int c = 0; c < 4; ++c) tc::tmem_st16(tP + c * 16, pk[c]);
       tc::tmem_wait_st();
-      if (m == 0 && kb + TK > keys) {
+      if (kb + TK > keys) {
         // zero V rows past the request's length (they may hold NaN) before P V reads them
-        const int qv = 2 * j + 1;
+        const int qv = pos_v(j, nt);
         if (!__all_sync(0xffffffffu, tc::mbar_wait(bar.full + slot_of(qv), use_parity(qv), abort))) {
           ok = false;
           break;
@@ -353,9 +465,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
         tc::fence_proxy_async_smem();
       }
       tc::tc_fence_before();
-      tc::mbar_arrive(bar.p_full + m);
+      tc::mbar_arrive(bar.p_full);
     }
-    if (ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(bar.o_done + m, 0, abort));
+    if (ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(bar.o_done, 0, abort));
     if (ok) {
       tc::tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -380,8 +492,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__
 
   tc::tc_fence_before();
   __syncthreads();
-  if (tid == 0 && *abort) set_err(err, GT_ERR_TIMEOUT);
-  if (warp == 9) {
+  const bool aborted = *abort != 0;
+  if (tid == 0 && aborted) set_err(err, GT_ERR_TIMEOUT);
+  if (multicast) {
+    // no CTA leaves while a peer may still multicast into it or release its slots
+    tc::cluster_sync_all();
+    if (aborted && tid == 0) {
+      // after an abort, loads a peer issued for items this CTA never consumed may still be
+      // landing: give them a millisecond (no producer of the cluster issues new ones now)
+      const uint64_t t_end = tc::globaltimer() + 1000000ull;
+      while (tc::globaltimer() < t_end) {
+      }
+    }
+    __syncthreads();
+  }
+  if (warp == 5) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, TMEM_COLS);
   }
@@ -410,56 +535,87 @@ bool encode(CUtensorMap *map, const void *ptr, int rank, const cuuint64_t *dims,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+int cluster_of(int g, int N) { return ceil_div(g * N, 128); }
+int loaders_of(int C) { return C >= 4 ? 4 : (C >= 2 ? 2 : 1); }
+
+bool set_attributes() {
+  static bool done = false;
+  if (done) return true;
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)TC_SMEM);
+  if (e != cudaSuccess) {
+    launch_status(e, "cudaFuncSetAttribute(attn_tc_kernel)");
+    return false;
+  }
+  done = true;
+  return true;
+}
+
 }  // namespace
 
 bool attn_tc_supported(int g, int N) {
-  return g >= 1 && g <= 128 && (128 % g) == 0 && g * N <= 512;
+  return g >= 1 && g <= 128 && (128 % g) == 0 && g * N <= 128 * MAX_CLUSTER;
+}
+
+int attn_tc_pieces(int g, int N) {
+  const int C = cluster_of(g, N);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    (void)cudaGetLastError();
+    return 1;
+  }
+  static int cache[64][MAX_CLUSTER + 1] = {};
+  if (cache[dev][C] > 0) return cache[dev][C];
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 1;
+  }
+  int clusters = sms / C;
+  if (set_attributes()) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(C * clusters);
+    cfg.blockDim = dim3(TC_THREADS);
+    cfg.dynamicSmemBytes = TC_SMEM;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = C;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int nc = 0;
+    if (cudaOccupancyMaxActiveClusters(&nc, attn_tc_kernel, &cfg) == cudaSuccess && nc > 0)
+      clusters = nc < clusters ? nc : clusters;
+    else
+      (void)cudaGetLastError();
+  }
+  cache[dev][C] = clusters > 0 ? clusters : 1;
+  return cache[dev][C];
 }
 
 int attn_tc_launch(const void *Q, const void *K, const void *V, const uint64_t *mask,
                    const SchedArgs &sa, int B, int N, int Hq, int Hkv, int Lcap, float scale,
                    const AttnWs &ws, int32_t *err, cudaStream_t s) {
   const int g = Hq / Hkv;
-  CUtensorMap mQ, mK, mV;
-  const cuuint64_t qdims[4] = {(cuuint64_t)ATTN_D, (cuuint64_t)g, (cuuint64_t)Hkv,
-                               (cuuint64_t)B * N};
-  const cuuint64_t qstr[3] = {(cuuint64_t)ATTN_D * 2, (cuuint64_t)g * ATTN_D * 2,
-                              (cuuint64_t)Hq * ATTN_D * 2};
-  const cuuint32_t qbox[4] = {64, (cuuint32_t)g, 1, (cuuint32_t)(128 / g)};
+  const int C = cluster_of(g, N), L = loaders_of(C);
+  CUtensorMap mK, mV;
   const cuuint64_t kdims[3] = {(cuuint64_t)ATTN_D, (cuuint64_t)Lcap, (cuuint64_t)B * Hkv};
   const cuuint64_t kstr[2] = {(cuuint64_t)ATTN_D * 2, (cuuint64_t)Lcap * ATTN_D * 2};
-  const cuuint32_t kbox[3] = {64, (cuuint32_t)TK, 1};
+  const cuuint32_t kbox[3] = {64, (cuuint32_t)(TK / L), 1};
   if (!encode_fn()) {
     note_error("cuTensorMapEncodeTiled entry point", cudaErrorNotSupported);
-    return GT_ERR_CUDA;
-  }
-  if (!encode(&mQ, Q, 4, qdims, qstr, qbox)) {
-    note_error("cuTensorMapEncodeTiled(Q)", cudaErrorInvalidValue);
     return GT_ERR_CUDA;
   }
   if (!encode(&mK, K, 3, kdims, kstr, kbox) || !encode(&mV, V, 3, kdims, kstr, kbox)) {
     note_error("cuTensorMapEncodeTiled(K/V)", cudaErrorInvalidValue);
     return GT_ERR_CUDA;
   }
-  static bool attr = false;
-  if (!attr) {
-    // the register split above is only valid at exactly TC_LAUNCH_REGS per thread
-    cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, attn_tc_kernel);
-    if (e != cudaSuccess) return launch_status(e, "cudaFuncGetAttributes(attn_tc_kernel)");
-    if (fa.numRegs != TC_LAUNCH_REGS) {
-      note_error("attn_tc_kernel register count differs from its register split",
-                 cudaErrorInvalidConfiguration);
-      return GT_ERR_CUDA;
-    }
-    e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)TC_SMEM);
-    if (e != cudaSuccess) return launch_status(e, "cudaFuncSetAttribute(attn_tc_kernel)");
-    attr = true;
-  }
-  const int row_groups = ceil_div(g * N, 256);
-  return launch(attn_tc_kernel, dim3(ws.maxp, row_groups), dim3(TC_THREADS), TC_SMEM, s, mQ, mK,
-                mV, mask, sa.prefix_len, sa.n_nodes, N, Hq, Hkv, scale, sa, ws, err);
+  if (!set_attributes()) return GT_ERR_CUDA;
+  // one cluster of C CTAs per piece; the schedule never makes more than ws.maxp pieces
+  return launch_cluster(attn_tc_kernel, dim3(C * ws.maxp), dim3(TC_THREADS), dim3(C, 1, 1),
+                        TC_SMEM, s, (const __nv_bfloat16 *)Q, mK, mV, mask, sa.prefix_len, sa.n_nodes, N, Hq, Hkv,
+                        scale, C, L, sa, ws, err);
 }
 
 }  // namespace gt

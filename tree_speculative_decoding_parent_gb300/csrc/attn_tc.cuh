@@ -13,6 +13,10 @@ constexpr int ATTN_TC_KEYS = 128;  // keys per K/V tile
 // True when the tcgen05 kernel handles g query heads per KV head and N tree nodes.
 bool attn_tc_supported(int g, int N);
 
+// Number of split-KV pieces to aim for: the thread-block clusters of the kernel (one per
+// piece, ceil(g*N/128) CTAs each, one CTA per SM) that fit on the device at once.
+int attn_tc_pieces(int g, int N);
+
 // Runs every split-KV piece of the schedule (tiles of ATTN_TC_KEYS keys, computed in the
 // kernel from `sa`) and writes the partial O / LSE rows of every piece.
 int attn_tc_launch(const void *Q, const void *K, const void *V, const uint64_t *mask,

@@ -109,6 +109,20 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *m, uin
       "r"(c3), "l"(policy)
       : "memory");
 }
+// The same 3-D tile load, multicast: the box lands at the same shared-memory offset in
+// every CTA of the cluster named in cta_mask, and each of those CTAs' mbarriers at the
+// offset of `bar` receives the complete_tx of the bytes written into that CTA.
+__device__ __forceinline__ void tma_load_3d_mc(void *dst, const CUtensorMap *m, uint64_t *bar,
+                                               int c0, int c1, int c2, uint16_t cta_mask,
+                                               uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5}], [%2], %6, %7;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
+      "h"(cta_mask), "l"(policy)
+      : "memory");
+}
 // 1-D bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16).
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
                                           uint64_t *bar, uint64_t policy) {
@@ -219,12 +233,67 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
       : "memory");
 }
 
+// As mma_commit, but the arrival goes to the mbarrier at the offset of `bar` in every CTA
+// of the cluster named in cta_mask.
+__device__ __forceinline__ void mma_commit_mc(uint64_t *bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
+// ---------------------------------------------------------------------------- cluster
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of every CTA of the cluster arrives; returns once all have arrived. Shared-
+// memory writes before it are visible to the other CTAs after it.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // 2^x by the hardware approximation (relative error about 2^-22, subnormals flushed,
 // 2^-inf = +0); used for softmax probabilities that are rounded to bf16 right after.
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Two fp32 values as one 64-bit register pair (lo in the low word), the operand form of
+// the packed .f32x2 instructions.
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float f32x2_sum(uint64_t v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return lo + hi;
+}
+// (p0, p1) = 2^(s * a + c) for a pair of scores: one packed FMA (two fp32 FMAs, each
+// rounded once, as fmaf) and two ex2.approx.ftz. a and c are packed pairs.
+__device__ __forceinline__ void ex2_fma_x2(float s0, float s1, uint64_t a, uint64_t c,
+                                           float &p0, float &p1) {
+  asm("{\n\t.reg .b64 sp, xp;\n\t.reg .f32 x0, x1;\n\t"
+      "mov.b64 sp, {%2, %3};\n\t"
+      "fma.rn.f32x2 xp, sp, %4, %5;\n\t"
+      "mov.b64 {x0, x1}, xp;\n\t"
+      "ex2.approx.ftz.f32 %0, x0;\n\t"
+      "ex2.approx.ftz.f32 %1, x1;\n\t}"
+      : "=f"(p0), "=f"(p1)
+      : "f"(s0), "f"(s1), "l"(a), "l"(c));
+}
+// acc += (p0, p1) with one packed add.
+__device__ __forceinline__ void add_x2(uint64_t &acc, float p0, float p1) {
+  asm("{\n\t.reg .b64 pp;\n\tmov.b64 pp, {%1, %2};\n\tadd.rn.f32x2 %0, %0, pp;\n\t}"
+      : "+l"(acc)
+      : "f"(p0), "f"(p1));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
