@@ -123,6 +123,23 @@ class ClockSampler:
                 "source": "nvml"}
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest x over all ranks (the slowest rank sets the job's time); x itself when
+    there is no process group."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, steps_per_rank: int, seconds: float) -> float:
+    """Whole-job steps/s: every rank ran its own replica of `steps_per_rank` steps, and the
+    job took as long as its slowest rank."""
+    return world * steps_per_rank / seconds
+
+
 def _traffic_record(kernel_key: str):
     """DRAM bytes per launch from a committed ncu summary, if the kernel source it was taken
     on is unchanged (sha256 of the CUDA sources), else None."""
@@ -302,11 +319,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     clocks = clk.stop() if clk else None
     if dist:
         dist.barrier()
-    ms = t0.elapsed_time(t1)
-    if dist:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(t0.elapsed_time(t1), dist, dev)
     errc = int(buf.err.item())
     if errc != 0:
         raise RuntimeError(f"device error {gt.status_string(errc)}")
@@ -351,11 +364,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     te = time.perf_counter()
     for _ in range(ne):
         e2e_step()
-    e2e_s = time.perf_counter() - te
-    if dist:
-        tt = torch.tensor([e2e_s], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_s = float(tt.item())
+    e2e_s = max_over_ranks(time.perf_counter() - te, dist, dev)
 
     breakdown = None
     if args.breakdown and rank == 0:
@@ -366,7 +375,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     peak, peak_kind = _peaks()
     ab = attn_bytes(scn)
     achieved = ab / (attn_avg_ms * 1e-3) / 1e9
-    value = world * args.steps / (ms * 1e-3)
+    value = job_throughput(world, args.steps, ms * 1e-3)
     line = {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
@@ -387,7 +396,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
                      "algorithmic_bytes_per_launch": ab,
                      "avg_launch_ms": attn_avg_ms,
                      "traffic": _traffic_record(f"tree_attn/config{args.config}")},
-        "e2e": {"value": world * ne / e2e_s, "unit": "steps/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_throughput(world, ne, e2e_s), "unit": "steps/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * KERNELS_PER_STEP,
         "clocks": clocks,
