@@ -1,0 +1,73 @@
+// Top-K selection over the nodes of one CTA (one node per thread) for the prune of
+// "TreeGraft 精读：多起草器共嫁接一棵草稿树，让投机解码跨越快与好的单选题" §三 / §四 How (keep the
+// Bver best nodes by cumulative path score) and the static-tree prune of
+// "浙江大学、阿里巴巴联手破解AI推理瓶颈" §四.
+#pragma once
+
+#include "gt_internal.cuh"
+
+namespace gt {
+
+// Among the candidate nodes of the CTA (thread t holds node t; key != 0 marks a
+// candidate, larger key = better, see order_key), keeps the K with the largest keys, equal
+// keys going to the smaller thread index. Node v is kept iff fewer than K candidates have a
+// larger key, or an equal key and a smaller index: the rank rule, found in O(n) by an
+// exact radix select of the K-th largest key (four passes of 8-bit digits through a
+// shared-memory histogram) and a block scan over the nodes that tie with it.
+// s_hist: 256 ints, s_sel: 2 ints, warp_tot: 32 ints of shared scratch. Every thread of
+// the CTA must call it (it synchronises).
+__device__ __forceinline__ bool topk_keys_keep(uint32_t key, int K, int *s_hist, int *s_sel,
+                                               int *warp_tot) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int total;
+  (void)block_excl_count(key != 0u, warp_tot, &total);
+  if (K <= 0) return false;
+  if (total <= K) return key != 0u;
+  uint32_t prefix = 0u;  // top bits of the K-th largest key fixed so far
+  int kr = K;            // its rank among the keys that share those bits
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += blockDim.x) s_hist[i] = 0;
+    __syncthreads();
+    const bool match =
+        key != 0u && (shift == 24 || (key >> (shift + 8)) == (prefix >> (shift + 8)));
+    if (match) atomicAdd(&s_hist[(key >> shift) & 255u], 1);
+    __syncthreads();
+    if (warp == 0) {
+      // lane L holds the digits 255 - 8L down to 248 - 8L: lanes run from high to low
+      int c[8], sum = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        c[i] = s_hist[255 - 8 * lane - i];
+        sum += c[i];
+      }
+      int incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int excl = incl - sum;
+      if (excl < kr && incl >= kr) {  // exactly one lane: the count reaches kr in its bins
+        int acc = excl;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (acc + c[i] >= kr) {
+            s_sel[0] = 255 - 8 * lane - i;
+            s_sel[1] = kr - acc;
+            break;
+          }
+          acc += c[i];
+        }
+      }
+    }
+    __syncthreads();
+    prefix |= (uint32_t)s_sel[0] << shift;
+    kr = s_sel[1];
+  }
+  // prefix is now the K-th largest key; kr of the keys equal to it are kept
+  int neq;
+  const int eq_rank = block_excl_count(key != 0u && key == prefix, warp_tot, &neq);
+  return key > prefix || (key == prefix && eq_rank < kr);
+}
+
+}  // namespace gt

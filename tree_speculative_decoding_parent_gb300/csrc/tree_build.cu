@@ -12,6 +12,7 @@
 #include <math.h>
 
 #include "gt_internal.cuh"
+#include "prune_select.cuh"
 #include "launch.cuh"
 
 namespace gt {
@@ -39,6 +40,7 @@ tree_build_kernel(const float *__restrict__ score, const int32_t *__restrict__ p
   int *s_ttok = s_tpar + Tb;                          // [Tb]
   int *s_tnew = s_ttok + Tb;                          // [Tb]
   __shared__ int warp_tot[32];
+  __shared__ int s_hist[256], s_sel[2];
   __shared__ int s_bad, s_maxd, s_n;
   const int b = blockIdx.x, t = threadIdx.x;
   const size_t in0 = (size_t)b * Nin, row0 = (size_t)b * N;
@@ -90,24 +92,10 @@ tree_build_kernel(const float *__restrict__ score, const int32_t *__restrict__ p
     return;
   }
   const float th = thresh ? thresh[b] : -INFINITY;
-  if (t == 0) s_score[0] = __int_as_float(0x7fc00000);  // the root never ranks
-  for (int u = n + t; u < Nin4; u += blockDim.x) s_score[u] = __int_as_float(0x7fc00000);
-  __syncthreads();
-  bool kept = (t == 0);
-  if (t > 0 && t < n && s >= th) {
-    const float4 *s4 = reinterpret_cast<const float4 *>(s_score);
-    int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-#pragma unroll 4
-    for (int q = 0; q < (n + 3) >> 2; ++q) {
-      const float4 x = s4[q];
-      const int u = 4 * q;
-      r0 += (x.x >= th) & ((x.x > s) | ((x.x == s) & (u < t)));
-      r1 += (x.y >= th) & ((x.y > s) | ((x.y == s) & (u + 1 < t)));
-      r2 += (x.z >= th) & ((x.z > s) | ((x.z == s) & (u + 2 < t)));
-      r3 += (x.w >= th) & ((x.w > s) | ((x.w == s) & (u + 3 < t)));
-    }
-    kept = (r0 + r1) + (r2 + r3) < ke - 1;
-  }
+  // the root is always kept; the other nodes compete for the remaining ke - 1 slots
+  const bool cand = t > 0 && t < n && s >= th;
+  const bool sel = topk_keys_keep(cand ? order_key(s) : 0u, ke - 1, s_hist, s_sel, warp_tot);
+  const bool kept = (t == 0) || sel;
   int nk;
   const int newi = block_excl_count(kept, warp_tot, &nk);
   if (t < n) s_new[t] = kept ? newi : -1;

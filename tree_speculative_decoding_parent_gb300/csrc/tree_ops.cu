@@ -11,13 +11,15 @@
 #include <math.h>
 
 #include "gt_internal.cuh"
+#include "prune_select.cuh"
 #include "launch.cuh"
 
 namespace gt {
 
 // ------------------------------------------------------------------------------------
 // a1: prune. Rank of non-root node v = number of eligible nodes better than v in the
-// order (score desc, index asc); keep v iff rank < keep-1 (the root takes one slot).
+// order (score desc, index asc); keep v iff rank < keep-1 (the root takes one slot). The
+// kept set is found without ranking every node: topk_keys_keep selects it in O(n).
 // With scores non-increasing from parent to child (checked), the kept set is
 // ancestor-closed, so a prefix count over kept flags renumbers it in index order.
 // ------------------------------------------------------------------------------------
@@ -29,10 +31,11 @@ prune_kernel(const float *__restrict__ score, const int32_t *__restrict__ parent
              float *__restrict__ out_score, int32_t *__restrict__ out_old,
              int32_t *__restrict__ n_out, int32_t *err) {
   pdl_enter();
-  extern __shared__ float s_score[];           // [Nin4] (NaN-padded), then s_new [Nin]
+  extern __shared__ float s_score[];           // [Nin4] scores, then s_new [Nin]
   const int Nin4 = (Nin + 3) & ~3;
   int *s_new = reinterpret_cast<int *>(s_score + Nin4);  // [Nin]
   __shared__ int warp_tot[32];
+  __shared__ int s_hist[256], s_sel[2];
   __shared__ int s_bad;
   const int b = blockIdx.x, v = threadIdx.x;
   const size_t in0 = (size_t)b * Nin, out0 = (size_t)b * Nout;
@@ -77,26 +80,10 @@ prune_kernel(const float *__restrict__ score, const int32_t *__restrict__ parent
     return;
   }
   const float th = thresh ? thresh[b] : -INFINITY;
-  // the rank loop compares against every node: hide the root and the padding behind NaN
-  // (NaN fails every comparison), then read four scores per shared-memory load
-  if (v == 0) s_score[0] = __int_as_float(0x7fc00000);
-  for (int u = n + v; u < Nin4; u += blockDim.x) s_score[u] = __int_as_float(0x7fc00000);
-  __syncthreads();
-  bool kept = (v == 0);
-  if (v > 0 && v < n && s >= th) {
-    const float4 *s4 = reinterpret_cast<const float4 *>(s_score);
-    int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-#pragma unroll 4
-    for (int q = 0; q < (n + 3) >> 2; ++q) {
-      const float4 x = s4[q];
-      const int u = 4 * q;
-      r0 += (x.x >= th) & ((x.x > s) | ((x.x == s) & (u < v)));
-      r1 += (x.y >= th) & ((x.y > s) | ((x.y == s) & (u + 1 < v)));
-      r2 += (x.z >= th) & ((x.z > s) | ((x.z == s) & (u + 2 < v)));
-      r3 += (x.w >= th) & ((x.w > s) | ((x.w == s) & (u + 3 < v)));
-    }
-    kept = (r0 + r1) + (r2 + r3) < ke - 1;
-  }
+  // the root is always kept; the other nodes compete for the remaining ke - 1 slots
+  const bool cand = v > 0 && v < n && s >= th;
+  const bool sel = topk_keys_keep(cand ? order_key(s) : 0u, ke - 1, s_hist, s_sel, warp_tot);
+  const bool kept = (v == 0) || sel;
   int total;
   const int newi = block_excl_count(kept, warp_tot, &total);
   if (v < n) s_new[v] = kept ? newi : -1;
