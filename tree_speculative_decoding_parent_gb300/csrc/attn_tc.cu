@@ -137,31 +137,21 @@ attn_tc_kernel(const __nv_bfloat16 *__restrict__ Qg, const __grid_constant__ CUt
                const int32_t *__restrict__ prefix_len, const int32_t *__restrict__ n_nodes,
                int N, int Hq, int Hkv, float scale, int C, int L, SchedArgs sa, AttnWs ws,
                int32_t *err) {
-  pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t tmem_sh;
   __shared__ int abort_sh;
 
-  // every CTA of a cluster gets the same piece, so a cluster leaves here as a whole
-  const int p = blockIdx.x / C;
-  const int4 pc = schedule_piece(sa, p, ws, err);
-  if (pc.x < 0) return;
-  const int seg = pc.x, b = seg / Hkv, h = seg - b * Hkv;
-  const int g = Hq / Hkv;
-  const int n = n_nodes[b], P = prefix_len[b], keys = P + n;
   const int rank = (int)tc::cluster_ctarank();
-  const int row0 = rank * 128;  // first segment row of this CTA (may lie past g*n)
-  const int t0 = pc.y, nt = pc.z - pc.y;
-  const int total = 2 * nt;
   const uint16_t all_mask = (uint16_t)((1u << C) - 1u);
   const bool multicast = C > 1;
   const int box_rows = TK / L;  // keys of each tile this CTA loads when rank < L
-
   uint8_t *base = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const Bars bar = bars_at(base);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
+  // Set-up that reads nothing the previous kernels of the stream write runs before the
+  // programmatic-dependency wait, overlapping their tail: barriers, tensor memory, cluster.
   if (tid == 0) {
     abort_sh = 0;
     tc::mbar_init(bar.q_full, 128);  // every softmax thread stored its Q row
@@ -190,6 +180,21 @@ attn_tc_kernel(const __nv_bfloat16 *__restrict__ Qg, const __grid_constant__ CUt
   tc::tc_fence_after();
   const uint32_t tmem = tmem_sh;
   volatile int *abort = &abort_sh;
+
+  pdl_enter();
+  // every CTA of a cluster gets the same piece, so a cluster leaves here as a whole
+  const int p = blockIdx.x / C;
+  const int4 pc = schedule_piece(sa, p, ws, err);
+  if (pc.x < 0) {
+    if (warp == 5) tc::tmem_dealloc(tmem, TMEM_COLS);
+    return;
+  }
+  const int seg = pc.x, b = seg / Hkv, h = seg - b * Hkv;
+  const int g = Hq / Hkv;
+  const int n = n_nodes[b], P = prefix_len[b], keys = P + n;
+  const int row0 = rank * 128;  // first segment row of this CTA (may lie past g*n)
+  const int t0 = pc.y, nt = pc.z - pc.y;
+  const int total = 2 * nt;
 
   if (warp == 4) {
     if (lane == 0) {
