@@ -29,10 +29,19 @@ constexpr size_t SIMT_SMEM =
     sizeof(float) * (2 * (size_t)ATTN_D * SIMT_LD + (size_t)SIMT_KEYS * ATTN_D +
                      (size_t)SIMT_ROWS * SIMT_SLD + 3 * SIMT_ROWS);
 
-template <typename T> __device__ __forceinline__ float to_f32(T x);
-template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
-template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
-  return __bfloat162float(x);
+
+// Four consecutive elements as fp32 (16-byte fp32 or 8-byte bf16 loads; callers keep the
+// element index a multiple of 4 and the base 16-byte aligned).
+template <typename T> __device__ __forceinline__ float4 load4(const T *p);
+template <> __device__ __forceinline__ float4 load4<float>(const float *p) {
+  return *reinterpret_cast<const float4 *>(p);
+}
+template <> __device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16 *p) {
+  const uint2 u = *reinterpret_cast<const uint2 *>(p);
+  const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&u.x);
+  const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162 *>(&u.y);
+  const float2 fa = __bfloat1622float2(a), fc = __bfloat1622float2(c);
+  return make_float4(fa.x, fa.y, fc.x, fc.y);
 }
 
 template <typename T>
@@ -61,15 +70,29 @@ attn_simt_kernel(const T *__restrict__ Q, const T *__restrict__ K, const T *__re
   if (r0 >= g * n) return;
   const int tid = threadIdx.x;
 
-  // Q rows (transposed into Qs), masks
-  for (int e = tid; e < SIMT_ROWS * ATTN_D; e += 256) {
-    const int rl = e / ATTN_D, dd = e - rl * ATTN_D, r = r0 + rl;
-    float q = 0.f;
-    if (r < g * n) {
-      const int i = r / g, hq = h * g + (r - i * g);
-      q = to_f32<T>(Q[(((size_t)b * N + i) * Hq + hq) * ATTN_D + dd]);
+  // Q rows (transposed into Qs), masks. Every load of a thread is issued before the first
+  // store, so the tile costs one memory round trip, not one per element.
+  constexpr int V4 = SIMT_ROWS * ATTN_D / 4 / 256;  // 4-element groups per thread (8)
+  {
+    float4 qv[V4];
+#pragma unroll
+    for (int k = 0; k < V4; ++k) {
+      const int e4 = tid + k * 256, rl = e4 / (ATTN_D / 4), d4 = e4 - rl * (ATTN_D / 4);
+      const int r = r0 + rl;
+      qv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (r < g * n) {
+        const int i = r / g, hq = h * g + (r - i * g);
+        qv[k] = load4<T>(Q + (((size_t)b * N + i) * Hq + hq) * ATTN_D + d4 * 4);
+      }
     }
-    Qs[dd * SIMT_LD + rl] = q;
+#pragma unroll
+    for (int k = 0; k < V4; ++k) {
+      const int e4 = tid + k * 256, rl = e4 / (ATTN_D / 4), d4 = e4 - rl * (ATTN_D / 4);
+      Qs[(d4 * 4 + 0) * SIMT_LD + rl] = qv[k].x;
+      Qs[(d4 * 4 + 1) * SIMT_LD + rl] = qv[k].y;
+      Qs[(d4 * 4 + 2) * SIMT_LD + rl] = qv[k].z;
+      Qs[(d4 * 4 + 3) * SIMT_LD + rl] = qv[k].w;
+    }
   }
   if (tid < SIMT_ROWS) {
     const int r = r0 + tid;
@@ -89,15 +112,28 @@ attn_simt_kernel(const T *__restrict__ Q, const T *__restrict__ K, const T *__re
   for (int tile = pc.y; tile < pc.z; ++tile) {
     const int kb = tile * SIMT_KEYS;
     __syncthreads();
-    for (int e = tid; e < SIMT_KEYS * ATTN_D; e += 256) {
-      const int c = e / ATTN_D, dd = e - c * ATTN_D, j = kb + c;
-      float kx = 0.f, vx = 0.f;
-      if (j < keys) {
-        kx = to_f32<T>(K[(kv0 + j) * ATTN_D + dd]);
-        vx = to_f32<T>(V[(kv0 + j) * ATTN_D + dd]);
+    {
+      constexpr int K4 = SIMT_KEYS * ATTN_D / 4 / 256;  // 4-element groups per thread (8)
+      float4 kv[K4], vv[K4];
+#pragma unroll
+      for (int k = 0; k < K4; ++k) {
+        const int e4 = tid + k * 256, c = e4 / (ATTN_D / 4), d4 = e4 - c * (ATTN_D / 4);
+        const int j = kb + c;
+        kv[k] = vv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (j < keys) {
+          kv[k] = load4<T>(K + (kv0 + j) * ATTN_D + d4 * 4);
+          vv[k] = load4<T>(V + (kv0 + j) * ATTN_D + d4 * 4);
+        }
       }
-      Ks[dd * SIMT_LD + c] = kx;
-      Vs[c * ATTN_D + dd] = vx;
+#pragma unroll
+      for (int k = 0; k < K4; ++k) {
+        const int e4 = tid + k * 256, c = e4 / (ATTN_D / 4), d4 = e4 - c * (ATTN_D / 4);
+        Ks[(d4 * 4 + 0) * SIMT_LD + c] = kv[k].x;
+        Ks[(d4 * 4 + 1) * SIMT_LD + c] = kv[k].y;
+        Ks[(d4 * 4 + 2) * SIMT_LD + c] = kv[k].z;
+        Ks[(d4 * 4 + 3) * SIMT_LD + c] = kv[k].w;
+        *reinterpret_cast<float4 *>(Vs + c * ATTN_D + d4 * 4) = vv[k];
+      }
     }
     __syncthreads();
     float s[4][4];

@@ -71,7 +71,8 @@ struct SchedArgs {
 // reports invalid requests. Every thread of the CTA must call it (it synchronises).
 __device__ __forceinline__ int4 schedule_piece(const SchedArgs &a, int p, AttnWs ws,
                                                int32_t *err) {
-  __shared__ long long s_red[32];
+  constexpr int CH = 4;  // segments per thread kept in registers; more are recomputed
+  __shared__ long long s_red[2][32];
   __shared__ int s_scan[32];
   __shared__ int4 s_piece;
   const int S = a.B * a.Hkv, tid = threadIdx.x, nt = blockDim.x;
@@ -86,20 +87,35 @@ __device__ __forceinline__ int4 schedule_piece(const SchedArgs &a, int p, AttnWs
     if (!ok && publisher && (s % a.Hkv) == 0 && err) atomicCAS(err, 0, GT_ERR_RANGE);
     return ok ? (P + n + a.TK - 1) / a.TK : 0;
   };
+  int tl[CH];  // tiles of this thread's first CH segments
+#pragma unroll
+  for (int i = 0; i < CH; ++i) tl[i] = c0 + i < c1 ? tiles_of(c0 + i) : 0;
+  // one barrier per sum: the scratch alternates, and the barrier of the next sum orders
+  // every read of this one before the one after it writes the same half
+  int sum_no = 0;
   auto block_sum = [&](long long v) {
 #pragma unroll
     for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    __syncthreads();  // every thread has read s_red from the previous sum
-    if (lane == 0) s_red[warp] = v;
+    long long *red = s_red[sum_no++ & 1];
+    if (lane == 0) red[warp] = v;
     __syncthreads();
     long long t = 0;
-    for (int w = 0; w < nw; ++w) t += s_red[w];
+    for (int w = 0; w < nw; ++w) t += red[w];
     return t;
+  };
+  auto pieces_of = [&](int tau) {  // sum over this thread's segments of ceil(tiles / tau)
+    long long c = 0;
+#pragma unroll
+    for (int i = 0; i < CH; ++i) c += (tl[i] + tau - 1) / tau;
+    for (int s = c0 + CH; s < c1; ++s) c += (tiles_of(s) + tau - 1) / tau;
+    return c;
   };
   if (tid == 0) s_piece = make_int4(-1, 0, 0, 0);
   // total tiles and (from bit 44 up) the number of non-empty segments in one sum
   long long local = 0;
-  for (int s = c0; s < c1; ++s) {
+#pragma unroll
+  for (int i = 0; i < CH; ++i) local += tl[i] + ((long long)(tl[i] > 0) << 44);
+  for (int s = c0 + CH; s < c1; ++s) {
     const int t = tiles_of(s);
     local += t + ((long long)(t > 0) << 44);
   }
@@ -113,17 +129,14 @@ __device__ __forceinline__ int4 schedule_piece(const SchedArgs &a, int p, AttnWs
     int lo = tau, hi = (int)max((long long)tau, (T + (a.G - Sn) - 1) / (a.G - Sn));
     while (lo < hi) {
       const int mid = lo + (hi - lo) / 2;
-      long long cnt = 0;
-      for (int s = c0; s < c1; ++s) cnt += (tiles_of(s) + mid - 1) / mid;
-      if (block_sum(cnt) <= a.G)
+      if (block_sum(pieces_of(mid)) <= a.G)
         hi = mid;
       else
         lo = mid + 1;
     }
     tau = lo;
   }
-  int lp = 0;
-  for (int s = c0; s < c1; ++s) lp += (tiles_of(s) + tau - 1) / tau;
+  const int lp = (int)pieces_of(tau);
   int incl = lp;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -138,7 +151,11 @@ __device__ __forceinline__ int4 schedule_piece(const SchedArgs &a, int p, AttnWs
     total += s_scan[w];
   }
   for (int s = c0; s < c1; ++s) {
-    const int t = tiles_of(s);
+    int t = 0;
+#pragma unroll
+    for (int i = 0; i < CH; ++i)
+      if (s == c0 + i) t = tl[i];
+    if (s >= c0 + CH) t = tiles_of(s);
     const int cnt = (t + tau - 1) / tau;
     if (publisher) ws.seg[s] = make_int2(off, cnt);
     if (p >= off && p < off + cnt) {

@@ -73,7 +73,8 @@ struct Smem {
   static constexpr int END = BAR + NBAR * 8;
 };
 constexpr size_t TC_SMEM = Smem::END + 1024;  // + alignment slack
-static_assert(TC_SMEM + 512 <= 232448, "shared memory of one CTA (dynamic + static)");
+static_assert(TC_SMEM + 768 <= 232448, "shared memory of one CTA (dynamic + static)");
+static_assert(128 * (ATTN_D * 4 + 16) <= SLOTS * SLOT_BYTES, "partial rows are staged in the ring");
 
 struct Bars {
   uint64_t *q_full, *full, *empty, *s_full, *s_free, *p_full, *o_ready, *o_done, *drain;
@@ -124,6 +125,18 @@ __device__ __forceinline__ void item_at(int q, int nt, bool &is_v, int &tile) {
 }
 __device__ __forceinline__ int slot_of(int q) { return q % SLOTS; }
 __device__ __forceinline__ uint32_t use_parity(int q) { return (uint32_t)((q / SLOTS) & 1); }
+
+// AND of `pred` over the four softmax warps (128 threads), through named barrier 1.
+__device__ __forceinline__ int __syncthreads_and_named(bool pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((unsigned)pred)
+      : "memory");
+  return r;
+}
 
 // Bounded wait that ignores the abort flag (used only while draining in-flight work).
 __device__ __forceinline__ bool drain_wait(uint64_t *bar, uint32_t parity) {
@@ -473,25 +486,39 @@ attn_tc_kernel(const __nv_bfloat16 *__restrict__ Qg, const __grid_constant__ CUt
       tc::mbar_arrive(bar.p_full);
     }
     if (ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(bar.o_done, 0, abort));
-    if (ok) {
+    // The normalised partial rows leave through shared memory so that every warp store
+    // covers a whole 512-byte row: the ring is idle once O is complete (every item was
+    // consumed, so no copy is in flight into it). Rows are staged at a 528-byte pitch,
+    // which keeps the threads' 16-byte writes free of bank conflicts.
+    constexpr int PITCH = ATTN_D * 4 + 16;
+    const bool wok = __all_sync(0xffffffffu, ok);
+    if (wok) {
       tc::tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      float *dst = ws.opart + ((size_t)p * ws.rows_pad + r) * ATTN_D;
+      uint8_t *srow = base + Smem::RING + rl * PITCH;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t o[32];
         tc::tmem_ld32(tO + c * 32, o);
         tc::tmem_wait_ld();
-        if (row_ok) {
 #pragma unroll
-          for (int q = 0; q < 32; q += 4)
-            *reinterpret_cast<float4 *>(dst + c * 32 + q) =
-                make_float4(__uint_as_float(o[q]) * inv, __uint_as_float(o[q + 1]) * inv,
-                            __uint_as_float(o[q + 2]) * inv, __uint_as_float(o[q + 3]) * inv);
-        }
+        for (int q = 0; q < 32; q += 4)
+          *reinterpret_cast<float4 *>(srow + (c * 32 + q) * 4) =
+              make_float4(__uint_as_float(o[q]) * inv, __uint_as_float(o[q + 1]) * inv,
+                          __uint_as_float(o[q + 2]) * inv, __uint_as_float(o[q + 3]) * inv);
       }
       if (row_ok)
         ws.lse[(size_t)p * ws.rows_pad + r] = l > 0.f ? (m_used + log2f(l)) * LN2 : -INFINITY;
+    }
+    // the four softmax warps meet (named barrier 1, 128 threads); each then writes 32 rows
+    const int wall = __syncthreads_and_named(wok);
+    if (wall) {
+      float *dst0 = ws.opart + ((size_t)p * ws.rows_pad + row0) * ATTN_D;
+      for (int rr = warp * 32; rr < warp * 32 + 32; ++rr) {
+        if (row0 + rr >= g * n) break;  // rows past the tree are never read
+        const float4 v = *reinterpret_cast<const float4 *>(base + Smem::RING + rr * PITCH + lane * 16);
+        *reinterpret_cast<float4 *>(dst0 + (size_t)rr * ATTN_D + lane * 4) = v;
+      }
     }
   }
 
