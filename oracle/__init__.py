@@ -10,6 +10,7 @@ from .step import (  # noqa: F401
     TreeError,
     bf16_to_f64,
     graft_expand,
+    kv_commit,
     prune_topB,
     stage_budget,
     step_tree_phase,

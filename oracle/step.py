@@ -362,6 +362,39 @@ def succ_update(table, tokens, topk_id, n_nodes):
 
 
 # --------------------------------------------------------------------------------------
+# KV commit: compaction of the accepted path's cache rows
+# --------------------------------------------------------------------------------------
+
+
+def kv_commit(K, Vc, kv_src, kv_dst, acc_len):
+    """Move the accepted path's K/V rows to the committed positions ([TreeGraft] §一: keep
+    the agreeing prefix, drop the rest; [Graft] §二 third gear: the verified tokens join the
+    context).
+
+    For every request b and j = 0..acc_len[b], row kv_dst[b][j] of every KV head ends up
+    holding what row kv_src[b][j] held before the commit; no other row changes. Written as
+    its definition: every source row is read from the unchanged cache, then written.
+    K, Vc: [B][Hkv][Lcap][d]; kv_src, kv_dst: [B][>= acc_len + 1]. Returns new copies.
+    """
+    K = np.array(K, copy=True)
+    Vc = np.array(Vc, copy=True)
+    B, _, Lcap, _ = K.shape
+    K0, V0 = K.copy(), Vc.copy()
+    for b in range(B):
+        L = int(acc_len[b])
+        if L < 0 or L + 1 > len(kv_src[b]):
+            raise OracleError("accepted length outside the path buffer")
+        src = [int(x) for x in kv_src[b][:L + 1]]
+        dst = [int(x) for x in kv_dst[b][:L + 1]]
+        if any(not 0 <= x < Lcap for x in src + dst):
+            raise OracleError("cache row outside the cache")
+        for j in range(L + 1):
+            K[b, :, dst[j]] = K0[b, :, src[j]]
+            Vc[b, :, dst[j]] = V0[b, :, src[j]]
+    return K, Vc
+
+
+# --------------------------------------------------------------------------------------
 # whole step
 # --------------------------------------------------------------------------------------
 
