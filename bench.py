@@ -423,9 +423,10 @@ def call_breakdown(torch, gt, buf, sets, scn, nsets, reps: int = 50):
     """Average device time of each C-ABI call of the step inside a CUDA graph: one graph
     per input set with an externally visible event between consecutive calls (the events
     also end the programmatic overlap between the calls, so the sum exceeds the step)."""
-    from tree_speculative_decoding_parent_gb300.step import (run_attn, run_tree_build,
-                                                             run_verify_commit)
-    names = ["gt_tree_build", "gt_tree_attn", "gt_verify_commit"]
+    from tree_speculative_decoding_parent_gb300.step import (run_attn, run_kv_commit,
+                                                             run_tree_build, run_verify_commit)
+    # the KV commit (compaction of the accepted rows) is timed too; it is not part of the step
+    names = ["gt_tree_build", "gt_tree_attn", "gt_verify_commit", "gt_kv_commit (not in step)"]
     graphs = []
     for k in range(nsets):
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
@@ -443,6 +444,8 @@ def call_breakdown(torch, gt, buf, sets, scn, nsets, reps: int = 50):
             gt.gt_event_record_external(evs[2], s)
             run_verify_commit(buf, inp, s)
             gt.gt_event_record_external(evs[3], s)
+            run_kv_commit(buf, inp, s)
+            gt.gt_event_record_external(evs[4], s)
         graphs.append((g, evs))
     tot = [0.0] * len(names)
     for r in range(reps):

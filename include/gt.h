@@ -213,6 +213,26 @@ int gt_verify_greedy(const float *logits, const int32_t *tokens, const int32_t *
                      int32_t *err, gt_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
+ * KV commit: compaction of the accepted path's cache rows.  [TreeGraft] §一 (keep the
+ * agreeing prefix, drop the rest); [Graft] §二 third gear (the verified tokens join the
+ * context).
+ *
+ * In place, for every request b and j = 0..acc_len[b]: row kv_dst[b][j] of every KV head
+ * of K and V receives the row that was at kv_src[b][j] before the call (the outputs of
+ * gt_verify_greedy / gt_verify_commit: src = prefix_len + path[j], dst = prefix_len + j).
+ * Every source is read before any destination is written, so a destination may be the
+ * source of another j. No other row changes.
+ *   device in/out: K, V [B][Hkv][Lcap][d] (dtype), 16-byte aligned
+ *   device in    : kv_src, kv_dst i32 [B][N]; acc_len i32 [B]
+ * Limits: 1 <= N <= 64, d * element size a multiple of 16 bytes and at most 1024.
+ * Device errors: GT_ERR_RANGE (acc_len outside [0, N), a row outside [0, Lcap)); such a
+ * request's rows stay as they were.
+ * ------------------------------------------------------------------------------------- */
+int gt_kv_commit(void *K, void *V, const int32_t *kv_src, const int32_t *kv_dst,
+                 const int32_t *acc_len, int B, int N, int Hkv, int d, int Lcap, int dtype,
+                 int32_t *err, gt_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
  * a7. Online successor-table update.  [Graft] §二 (third gear), §六.
  *
  * For every verified node (b, v), v < n_nodes[b], accepted or not: row tokens[b][v] of

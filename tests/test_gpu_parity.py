@@ -215,3 +215,74 @@ def test_device_errors_are_reported():
     # host-visible errors raise without launching
     with pytest.raises(gt.GTError):
         gt.gt_vocab_topk(inp["logits"], 1, scn.V, 17, buf.topk_id, buf.topk_val)
+
+
+# ------------------------------------------------------------------------------ KV commit
+
+
+def _bits(x: torch.Tensor) -> np.ndarray:
+    """Raw element bits of a device tensor (bf16 -> uint16, fp32 -> uint32)."""
+    if x.dtype == torch.bfloat16:
+        return np_(x.view(torch.int16)).view(np.uint16)
+    return np_(x).view(np.uint32)
+
+
+def _host_bits(a: np.ndarray) -> np.ndarray:
+    return a.view(np.uint16) if a.dtype == np.uint16 else np.ascontiguousarray(a, np.float32).view(np.uint32)
+
+
+@pytest.mark.parametrize("cid", [1, 2])
+def test_kv_commit_after_step(cid):
+    scn = make_scenario(cid, **SMALL[cid])
+    tree = oracle_tree(scn)
+    logits = scn.logits(tree["parent"], tree["tokens"], tree["n_nodes"])
+    buf, inp = run_gpu_step(scn, logits)
+    res = oracle.step_verify_phase(tree, logits, scn.table, scn.prefix_len, scn.k)
+    s = shape_of(scn)
+    gt.gt_kv_commit(inp["K"], inp["V"], buf.kv_src, buf.kv_dst, buf.acc_len, s.B, s.N, s.Hkv,
+                    s.d, s.Lcap, s.dtype, buf.err)
+    torch.cuda.synchronize()
+    assert buf.err.item() == 0
+    Ke, Ve = oracle.kv_commit(scn.K, scn.Vc, res["kv_src"], res["kv_dst"], res["acc_len"])
+    assert np.array_equal(_bits(inp["K"]), _host_bits(Ke))
+    assert np.array_equal(_bits(inp["V"]), _host_bits(Ve))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_kv_commit_random_paths_and_bad_requests(dtype):
+    rng = np.random.default_rng(11)
+    B, Hkv, N, d, Lcap = 9, 3, 64, 128, 300
+    P = rng.integers(0, Lcap - N, size=B).astype(np.int32)
+    L = rng.integers(0, N, size=B).astype(np.int32)
+    L[0] = N - 1                                   # the longest path the buffers hold
+    src = np.full((B, N), -1, np.int32)
+    dst = np.full((B, N), -1, np.int32)
+    for b in range(B):
+        # a root path of an N-node tree: node indices increase, path[j] >= j, and
+        # consecutive nodes are often adjacent, so destinations overlap later sources
+        nodes = np.sort(rng.choice(np.arange(1, N), size=L[b], replace=False))
+        path = np.concatenate([[0], nodes])
+        src[b, :L[b] + 1] = P[b] + path
+        dst[b, :L[b] + 1] = P[b] + np.arange(L[b] + 1)
+    bad = [3, 6]
+    L[3] = N                                       # accepted length past the path buffer
+    src[6, 1] = Lcap + 5                           # a row outside the cache
+    x = rng.standard_normal((2, B, Hkv, Lcap, d)).astype(np.float32)
+    if dtype == "bf16":
+        from workload import f32_to_bf16_bits
+        host = [f32_to_bf16_bits(x[0]), f32_to_bf16_bits(x[1])]
+        dev = [torch.from_numpy(h.view(np.int16)).view(torch.bfloat16).cuda() for h in host]
+    else:
+        host = [x[0], x[1]]
+        dev = [torch.from_numpy(h.copy()).cuda() for h in host]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gt.gt_kv_commit(dev[0], dev[1], _t(src), _t(dst), _t(L), B, N, Hkv, d, Lcap,
+                    gt.GT_BF16 if dtype == "bf16" else gt.GT_F32, err)
+    torch.cuda.synchronize()
+    assert err.item() == gt.GT_ERR_RANGE
+    good = [b for b in range(B) if b not in bad]
+    Ke, Ve = oracle.kv_commit(host[0][good], host[1][good], src[good], dst[good], L[good])
+    for got, want, orig in ((dev[0], Ke, host[0]), (dev[1], Ve, host[1])):
+        g_bits = _bits(got)
+        assert np.array_equal(g_bits[good], _host_bits(want))
+        assert np.array_equal(g_bits[bad], _host_bits(orig[bad]))   # bad requests untouched

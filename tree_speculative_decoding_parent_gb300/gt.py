@@ -30,6 +30,7 @@ _SIGS = {
     "gt_tree_attn_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f,
                                   _vp, _vp, _vp]),
     "gt_vocab_topk": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp]),
+    "gt_kv_commit": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp]),
     "gt_verify_greedy": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp,
                               _vp, _vp, _vp, _vp]),
     "gt_succ_update": (_i, [_vp, _i, _i, _vp, _vp, _vp, _i, _i, _vp, _vp]),
@@ -148,6 +149,12 @@ def gt_tree_attn_noalloc(Q, K, V, mask, prefix_len, n_nodes, B, N, Hq, Hkv, d, L
     _check("gt_tree_attn_noalloc", load().gt_tree_attn_noalloc(
         _p(Q), _p(K), _p(V), _p(mask), _p(prefix_len), _p(n_nodes), B, N, Hq, Hkv, d, Lcap,
         dtype, float(scale), _p(O), _p(err), _s(stream)))
+
+
+def gt_kv_commit(K, V, kv_src, kv_dst, acc_len, B, N, Hkv, d, Lcap, dtype, err, stream=None):
+    _check("gt_kv_commit", load().gt_kv_commit(
+        _p(K), _p(V), _p(kv_src), _p(kv_dst), _p(acc_len), B, N, Hkv, d, Lcap, dtype, _p(err),
+        _s(stream)))
 
 
 def gt_vocab_topk(logits, rows, V, k, ids, vals, stream=None):

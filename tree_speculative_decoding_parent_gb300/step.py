@@ -125,6 +125,13 @@ def run_verify_commit(buf: StepBuffers, inp: dict, stream=None):
                         buf.out_tok, buf.kv_src, buf.kv_dst, inp["table"], buf.err, stream)
 
 
+def run_kv_commit(buf: StepBuffers, inp: dict, stream=None):
+    """Move the accepted path's K/V rows to their committed positions (in place)."""
+    s = buf.shape
+    gt.gt_kv_commit(inp["K"], inp["V"], buf.kv_src, buf.kv_dst, buf.acc_len, s.B, s.N, s.Hkv,
+                    s.d, s.Lcap, s.dtype, buf.err, stream)
+
+
 def run_step(buf: StepBuffers, inp: dict, stream=None, scale=None, fused: bool = True):
     """The whole verify-and-graft step (a1..a7) on one stream, no host synchronisation."""
     if fused:
