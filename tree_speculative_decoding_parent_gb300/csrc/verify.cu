@@ -321,19 +321,41 @@ topk_cluster_kernel(const float *__restrict__ logits, int row0, int V, int k,
   }
 }
 
+template <int KK, int CL>
+static int topk_launch_cl(const float *logits, int r0, int nr, int V, int k, int32_t *ids,
+                          float *vals, cudaStream_t s) {
+  return launch_cluster(topk_cluster_kernel<KK, CL>, dim3(CL, nr), dim3(TOPK_THREADS),
+                        dim3(CL, 1, 1), 0, s, logits, r0, V, k, ids, vals);
+}
+
+template <int KK>
+static int topk_launch_k(const float *logits, int r0, int nr, int V, int k, int32_t *ids,
+                         float *vals, int cl, cudaStream_t s) {
+  switch (cl) {
+    case 2: return topk_launch_cl<KK, 2>(logits, r0, nr, V, k, ids, vals, s);
+    case 4: return topk_launch_cl<KK, 4>(logits, r0, nr, V, k, ids, vals, s);
+    default: return topk_launch_cl<KK, TOPK_CLUSTER>(logits, r0, nr, V, k, ids, vals, s);
+  }
+}
+
 static int topk_launch(const float *logits, int rows, int V, int k, int32_t *ids, float *vals,
                        cudaStream_t s) {
+  // CTAs per row: enough that the rows fill the GPU with about four CTAs per SM, and at
+  // least two. Each split costs one more merge per row, while a whole-row CTA takes its
+  // threshold from too small a first chunk of a long row and overflows its candidate
+  // buffer (measured at 960 rows of 151,936: 2 CTAs 103 us, 8 CTAs 117 us, 1 CTA 256 us).
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    sms = 148;
+  }
+  int cl = 2;
+  while (cl < TOPK_CLUSTER && (long long)rows * cl < 4ll * sms) cl *= 2;
   for (int r0 = 0; r0 < rows; r0 += 65535) {
     const int nr = min(65535, rows - r0);
-    int rc;
-    if (k <= 8)
-      rc = launch_cluster(topk_cluster_kernel<8, TOPK_CLUSTER>, dim3(TOPK_CLUSTER, nr),
-                          dim3(TOPK_THREADS), dim3(TOPK_CLUSTER, 1, 1), 0, s, logits, r0, V, k,
-                          ids, vals);
-    else
-      rc = launch_cluster(topk_cluster_kernel<16, TOPK_CLUSTER>, dim3(TOPK_CLUSTER, nr),
-                          dim3(TOPK_THREADS), dim3(TOPK_CLUSTER, 1, 1), 0, s, logits, r0, V, k,
-                          ids, vals);
+    const int rc = k <= 8 ? topk_launch_k<8>(logits, r0, nr, V, k, ids, vals, cl, s)
+                          : topk_launch_k<16>(logits, r0, nr, V, k, ids, vals, cl, s);
     if (rc != GT_OK) return rc;
   }
   return GT_OK;
@@ -455,7 +477,9 @@ update_kernel(int32_t *__restrict__ table, int V, int k, const int32_t *__restri
 // ------------------------------------------------------------------------------------
 // a6 + a7 fused: CTA b walks request b's tree (as walk_kernel) and then writes the table
 // rows its verified nodes win (as update_kernel: the largest linear index b*N + v of a
-// token wins). Every CTA stages the tokens of all requests in shared memory for that test.
+// token wins). Every CTA stages the tokens of all requests in shared memory for that test
+// and, when it fits, hashes them (open addressing, token -> largest index) so that the
+// test is one lookup per node instead of a scan of every later node.
 // ------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024)
 walk_update_kernel(const int32_t *__restrict__ tokens, const int32_t *__restrict__ parent,
@@ -463,12 +487,14 @@ walk_update_kernel(const int32_t *__restrict__ tokens, const int32_t *__restrict
                    int B, int N, int k, const int32_t *__restrict__ topk_id,
                    int32_t *__restrict__ acc_len, int32_t *__restrict__ path,
                    int32_t *__restrict__ out_tok, int32_t *__restrict__ kv_src,
-                   int32_t *__restrict__ kv_dst, int32_t *__restrict__ table, int V,
+                   int32_t *__restrict__ kv_dst, int32_t *__restrict__ table, int V, int hs,
                    int32_t *err) {
   pdl_enter();
   extern __shared__ int s_w[];
   int *s_par = s_w, *s_tok = s_w + N, *s_am = s_w + 2 * N, *s_path = s_w + 3 * N;
   int *s_all = s_w + 4 * N;  // [B*N] verified tokens of every request (-1: none)
+  int *s_hk = s_all + B * N, *s_hv = s_hk + hs;  // [hs] hash keys (tokens) and last indices
+  for (int i = threadIdx.x; i < hs; i += blockDim.x) s_hk[i] = s_hv[i] = -1;
   __shared__ uint32_t s_best[32];
   __shared__ int s_bad;
   const int b = blockIdx.x, v = threadIdx.x;
@@ -546,16 +572,37 @@ walk_update_kernel(const int32_t *__restrict__ tokens, const int32_t *__restrict
   }
   if (v == 0) acc_len[b] = bad ? 0 : L;
   // table rows won by this request's verified nodes
+  auto slot0 = [&](int t) { return (int)(((uint32_t)t * 2654435761u) & (uint32_t)(hs - 1)); };
+  if (hs > 0) {  // hs is a power of two above B*N, so every probe sequence ends
+    for (int i = v; i < total; i += blockDim.x) {
+      const int t = s_all[i];
+      if (t < 0) continue;
+      for (int h = slot0(t);; h = (h + 1) & (hs - 1)) {
+        const int prev = atomicCAS(&s_hk[h], -1, t);
+        if (prev == -1 || prev == t) {
+          atomicMax(&s_hv[h], i);
+          break;
+        }
+      }
+    }
+    __syncthreads();
+  }
   for (int vv = v; vv < N; vv += blockDim.x) {
     const int i = b * N + vv;
     const int t = s_all[i];
     if (t < 0) continue;
     bool last = true;
-    for (int j = i + 1; j < total; ++j)
-      if (s_all[j] == t) {
-        last = false;
-        break;
-      }
+    if (hs > 0) {
+      int h = slot0(t);
+      while (s_hk[h] != t) h = (h + 1) & (hs - 1);
+      last = s_hv[h] == i;
+    } else {
+      for (int j = i + 1; j < total; ++j)
+        if (s_all[j] == t) {
+          last = false;
+          break;
+        }
+    }
     if (!last) continue;
     const int32_t *src = topk_id + (size_t)i * k;
     int32_t *dst = table + (size_t)t * k;
@@ -630,7 +677,13 @@ GT_API int gt_verify_commit(const float *logits, const int32_t *tokens, const in
   int rc = topk_launch(logits, B * N, V, k, topk_id, topk_val, s);
   if (rc != GT_OK) return rc;
   const int threads = (N + 31) / 32 * 32;
-  const size_t smem = sizeof(int) * (4 * (size_t)N + (size_t)B * N);
+  size_t smem = sizeof(int) * (4 * (size_t)N + (size_t)B * N);
+  // the token hash: a power of two at least twice B*N, when it fits (else the scan)
+  int hs = 1;
+  while (hs < 2 * B * N) hs *= 2;
+  if (smem + 2 * sizeof(int) * (size_t)hs > 160 * 1024)
+    hs = 0;
+  smem += 2 * sizeof(int) * (size_t)hs;
   if (smem > 48 * 1024) {
     const cudaError_t e = cudaFuncSetAttribute(
         walk_update_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -638,5 +691,5 @@ GT_API int gt_verify_commit(const float *logits, const int32_t *tokens, const in
   }
   return launch(walk_update_kernel, dim3(B), dim3(threads), smem, s, tokens, parent, n_nodes,
                 prefix_len, B, N, k, topk_id, acc_len, path, out_tok, kv_src, kv_dst, table, V,
-                err);
+                hs, err);
 }
