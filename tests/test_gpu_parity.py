@@ -51,6 +51,19 @@ def test_step_parity_nan_kv_tail_and_zero_prefix():
     _full_check(make_scenario(4, V=4096, P=(0, 200), B=3, stream_len=20000, kv_fill="nan"))
 
 
+def test_step_parity_root_only_trees():
+    # keep = 1 and no graft: every tree is its root alone (one query row per head, an empty
+    # path, the bonus token only)
+    for cid, kw in ((2, dict(V=5000, P=300)), (4, dict(V=4096, P=(0, 200), B=3, stream_len=20000))):
+        scn = make_scenario(cid, **kw)
+        scn.keep[:] = 1
+        scn.R[:] = 0
+        if scn.thresh is not None:
+            scn.thresh[:] = np.float32(np.inf)
+        buf, tree = _full_check(scn)
+        assert (np_(buf.n_nodes) == 1).all() and (np_(buf.acc_len) == 0).all()
+
+
 @pytest.mark.parametrize("cid", [2, 3, 5])
 def test_step_parity_full_size(cid):
     _full_check(make_scenario(cid))
@@ -286,3 +299,66 @@ def test_kv_commit_random_paths_and_bad_requests(dtype):
         g_bits = _bits(got)
         assert np.array_equal(g_bits[good], _host_bits(want))
         assert np.array_equal(g_bits[bad], _host_bits(orig[bad]))   # bad requests untouched
+
+
+# ------------------------------------------------------------------ attention edge shapes
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_tree_attn_edge_shapes(dtype):
+    """Random trees through gt_tree_attn alone, masks from the oracle: a full 64-node mask
+    word, single-node trees, zero prefixes, prefixes on and next to 128-key tile edges,
+    and 8 query heads per KV head (512 query rows of one KV head)."""
+    from workload import f32_to_bf16_bits
+    rng = np.random.default_rng(21)
+    cases = [  # B, N, Hq, Hkv, prefixes, nodes per request (None: N)
+        (1, 64, 8, 8, [0], None),
+        (2, 1, 32, 8, [0, 5], None),
+        (3, 64, 16, 2, [127, 128, 129], [64, 33, 1]),
+        (2, 40, 4, 4, [1000, 255], [40, 17]),
+    ]
+    for B, N, Hq, Hkv, P, nn in cases:
+        d = 128
+        n = np.array(nn if nn else [N] * B, np.int32)
+        P = np.array(P, np.int32)
+        Lcap = int((P + N).max() + 64) // 64 * 64
+        parent = np.full((B, N), -1, np.int32)
+        for b in range(B):
+            parent[b, 1:n[b]] = [rng.integers(0, v) for v in range(1, n[b])]
+        mask = np.zeros((B, N, 1), np.uint64)
+        for b in range(B):
+            _, _, mask[b] = oracle.tree_mask(parent[b], int(n[b]), int(P[b]), N)
+        Q = rng.standard_normal((B, N, Hq, d), dtype=np.float32)
+        K = rng.standard_normal((B, Hkv, Lcap, d), dtype=np.float32)
+        Vv = rng.standard_normal((B, Hkv, Lcap, d), dtype=np.float32)
+        for b in range(B):  # cache rows past each request's length must never be read
+            K[b, :, P[b] + n[b]:] = np.nan
+            Vv[b, :, P[b] + n[b]:] = np.nan
+        if dtype == "bf16":
+            hq, hk, hv = (f32_to_bf16_bits(x) for x in (Q, K, Vv))
+            dev = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).cuda() for x in (hq, hk, hv)]
+            dec = oracle.bf16_to_f64
+            O = torch.empty((B, N, Hq, d), dtype=torch.bfloat16, device="cuda")
+            gdt = gt.GT_BF16
+        else:
+            hq, hk, hv = Q, K, Vv
+            dev = [_t(x) for x in (Q, K, Vv)]
+            dec = lambda a: np.asarray(a, np.float64)  # noqa: E731
+            O = torch.empty((B, N, Hq, d), dtype=torch.float32, device="cuda")
+            gdt = gt.GT_F32
+        wsb = gt.gt_tree_attn_workspace(B, N, Hq, Hkv, d, Lcap)
+        ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        scale = 1.0 / np.sqrt(d)
+        gt.gt_tree_attn(dev[0], dev[1], dev[2], _t(mask), _t(P), _t(n), B, N, Hq, Hkv, d, Lcap,
+                        gdt, scale, O, ws, wsb, err)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        got = O.float().cpu().numpy().astype(np.float64)
+        for b in range(B):
+            L = int(P[b] + n[b])
+            ref = oracle.tree_attn(dec(hq[b]), dec(hk[b][:, :L]), dec(hv[b][:, :L]), parent[b],
+                                   int(n[b]), int(P[b]), scale)
+            e = float(np.abs(got[b, :n[b]] - ref).max())
+            assert e <= TOL[dtype], (B, N, Hq, Hkv, b, e)
+            assert np.all(got[b, n[b]:] == 0.0)

@@ -245,14 +245,24 @@ __global__ void __launch_bounds__(256)
 attn_combine_kernel(const int32_t *__restrict__ n_nodes, int B, int N, int Hq, int Hkv,
                     AttnWs ws, T *__restrict__ O) {
   pdl_enter();
+  constexpr int PRE = 16;  // partials per lane loaded before any arithmetic
   const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (w >= B * N * Hq) return;
   const int hq = w % Hq, i = (w / Hq) % N, b = w / (Hq * N);
   const int g = Hq / Hkv, h = hq / g, r = i * g + (hq - h * g);
   T *dst = O + (size_t)w * ATTN_D + lane * 4;
+  // the node count and the segment's pieces are independent loads: issue them together
   const int n = n_nodes[b];
-  const int2 sg = (i < n) ? ws.seg[b * Hkv + h] : make_int2(0, 0);
-  // the pieces' log-sum-exps are read in parallel across lanes (one round trip per 32)
+  int2 sg = ws.seg[b * Hkv + h];
+  if (i >= n) sg = make_int2(0, 0);  // rows past the tree are zero
+  const size_t stride = (size_t)ws.rows_pad * ATTN_D;
+  const float *src = ws.opart + ((size_t)sg.x * ws.rows_pad + r) * ATTN_D + lane * 4;
+  // the first PRE partials and the log-sum-exps leave in one round trip
+  float4 part[PRE];
+#pragma unroll
+  for (int j = 0; j < PRE; ++j)
+    part[j] = j < sg.y ? *reinterpret_cast<const float4 *>(src + j * stride)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
   float mx = -INFINITY;
   for (int j = lane; j < sg.y; j += 32) mx = fmaxf(mx, ws.lse[(size_t)(sg.x + j) * ws.rows_pad + r]);
 #pragma unroll
@@ -265,16 +275,22 @@ attn_combine_kernel(const int32_t *__restrict__ n_nodes, int B, int N, int Hq, i
       const float myw =
           lane < cnt ? expf(ws.lse[(size_t)(sg.x + j0 + lane) * ws.rows_pad + r] - mx) : 0.f;
       wsum += myw;
-      const float *src = ws.opart + ((size_t)(sg.x + j0) * ws.rows_pad + r) * ATTN_D + lane * 4;
-      const size_t stride = (size_t)ws.rows_pad * ATTN_D;
 #pragma unroll 8
-      for (int j = 0; j < cnt; ++j) {  // independent loads: several partials in flight
+      for (int j = 0; j < cnt; ++j) {
         const float wt = __shfl_sync(0xffffffffu, myw, j);
-        const float4 o = *reinterpret_cast<const float4 *>(src + j * stride);
-        acc.x = fmaf(wt, o.x, acc.x);
-        acc.y = fmaf(wt, o.y, acc.y);
-        acc.z = fmaf(wt, o.z, acc.z);
-        acc.w = fmaf(wt, o.w, acc.w);
+        const int q = j0 + j;
+        float4 v;
+        if (q < PRE) {
+#pragma unroll
+          for (int u = 0; u < PRE; ++u)  // a register, not a local-memory index
+            if (u == q) v = part[u];
+        } else {
+          v = *reinterpret_cast<const float4 *>(src + q * stride);
+        }
+        acc.x = fmaf(wt, v.x, acc.x);
+        acc.y = fmaf(wt, v.y, acc.y);
+        acc.z = fmaf(wt, v.z, acc.z);
+        acc.w = fmaf(wt, v.w, acc.w);
       }
     }
 #pragma unroll
