@@ -149,12 +149,16 @@ def prune_topB(score, parent, tokens, n_in: int, keep: int, thresh: Optional[flo
 # --------------------------------------------------------------------------------------
 
 
-def graft_expand(parent, tokens, n_kept: int, tpar, trank, R: int, table, Nmax: int):
-    """Refill freed slots from the successor table ([Graft] §二, second gear).
+def graft_expand(parent, tokens, n_kept: int, tpar, trank, R: int, table, Nmax: int,
+                 anchor: int = 0):
+    """Refill freed slots from the successor table ([Graft] §二, second gear; §七 for the
+    tail graft of block drafts, Graft-TAIL).
 
-    The retrieved tree hangs from the tree root (the current token). Template node t
+    The retrieved tree hangs from the anchor node: the tree root (the current token) by
+    default; for Graft-TAIL the last kept node of the pruned draft chain (anchor = -1
+    means node n_kept - 1). Template node t
     (t = 0 .. R'-1 with R' = min(R, Nmax - n_kept, T)) has template parent tpar[t]
-    (-1 = root) and successor rank trank[t]; its token is row ``token(parent)`` of the
+    (-1 = the anchor) and successor rank trank[t]; its token is row ``token(parent)`` of the
     table at column ``trank[t]``. An empty entry (-1) drops the node, and with it every
     template descendant. Survivors are appended after the kept nodes in template order.
 
@@ -167,6 +171,9 @@ def graft_expand(parent, tokens, n_kept: int, tpar, trank, R: int, table, Nmax: 
     for t in out_t:
         if not 0 <= t < V:
             raise TreeError("token out of range")
+    a = n_kept - 1 if int(anchor) == -1 else int(anchor)
+    if not 0 <= a < n_kept:
+        raise OracleError("graft anchor outside the kept tree")
     r = max(0, min(int(R), Nmax - n_kept, T))
     node_of = {}
     for t in range(r):
@@ -174,7 +181,7 @@ def graft_expand(parent, tokens, n_kept: int, tpar, trank, R: int, table, Nmax: 
         if not -1 <= tp < t or not 0 <= rank < k:
             raise TreeError("template parent must precede its child; rank < k")
         if tp == -1:
-            pnode = 0
+            pnode = a
         elif tp in node_of:
             pnode = node_of[tp]
         else:
@@ -400,8 +407,9 @@ def kv_commit(K, Vc, kv_src, kv_dst, acc_len):
 
 
 def step_tree_phase(parent_in, tokens_in, score_in, n_in, keep, thresh, tpar, trank, R, table,
-                    prefix_len, N: int):
-    """a1 + a2 + a3 for every request: prune, graft, mask. Returns a dict of arrays."""
+                    prefix_len, N: int, anchor=None):
+    """a1 + a2 + a3 for every request: prune, graft (at anchor[b], default the root),
+    mask. Returns a dict of arrays."""
     B = len(keep)
     W = (N + 63) // 64
     out = dict(parent=np.full((B, N), -1, np.int32), tokens=np.full((B, N), -1, np.int32),
@@ -419,7 +427,8 @@ def step_tree_phase(parent_in, tokens_in, score_in, n_in, keep, thresh, tpar, tr
         out["n_kept"][b] = nk
         out["old_idx"][b, :nk] = o
         out["score"][b, :nk] = s
-        gp, gt, n = graft_expand(p, t, nk, tpar, trank, int(R[b]), table, N)
+        gp, gt, n = graft_expand(p, t, nk, tpar, trank, int(R[b]), table, N,
+                                 0 if anchor is None else int(anchor[b]))
         out["parent"][b], out["tokens"][b], out["n_nodes"][b] = gp, gt, n
         d, ps, m = tree_mask(gp, n, int(prefix_len[b]), N)
         out["depth"][b], out["pos"][b], out["mask"][b] = d, ps, m

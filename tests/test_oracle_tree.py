@@ -332,3 +332,23 @@ def test_update_last_writer_and_untouched_rows():
             assert t[row].tolist() == topk[b, v].tolist()
         else:
             assert t[row].tolist() == table[row].tolist()
+
+
+def test_graft_at_anchor_tail_of_a_chain():
+    # Graft-TAIL: a 5-node chain kept, the retrieved nodes hang from its last node
+    table = np.array([[1, 2], [3, 4], [0, 1], [4, 0], [2, 3]], np.int32)  # V = 5, k = 2
+    parent = [-1, 0, 1, 2, 3, -1, -1, -1, -1, -1]
+    tokens = [0, 1, 3, 4, 2, -1, -1, -1, -1, -1]
+    tpar, trank = [-1, -1, 0], [0, 1, 0]
+    p, t, n = oracle.graft_expand(parent, tokens, 5, tpar, trank, 3, table, 10, anchor=-1)
+    # anchor = node 4 (token 2): children table[2] = (0, 1); grandchild table[0][0] = 1
+    assert n == 8
+    assert p[:8] == [-1, 0, 1, 2, 3, 4, 4, 5]
+    assert t[:8] == [0, 1, 3, 4, 2, 0, 1, 1]
+    # an explicit anchor inside the kept tree, and the default (root) unchanged
+    p2, t2, n2 = oracle.graft_expand(parent, tokens, 5, tpar, trank, 3, table, 10, anchor=2)
+    assert p2[5:8] == [2, 2, 5] and t2[5:8] == [4, 0, 2]
+    assert oracle.graft_expand(parent, tokens, 5, tpar, trank, 3, table, 10, anchor=0) == \
+        oracle.graft_expand(parent, tokens, 5, tpar, trank, 3, table, 10)
+    with pytest.raises(oracle.OracleError):
+        oracle.graft_expand(parent, tokens, 5, tpar, trank, 3, table, 10, anchor=5)
