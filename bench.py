@@ -175,7 +175,7 @@ def time_oracle(scn, steps: int, budget_s: float):
     import oracle
     tree = oracle.step_tree_phase(scn.parent_in, scn.tokens_in, scn.score_in,
                                   [scn.Nin] * scn.B, scn.keep, scn.thresh, scn.tpar, scn.trank,
-                                  scn.R, scn.table, scn.prefix_len, scn.N)
+                                  scn.R, scn.table, scn.prefix_len, scn.N, anchor=scn.anchor)
     logits = scn.logits(tree["parent"], tree["tokens"], tree["n_nodes"])
     dec = oracle.bf16_to_f64 if scn.dtype == "bf16" else (lambda a: np.asarray(a, np.float64))
     done, t0 = 0, time.perf_counter()
@@ -183,7 +183,8 @@ def time_oracle(scn, steps: int, budget_s: float):
     while done < steps:
         tree = oracle.step_tree_phase(scn.parent_in, scn.tokens_in, scn.score_in,
                                       [scn.Nin] * scn.B, scn.keep, scn.thresh, scn.tpar,
-                                      scn.trank, scn.R, table, scn.prefix_len, scn.N)
+                                      scn.trank, scn.R, table, scn.prefix_len, scn.N,
+                                      anchor=scn.anchor)
         for b in range(scn.B):
             n, P = int(tree["n_nodes"][b]), int(scn.prefix_len[b])
             oracle.tree_attn(dec(scn.Q[b]), dec(scn.K[b][:, :P + n]), dec(scn.Vc[b][:, :P + n]),
@@ -254,6 +255,8 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
                 Q=qkv(scn.Q), K=qkv(scn.K), V=qkv(scn.Vc))
     if scn.thresh is not None:
         base["thresh"] = to_dev(scn.thresh)
+    if scn.anchor is not None:
+        base["anchor"] = to_dev(scn.anchor)
     if len(scn.tpar):
         base["tpar"], base["trank"] = to_dev(scn.tpar), to_dev(scn.trank)
     # plant the target logits on the tree this GPU path builds from the inputs
@@ -333,8 +336,9 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     # ---- end to end through host buffers: H2D of the step's inputs, D2H of its result
     pin = lambda t: t.cpu().pin_memory()  # noqa: E731
     h_tree = {k: pin(base[k]) for k in ("score_in", "parent_in", "tokens_in", "keep", "R")}
-    if "thresh" in base:
-        h_tree["thresh"] = pin(base["thresh"])
+    for key in ("thresh", "anchor"):
+        if key in base:
+            h_tree[key] = pin(base[key])
     h_q = pin(base["Q"])
     P = scn.prefix_len
     h_kv = [(pin(base["K"][b, :, P[b]:P[b] + scn.N]), pin(base["V"][b, :, P[b]:P[b] + scn.N]))

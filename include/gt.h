@@ -89,23 +89,29 @@ int gt_prune_topB(const float *score, const int32_t *parent, const int32_t *toke
                   gt_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
- * a2. Graft retrieved nodes into the freed slots.  [Graft] §二 (second gear), §四.
+ * a2. Graft retrieved nodes into the freed slots.  [Graft] §二 (second gear), §四;
+ *     Graft-TAIL: [Graft] §一 (the suffix of a drafter's chain is extended by retrieval).
  *
- * In place on the kept trees. For request b with n = n_nodes[b] kept nodes, template
+ * In place on the kept trees. For request b with n = n_nodes[b] kept nodes, the
+ * retrieved tree hangs from the anchor node a = anchor[b] (anchor NULL: a = 0, the root;
+ * anchor[b] = -1: a = n - 1, the last kept node, i.e. the tail of a pruned chain). Template
  * nodes t = 0 .. R'-1, R' = min(R[b], Nmax - n, T), are tried in order: template parent
- * tpar[t] (-1 = the tree root, else an earlier template node) and successor rank
+ * tpar[t] (-1 = the anchor, else an earlier template node) and successor rank
  * trank[t]; the node's token is table[token(parent)][trank[t]]. An empty entry (-1)
  * drops the node and all its template descendants. Survivors are appended at n, n+1, ...
  * in template order; slots from the new count to Nmax-1 are set to -1.
  *   device in/out: parent, tokens i32 [B][Nmax]; n_nodes i32 [B] (in: kept, out: total)
- *   device in    : tpar, trank i32 [T]; R i32 [B]; table i32 [V][k] (entries in [-1, V))
+ *   device in    : tpar, trank i32 [T]; R i32 [B]; anchor i32 [B] (nullable);
+ *                  table i32 [V][k] (entries in [-1, V))
  * Limits: 0 <= T <= 1024, k >= 1, V >= 1. Device errors: GT_ERR_TREE (template parent
  * not earlier, rank >= k, a token or table entry outside its range), GT_ERR_RANGE
- * (n_nodes outside [1, Nmax]).
+ * (n_nodes outside [1, Nmax], or the anchor outside the kept tree: that request keeps its
+ * tree and grafts nothing).
  * ------------------------------------------------------------------------------------- */
 int gt_graft_expand(int32_t *parent, int32_t *tokens, int32_t *n_nodes, int B, int Nmax,
                     const int32_t *tpar, const int32_t *trank, int T, const int32_t *R,
-                    const int32_t *table, int V, int k, int32_t *err, gt_stream_t stream);
+                    const int32_t *anchor, const int32_t *table, int V, int k, int32_t *err,
+                    gt_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
  * a3. Ancestor mask and tree position ids.  [Graft] §二 (third gear).
@@ -256,7 +262,8 @@ int gt_succ_update(int32_t *table, int V, int k, const int32_t *tokens,
  *   one CTA per request holding the tree in shared memory. [TreeGraft] §三, §四 How;
  *   [Graft] §二, §四. Outputs: parent, tokens i32 [B][N] (final tree, -1 padded);
  *   out_score f32 / out_old_idx i32 [B][N] (kept nodes, nullable); n_nodes i32 [B] (final
- *   count); depth, pos i32 [B][N]; mask u64 [B][N][ceil(N/64)].
+ *   count); depth, pos i32 [B][N]; mask u64 [B][N][ceil(N/64)]. anchor i32 [B] (nullable)
+ *   as in gt_graft_expand, counted in the pruned tree.
  *   Limits: 1 <= Nin, N <= 1024, 0 <= T <= 1024.
  * gt_verify_commit = gt_verify_greedy -> gt_succ_update on `table` i32 [V][k] (in place).
  *   [Graft] §二 (third gear), §六; [TreeGraft] §一, §三. Limits: N <= 1024, k <= 16,
@@ -265,7 +272,8 @@ int gt_succ_update(int32_t *table, int V, int k, const int32_t *tokens,
 int gt_tree_build(const float *score, const int32_t *parent_in, const int32_t *tokens_in,
                   const int32_t *n_in, int B, int Nin, const int32_t *keep, const float *thresh,
                   const int32_t *tpar, const int32_t *trank, int T, const int32_t *R,
-                  const int32_t *table, int V, int k, const int32_t *prefix_len, int N,
+                  const int32_t *anchor, const int32_t *table, int V, int k,
+                  const int32_t *prefix_len, int N,
                   int32_t *parent, int32_t *tokens, float *out_score, int32_t *out_old_idx,
                   int32_t *n_nodes, int32_t *depth, int32_t *pos, uint64_t *mask, int32_t *err,
                   gt_stream_t stream);

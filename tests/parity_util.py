@@ -29,6 +29,8 @@ def device_inputs(scn, logits: np.ndarray, dev="cuda") -> dict:
              logits=t(logits))
     if scn.thresh is not None:
         d["thresh"] = t(scn.thresh)
+    if scn.anchor is not None:
+        d["anchor"] = t(scn.anchor)
     if len(scn.tpar):
         d["tpar"], d["trank"] = t(scn.tpar), t(scn.trank)
     if scn.dtype == "bf16":
@@ -41,7 +43,7 @@ def device_inputs(scn, logits: np.ndarray, dev="cuda") -> dict:
 def oracle_tree(scn) -> dict:
     return oracle.step_tree_phase(scn.parent_in, scn.tokens_in, scn.score_in, [scn.Nin] * scn.B,
                                   scn.keep, scn.thresh, scn.tpar, scn.trank, scn.R, scn.table,
-                                  scn.prefix_len, scn.N)
+                                  scn.prefix_len, scn.N, anchor=scn.anchor)
 
 
 def decode(x: np.ndarray, dtype: str) -> np.ndarray:

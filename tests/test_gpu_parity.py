@@ -9,7 +9,8 @@ import oracle
 from parity_util import (TOL, attn_max_err, compare_tree, compare_verify, device_inputs, np_,
                          oracle_tree, run_gpu_step, shape_of)
 from tree_speculative_decoding_parent_gb300 import gt
-from tree_speculative_decoding_parent_gb300.step import StepBuffers, run_step
+from tree_speculative_decoding_parent_gb300.step import (StepBuffers, run_step, run_tree_build,
+                                                         run_tree_phase)
 from workload import make_scenario
 
 pytestmark = pytest.mark.gpu
@@ -159,7 +160,7 @@ def test_graft_with_empty_entries():
         R = rng.integers(0, 60, size=B).astype(np.int32)
         dp, dtk, dn = _t(parent), _t(tokens), _t(nk)
         err = torch.zeros(1, dtype=torch.int32, device="cuda")
-        gt.gt_graft_expand(dp, dtk, dn, B, Nmax, _t(tpar), _t(trank), 52, _t(R), _t(table), V, k,
+        gt.gt_graft_expand(dp, dtk, dn, B, Nmax, _t(tpar), _t(trank), 52, _t(R), None, _t(table), V, k,
                            err)
         torch.cuda.synchronize()
         assert err.item() == 0
@@ -168,6 +169,78 @@ def test_graft_with_empty_entries():
                                           table, Nmax)
             assert np_(dn)[b] == n
             assert np_(dp)[b].tolist() == p and np_(dtk)[b].tolist() == t
+
+
+def test_graft_at_anchors_and_bad_anchor():
+    """Graft-TAIL: the retrieved tree hangs from anchor[b] (-1 = the last kept node)."""
+    rng = np.random.default_rng(13)
+    from workload import default_template
+    V, k, B, Nmax = 50, 8, 8, 60
+    tpar, trank = default_template(52, k)
+    for trial in range(4):
+        table = rng.integers(0, V, size=(V, k)).astype(np.int32)
+        table[rng.random((V, k)) < 0.2] = -1
+        nk = rng.integers(1, 24, size=B).astype(np.int32)
+        parent = np.full((B, Nmax), -1, np.int32)
+        tokens = np.full((B, Nmax), -1, np.int32)
+        for b in range(B):
+            parent[b, 1:nk[b]] = [rng.integers(0, v) for v in range(1, nk[b])]
+            tokens[b, :nk[b]] = rng.integers(0, V, size=nk[b])
+        anchor = np.array([-1, 0] + [int(rng.integers(0, nk[b])) for b in range(2, B)], np.int32)
+        bad = trial % 2 == 1
+        if bad:  # request 3 names a node past its kept tree: it keeps its tree, no graft
+            anchor[3] = nk[3]
+        R = rng.integers(0, 60, size=B).astype(np.int32)
+        dp, dtk, dn = _t(parent), _t(tokens), _t(nk)
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        gt.gt_graft_expand(dp, dtk, dn, B, Nmax, _t(tpar), _t(trank), 52, _t(R), _t(anchor),
+                           _t(table), V, k, err)
+        torch.cuda.synchronize()
+        assert err.item() == (gt.GT_ERR_RANGE if bad else 0)
+        for b in range(B):
+            if bad and b == 3:
+                p, t, n = oracle.graft_expand(parent[b], tokens[b], int(nk[b]), tpar, trank, 0,
+                                              table, Nmax)
+            else:
+                p, t, n = oracle.graft_expand(parent[b], tokens[b], int(nk[b]), tpar, trank,
+                                              int(R[b]), table, Nmax, int(anchor[b]))
+            assert np_(dn)[b] == n
+            assert np_(dp)[b].tolist() == p and np_(dtk)[b].tolist() == t
+
+
+@pytest.mark.parametrize("fused", [True, False], ids=["fused", "separate"])
+def test_step_parity_dflash_tail(fused):
+    """A 16-token block draft: threshold prune to a prefix, graft at the prefix's tail."""
+    scn = make_scenario(6, V=4099, P=777, B=6, stream_len=50000)
+    buf, tree = _full_check(scn, fused=fused)
+    for b in range(scn.B):
+        nk, n = int(tree["n_kept"][b]), int(tree["n_nodes"][b])
+        assert tree["parent"][b][:nk].tolist() == list(range(-1, nk - 1))  # a kept prefix
+        assert all(tree["parent"][b][v] >= nk - 1 for v in range(nk, n))  # below the tail
+    assert len(set(tree["n_kept"].tolist())) > 1  # the thresholds keep prefixes of several lengths
+
+
+def test_step_parity_dflash_tail_full_size():
+    _full_check(make_scenario(6))
+
+
+@pytest.mark.parametrize("fused", [True, False], ids=["fused", "separate"])
+def test_tree_phase_bad_anchor_keeps_the_pruned_tree(fused):
+    scn = make_scenario(6, V=3001, P=200, B=3, stream_len=20000)
+    nk = oracle_tree(scn)["n_kept"]
+    scn.anchor = np.array([-1, nk[1], 0], np.int32)  # request 1: one past its kept tree
+    shape = shape_of(scn)
+    buf = StepBuffers(shape)
+    inp = device_inputs(scn, np.zeros((scn.B, scn.N, scn.V), np.float32))
+    (run_tree_build if fused else run_tree_phase)(buf, inp)
+    torch.cuda.synchronize()
+    assert int(buf.err.item()) == gt.GT_ERR_RANGE
+    R = scn.R.copy()
+    R[1] = 0
+    want = oracle.step_tree_phase(scn.parent_in, scn.tokens_in, scn.score_in, [scn.Nin] * scn.B,
+                                  scn.keep, scn.thresh, scn.tpar, scn.trank, R, scn.table,
+                                  scn.prefix_len, scn.N, anchor=np.array([-1, 0, 0], np.int32))
+    compare_tree(buf, want)
 
 
 def test_prune_ties_and_threshold():

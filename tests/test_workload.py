@@ -59,3 +59,13 @@ def test_scenarios_small_are_valid_and_reproducible():
     assert make_scenario(1, V=3000, P=100).Nin == 411
     assert make_scenario(5, V=3000, P=100).Nin == 256
     assert make_scenario(4, V=3000, P=(100, 200), B=2).Nin == 60
+
+
+def test_block_draft_is_a_chain_with_falling_scores():
+    s = make_scenario(6, V=3000, P=100, B=4, stream_len=20000)
+    assert s.Nin == 17 and s.N == 17 and s.anchor.tolist() == [-1] * 4
+    for b in range(s.B):
+        assert s.parent_in[b].tolist() == list(range(-1, 16))
+        assert np.all(np.diff(s.score_in[b].astype(np.float64)) < 0)
+        # the threshold lies strictly inside the chain's score range
+        assert s.score_in[b, -1] < s.thresh[b] < s.score_in[b, 1]

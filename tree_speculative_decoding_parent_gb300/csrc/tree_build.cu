@@ -22,7 +22,8 @@ tree_build_kernel(const float *__restrict__ score, const int32_t *__restrict__ p
                   const int32_t *__restrict__ tokens_in, const int32_t *__restrict__ n_in,
                   int Nin, const int32_t *__restrict__ keep, const float *__restrict__ thresh,
                   const int32_t *__restrict__ tpar, const int32_t *__restrict__ trank, int T,
-                  const int32_t *__restrict__ R, const int32_t *__restrict__ table, int V, int k,
+                  const int32_t *__restrict__ R, const int32_t *__restrict__ anchor,
+                  const int32_t *__restrict__ table, int V, int k,
                   const int32_t *__restrict__ prefix_len, int N, int W,
                   int32_t *__restrict__ parent, int32_t *__restrict__ tokens,
                   float *__restrict__ out_score, int32_t *__restrict__ out_old,
@@ -113,8 +114,18 @@ tree_build_kernel(const float *__restrict__ score, const int32_t *__restrict__ p
   __syncthreads();
 
   // ---------------------------------------------------------------- phase B: graft
-  const int root_tok = s_tok[0];
-  code = (root_tok < 0 || root_tok >= V) ? GT_ERR_TREE : 0;
+  // the retrieved tree hangs from the anchor: the root, or (Graft-TAIL) the last kept node
+  int a = 0;
+  code = 0;
+  if (anchor) {
+    a = anchor[b] == -1 ? nk - 1 : anchor[b];
+    if (a < 0 || a >= nk) {
+      code = GT_ERR_RANGE;
+      a = 0;
+    }
+  }
+  const int root_tok = s_tok[a];
+  if (!code && (root_tok < 0 || root_tok >= V)) code = GT_ERR_TREE;
   const int r = code ? 0 : max(0, min(min(R[b], N - nk), T));
   const bool active = t < r;
   int tp = -1, rk = 0;
@@ -158,7 +169,7 @@ tree_build_kernel(const float *__restrict__ score, const int32_t *__restrict__ p
     if (active) s_tnew[t] = gi;
     __syncthreads();
     if (alive) {
-      s_par[nk + gi] = (tp == -1) ? 0 : nk + s_tnew[tp];
+      s_par[nk + gi] = (tp == -1) ? a : nk + s_tnew[tp];
       s_tok[nk + gi] = s_ttok[t];
     }
     n_final = nk + cnt;
@@ -208,7 +219,8 @@ using namespace gt;
 GT_API int gt_tree_build(const float *score, const int32_t *parent_in, const int32_t *tokens_in,
                          const int32_t *n_in, int B, int Nin, const int32_t *keep,
                          const float *thresh, const int32_t *tpar, const int32_t *trank, int T,
-                         const int32_t *R, const int32_t *table, int V, int k,
+                         const int32_t *R, const int32_t *anchor, const int32_t *table, int V,
+                         int k,
                          const int32_t *prefix_len, int N, int32_t *parent, int32_t *tokens,
                          float *out_score, int32_t *out_old_idx, int32_t *n_nodes,
                          int32_t *depth, int32_t *pos, uint64_t *mask, int32_t *err,
@@ -224,7 +236,7 @@ GT_API int gt_tree_build(const float *score, const int32_t *parent_in, const int
   const int threads = (max(max(Nin, N), Tb) + 31) / 32 * 32;
   const size_t smem = sizeof(int) * ((size_t)((Nin + 3) & ~3) + Nin + 2 * (size_t)N + 3 * (size_t)Tb);
   return launch(tree_build_kernel, dim3(B), dim3(threads), smem, (cudaStream_t)stream, score,
-                parent_in, tokens_in, n_in, Nin, keep, thresh, tpar, trank, T, R, table, V, k,
+                parent_in, tokens_in, n_in, Nin, keep, thresh, tpar, trank, T, R, anchor, table, V, k,
                 prefix_len, N, W, parent, tokens, out_score, out_old_idx, n_nodes, depth, pos,
                 mask, err);
 }

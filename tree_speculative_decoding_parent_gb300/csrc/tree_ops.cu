@@ -106,13 +106,15 @@ prune_kernel(const float *__restrict__ score, const int32_t *__restrict__ parent
 
 // ------------------------------------------------------------------------------------
 // a2: graft. Template nodes are resolved level by level (a node's token needs its
-// template parent's token), then survivors are compacted by a prefix count.
+// template parent's token), then survivors are compacted by a prefix count. The retrieved
+// tree hangs from the anchor node: the root, or (Graft-TAIL) the last kept node.
 // ------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024)
 graft_kernel(int32_t *__restrict__ parent, int32_t *__restrict__ tokens,
              int32_t *__restrict__ n_nodes, int Nmax, const int32_t *__restrict__ tpar,
              const int32_t *__restrict__ trank, int T, const int32_t *__restrict__ R,
-             const int32_t *__restrict__ table, int V, int k, int32_t *err) {
+             const int32_t *__restrict__ anchor, const int32_t *__restrict__ table, int V,
+             int k, int32_t *err) {
   pdl_enter();
   extern __shared__ int s_i32[];
   int *s_par = s_i32;           // [T]
@@ -128,7 +130,12 @@ graft_kernel(int32_t *__restrict__ parent, int32_t *__restrict__ tokens,
     s_maxd = 0;
   }
   int code = (n < 1 || n > Nmax) ? GT_ERR_RANGE : 0;
-  const int root_tok = code ? -1 : tokens[row0];
+  int a = 0;  // anchor node of the retrieved tree
+  if (!code && anchor) {
+    a = anchor[b] == -1 ? n - 1 : anchor[b];
+    if (a < 0 || a >= n) code = GT_ERR_RANGE;
+  }
+  const int root_tok = code ? -1 : tokens[row0 + a];
   if (!code && (root_tok < 0 || root_tok >= V)) code = GT_ERR_TREE;
   const int r = code ? 0 : max(0, min(min(R[b], Nmax - n), T));
   const bool active = t < r;
@@ -145,7 +152,7 @@ graft_kernel(int32_t *__restrict__ parent, int32_t *__restrict__ tokens,
   const int bad = s_bad;
   if (bad) {
     if (t == 0) set_err(err, bad);
-    if (bad != GT_ERR_RANGE)  // kept tree stays valid: no graft, pad the free slots
+    if (n >= 1 && n <= Nmax)  // kept tree stays valid: no graft, pad the free slots
       for (int j = n + t; j < Nmax; j += blockDim.x) parent[row0 + j] = tokens[row0 + j] = -1;
     return;
   }
@@ -179,7 +186,7 @@ graft_kernel(int32_t *__restrict__ parent, int32_t *__restrict__ tokens,
   __syncthreads();
   if (alive) {
     const size_t o = row0 + n + newi;
-    parent[o] = (tp == -1) ? 0 : n + s_new[tp];
+    parent[o] = (tp == -1) ? a : n + s_new[tp];
     tokens[o] = s_tok[t];
   }
   for (int j = n + cnt + t; j < Nmax; j += blockDim.x) parent[row0 + j] = tokens[row0 + j] = -1;
@@ -265,8 +272,8 @@ GT_API int gt_prune_topB(const float *score, const int32_t *parent, const int32_
 
 GT_API int gt_graft_expand(int32_t *parent, int32_t *tokens, int32_t *n_nodes, int B,
                            int Nmax, const int32_t *tpar, const int32_t *trank, int T,
-                           const int32_t *R, const int32_t *table, int V, int k, int32_t *err,
-                           gt_stream_t stream) {
+                           const int32_t *R, const int32_t *anchor, const int32_t *table, int V,
+                           int k, int32_t *err, gt_stream_t stream) {
   if (B < 0 || Nmax < 1 || T < 0 || V < 1 || k < 1) return GT_ERR_ARG;
   if (T > 1024) return GT_ERR_SHAPE;
   if (B == 0) return GT_OK;
@@ -275,7 +282,7 @@ GT_API int gt_graft_expand(int32_t *parent, int32_t *tokens, int32_t *n_nodes, i
   const int Tb = T > 0 ? T : 1;
   const size_t smem = 3 * sizeof(int) * (size_t)Tb;
   return launch(graft_kernel, dim3(B), dim3(round32(Tb)), smem, (cudaStream_t)stream, parent,
-                tokens, n_nodes, Nmax, tpar, trank, T, R, table, V, k, err);
+                tokens, n_nodes, Nmax, tpar, trank, T, R, anchor, table, V, k, err);
 }
 
 GT_API int gt_tree_mask(const int32_t *parent, const int32_t *n_nodes,

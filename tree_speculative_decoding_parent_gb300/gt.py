@@ -22,7 +22,8 @@ _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_
 _SIGS = {
     "gt_prune_topB": (_i, [_vp, _vp, _vp, _vp, _i, _i, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp,
                            _vp, _vp]),
-    "gt_graft_expand": (_i, [_vp, _vp, _vp, _i, _i, _vp, _vp, _i, _vp, _vp, _i, _i, _vp, _vp]),
+    "gt_graft_expand": (_i, [_vp, _vp, _vp, _i, _i, _vp, _vp, _i, _vp, _vp, _vp, _i, _i, _vp,
+                             _vp]),
     "gt_tree_mask": (_i, [_vp, _vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp]),
     "gt_tree_attn_workspace": (_sz, [_i, _i, _i, _i, _i, _i]),
     "gt_tree_attn": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp,
@@ -34,8 +35,8 @@ _SIGS = {
     "gt_verify_greedy": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp,
                               _vp, _vp, _vp, _vp]),
     "gt_succ_update": (_i, [_vp, _i, _i, _vp, _vp, _vp, _i, _i, _vp, _vp]),
-    "gt_tree_build": (_i, [_vp, _vp, _vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _i,
-                           _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "gt_tree_build": (_i, [_vp, _vp, _vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _i,
+                           _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "gt_verify_commit": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp,
                               _vp, _vp, _vp, _vp, _vp]),
     "gt_stage_budget": (_i, [_i, _i, _vp, _vp]),
@@ -120,11 +121,11 @@ def gt_prune_topB(score, parent, tokens, n_in, B, Nin, keep, thresh, Nout, out_p
         _s(stream)))
 
 
-def gt_graft_expand(parent, tokens, n_nodes, B, Nmax, tpar, trank, T, R, table, V, k, err,
-                    stream=None):
+def gt_graft_expand(parent, tokens, n_nodes, B, Nmax, tpar, trank, T, R, anchor, table, V, k,
+                    err, stream=None):
     _check("gt_graft_expand", load().gt_graft_expand(
-        _p(parent), _p(tokens), _p(n_nodes), B, Nmax, _p(tpar), _p(trank), T, _p(R), _p(table),
-        V, k, _p(err), _s(stream)))
+        _p(parent), _p(tokens), _p(n_nodes), B, Nmax, _p(tpar), _p(trank), T, _p(R), _p(anchor),
+        _p(table), V, k, _p(err), _s(stream)))
 
 
 def gt_tree_mask(parent, n_nodes, prefix_len, B, N, depth, pos, mask, err, stream=None):
@@ -176,11 +177,11 @@ def gt_succ_update(table, V, k, tokens, topk_id, n_nodes, B, N, err, stream=None
 
 
 def gt_tree_build(score, parent_in, tokens_in, n_in, B, Nin, keep, thresh, tpar, trank, T, R,
-                  table, V, k, prefix_len, N, parent, tokens, out_score, out_old_idx, n_nodes,
-                  depth, pos, mask, err, stream=None):
+                  anchor, table, V, k, prefix_len, N, parent, tokens, out_score, out_old_idx,
+                  n_nodes, depth, pos, mask, err, stream=None):
     _check("gt_tree_build", load().gt_tree_build(
         _p(score), _p(parent_in), _p(tokens_in), _p(n_in), B, Nin, _p(keep), _p(thresh),
-        _p(tpar), _p(trank), T, _p(R), _p(table), V, k, _p(prefix_len), N, _p(parent),
+        _p(tpar), _p(trank), T, _p(R), _p(anchor), _p(table), V, k, _p(prefix_len), N, _p(parent),
         _p(tokens), _p(out_score), _p(out_old_idx), _p(n_nodes), _p(depth), _p(pos), _p(mask),
         _p(err), _s(stream)))
 

@@ -77,7 +77,8 @@ def run_tree_phase(buf: StepBuffers, inp: dict, stream=None):
                      buf.score, buf.old_idx, buf.n_nodes, buf.err, stream)
     if s.T > 0:
         gt.gt_graft_expand(buf.parent, buf.tokens, buf.n_nodes, s.B, s.N, inp["tpar"],
-                           inp["trank"], s.T, inp["R"], inp["table"], s.V, s.k, buf.err, stream)
+                           inp["trank"], s.T, inp["R"], inp.get("anchor"), inp["table"], s.V, s.k,
+                           buf.err, stream)
     gt.gt_tree_mask(buf.parent, buf.n_nodes, inp["prefix_len"], s.B, s.N, buf.depth, buf.pos,
                     buf.mask, buf.err, stream)
 
@@ -102,7 +103,8 @@ def run_tree_build(buf: StepBuffers, inp: dict, stream=None):
     s = buf.shape
     gt.gt_tree_build(inp["score_in"], inp["parent_in"], inp["tokens_in"], inp.get("n_in"), s.B,
                      s.Nin, inp["keep"], inp.get("thresh"), inp.get("tpar"), inp.get("trank"),
-                     s.T, inp["R"], inp["table"], s.V, s.k, inp["prefix_len"], s.N, buf.parent,
+                     s.T, inp["R"], inp.get("anchor"), inp["table"], s.V, s.k, inp["prefix_len"],
+                     s.N, buf.parent,
                      buf.tokens, buf.score, buf.old_idx, buf.n_nodes, buf.depth, buf.pos,
                      buf.mask, buf.err, stream)
 

@@ -5,6 +5,7 @@ from .synth import (  # noqa: F401
     bf16_bits_to_f32,
     bigram_table,
     default_template,
+    dflash_chain,
     eagle_tree,
     f32_to_bf16_bits,
     make_scenario,

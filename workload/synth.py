@@ -146,6 +146,24 @@ def treegraft_tree(rng_small: np.random.Generator, rng_mid: np.random.Generator,
             np.asarray(score, np.float32))
 
 
+def dflash_chain(rng: np.random.Generator, V: int, L: int = 16):
+    """One block draft of L tokens as a chain below the root (Graft write-up §五, DFlash).
+
+    A block drafter proposes L tokens at once, each with its own confidence. The tokens
+    are uniform draws; the confidence c_i of position i is a Beta(8, 2) draw scaled by
+    (1 - 0.03 i), so later positions of the block are less sure on average. The node score
+    is the fp32 running product of the confidences, non-increasing along the chain like
+    the path scores of the tree drafters, so a score threshold keeps a prefix of the block.
+    """
+    tokens = rng.integers(0, V, size=L + 1).astype(np.int32)
+    conf = (rng.beta(8.0, 2.0, size=L) * (1.0 - 0.03 * np.arange(L))).astype(np.float32)
+    score = [np.float32(1.0)]
+    for c in conf:
+        score.append(np.float32(score[-1] * c))
+    parent = np.arange(-1, L, dtype=np.int32)
+    return parent, tokens, np.asarray(score, np.float32)
+
+
 # ----------------------------------------------------------------------------------------
 # Retrieval template (an input of the graft; its shape is a reading, see default_template)
 # ----------------------------------------------------------------------------------------
@@ -299,6 +317,11 @@ CONFIGS = {
     5: dict(name="llama3-70b-h64kv8-P16384-V128256-treegraft256to63", B=1, Hq=64, Hkv=8,
             d=128, dtype="bf16", V=128256, k=8, P=16384, tree="treegraft", keep=63, R=0,
             N=63, p_accept=0.55, table="bigram"),
+    # Graft-TAIL on a block draft: keep the confident prefix of a 16-token DFlash chain,
+    # refill the freed slots with retrieved candidates hung from the prefix's last token
+    6: dict(name="qwen3-8b-h32kv8-P4096-V151936-dflash16-tail", B=1, Hq=32, Hkv=8, d=128,
+            dtype="bf16", V=151936, k=8, P=4096, tree="dflash", keep=17, R=17, N=17,
+            p_accept=0.6, table="stream", anchor=-1),
 }
 
 EAGLE_STEPS = [(1, 10), (10, 10), (10, 10), (10, 10), (10, 10)]  # D=5, W=10, m=10
@@ -335,6 +358,7 @@ class Scenario:
     Vc: np.ndarray          # [B][Hkv][Lcap][d]
     p_accept: float
     seed: int
+    anchor: Optional[np.ndarray] = None  # int32 [B] graft anchor (-1: last kept node) or None
 
     @property
     def g(self) -> int:
@@ -382,6 +406,8 @@ def make_scenario(cid: int, seed: Optional[int] = None, *, V: Optional[int] = No
             trees.append(eagle_tree(r_tree, V, tree_scale or EAGLE_STEPS))
         elif c["tree"] == "static60":
             trees.append(eagle_tree(r_tree, V, tree_scale or static_tree_widths()))
+        elif c["tree"] == "dflash":
+            trees.append(dflash_chain(r_tree, V, c["N"] - 1))
         else:
             trees.append(treegraft_tree(r_small, r_mid, V))
     Nin = max(len(t[0]) for t in trees)
@@ -396,7 +422,7 @@ def make_scenario(cid: int, seed: Optional[int] = None, *, V: Optional[int] = No
 
     keep = np.full(B, min(c["keep"], Nin), np.int32)
     thresh = None
-    if c["tree"] == "static60":
+    if c["tree"] in ("static60", "dflash"):
         # seeded confidence threshold: log-uniform between the smallest and largest
         # non-root score, at a seeded fraction q_b of that range
         thresh = np.zeros(B, np.float32)
@@ -433,4 +459,5 @@ def make_scenario(cid: int, seed: Optional[int] = None, *, V: Optional[int] = No
                     d=d, dtype=c["dtype"], Lcap=Lcap, scale=float(np.float32(1.0 / np.sqrt(d))),
                     parent_in=parent_in, tokens_in=tokens_in, score_in=score_in, keep=keep,
                     thresh=thresh, tpar=tpar, trank=trank, R=R, table=table, prefix_len=prefix,
-                    Q=Q, K=Kc, Vc=Vc, p_accept=c["p_accept"], seed=seed)
+                    Q=Q, K=Kc, Vc=Vc, p_accept=c["p_accept"], seed=seed,
+                    anchor=None if "anchor" not in c else np.full(B, c["anchor"], np.int32))
