@@ -21,3 +21,9 @@ from .step import (  # noqa: F401
     verify_greedy,
     vocab_topk,
 )
+from .sampling import (  # noqa: F401
+    philox4x32_10,
+    step_verify_sampled,
+    verify_sampled,
+    vocab_sample,
+)
