@@ -29,8 +29,13 @@ Readings where the pages are silent (each one is also listed in the design doc):
   * The target distribution at node u is softmax(z_u / T) over the whole vocabulary.
   * The draw y_u is the Gumbel-max sample of row r = b * N + u: score_j = z_j * (1/T) +
     G_j in float32 (1/T rounded to float32 once), G_j = -log(-log U_j), U_j the uniform
-    ((x >> 9) + 0.5) * 2^-23 of word (j mod 4) of Philox-4x32-10 at counter
-    (j div 4, r, step mod 2^32, step div 2^32) and key (seed mod 2^32, seed div 2^32);
+    ((x_j >> 9) + 0.5) * 2^-23 of a 32-bit word x_j = (A_j << 24) | (B_j >> 8). A_j is byte
+    (j mod 16) (little-endian, word (j mod 16) div 4) of the Philox-4x32-10 block at counter
+    (j div 16, r, step mod 2^32, step div 2^32); B_j is word (j mod 4) of the block at
+    counter ((j div 4) + 2^31, r, step mod 2^32, step div 2^32); both with key
+    (seed mod 2^32, seed div 2^32). The two counter ranges never meet (j < 2^30), so x_j
+    is a uniform 32-bit word independent across j; its top byte alone tells whether U_j
+    can be large, which lets a kernel skip the logarithms of almost every element;
     the largest score wins, ties to the smaller index; NaN ranks below -inf and +0.0
     equals -0.0 (the top-k order). Every float32 operation is one IEEE round to nearest,
     in the order written in ``log_f32`` and ``gumbel_scores``, so a float32 kernel that
@@ -114,28 +119,42 @@ def log_f32(x):
     return e.astype(np.float32) * _LN2 + lm
 
 
+def _byte_word(w, e):
+    """Byte e (0..15) of a Philox block given as four word arrays, little-endian words."""
+    return (w[e // 4] >> np.uint32(8 * (e % 4))) & np.uint32(0xFF)
+
+
+def noise_words(V: int, rows, seed: int, step: int):
+    """The 32-bit words x_j [R][V] of the rows ``rows`` (see the readings above)."""
+    rows = np.asarray(rows, np.uint64)
+    key = (seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF)
+    s_lo, s_hi = step & 0xFFFFFFFF, (step >> 32) & 0xFFFFFFFF
+    j = np.arange(V, dtype=np.int64)
+    A16 = philox4x32_10(np.arange((V + 15) // 16, dtype=np.uint64)[None, :], rows[:, None],
+                        s_lo, s_hi, *key)
+    A = np.stack([_byte_word(A16, e) for e in range(16)], axis=-1).reshape(len(rows), -1)[:, :V]
+    B4 = philox4x32_10(np.arange((V + 3) // 4, dtype=np.uint64)[None, :] + np.uint64(1 << 31),
+                       rows[:, None], s_lo, s_hi, *key)
+    B = np.stack(B4, axis=-1).reshape(len(rows), -1)[:, :V]
+    assert A.shape[1] == B.shape[1] == j.size
+    return (A << np.uint32(24)) | (B >> np.uint32(8))
+
+
 def gumbel_scores(z, rows, temperature: float, seed: int, step: int):
     """Perturbed scores z * (1/T) + G of logit rows ``z`` [R][V] whose global row numbers
-    are ``rows`` [R] (float32 [R][V]). Element j of a row takes word j mod 4 of the
-    Philox block at counter j div 4."""
+    are ``rows`` [R] (float32 [R][V])."""
     z = np.asarray(z, np.float32)
     R, V = z.shape
     inv_t = _F(1) / _F(temperature)
-    G = (V + 3) // 4
-    g_idx = np.arange(G, dtype=np.uint64)
     rows = np.asarray(rows, np.uint64)
     out = np.empty((R, V), np.float32)
-    chunk = max(1, (1 << 21) // G)  # rows per batch of Philox blocks
+    chunk = max(1, (1 << 20) // max(V, 1))  # rows per batch
     for r0 in range(0, R, chunk):
         rr = rows[r0:r0 + chunk]
-        words = philox4x32_10(g_idx[None, :], rr[:, None], step & 0xFFFFFFFF,
-                              (step >> 32) & 0xFFFFFFFF, seed & 0xFFFFFFFF,
-                              (seed >> 32) & 0xFFFFFFFF)
-        # element j of a row = word j % 4 of block j // 4
-        x = np.stack(words, axis=-1).reshape(len(rr), 4 * G)[:, :V]
-        u = uniform_f32(x)
+        u = uniform_f32(noise_words(V, rr, seed, step))
         g = -log_f32(-log_f32(u))
-        out[r0:r0 + len(rr)] = z[r0:r0 + len(rr)] * inv_t + g
+        with np.errstate(over="ignore"):  # z / T may overflow to +-inf, as in IEEE float32
+            out[r0:r0 + len(rr)] = z[r0:r0 + len(rr)] * inv_t + g
     return out
 
 

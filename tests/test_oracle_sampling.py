@@ -7,7 +7,7 @@ import pytest
 
 import oracle
 from conftest import golden
-from oracle.sampling import (argmax_first, gumbel_scores, log_f32, philox4x32_10,
+from oracle.sampling import (argmax_first, gumbel_scores, log_f32, noise_words, philox4x32_10,
                              step_verify_sampled, uniform_f32, verify_sampled, vocab_sample)
 
 
@@ -17,6 +17,24 @@ def test_philox_known_answers():
         k = [int(x, 16) for x in vec["key"]]
         out = philox4x32_10(*[np.array([x]) for x in c], *k)
         assert [int(w[0]) for w in out] == [int(x, 16) for x in vec["out"]]
+
+
+def test_noise_words_are_uniform_and_independent():
+    x = noise_words(200003, np.arange(4), seed=8, step=2).astype(np.uint64)
+    n = x.size
+    # the top byte and the low 24 bits come from different Philox blocks: each uniform
+    for part, bins in ((x >> np.uint64(24), 256), ((x >> np.uint64(8)) & np.uint64(0xFF), 256),
+                       (x & np.uint64(0xFF), 256)):
+        cnt = np.bincount(part.astype(np.int64).ravel(), minlength=bins)
+        chi2 = ((cnt - n / bins) ** 2 / (n / bins)).sum()
+        assert chi2 < bins + 6 * np.sqrt(2 * bins)  # mean bins - 1, sd sqrt(2 (bins - 1))
+    u = x.astype(np.float64) / 2.0 ** 32
+    for a, b in ((u[:, :-1], u[:, 1:]), (u[:, :-16], u[:, 16:]), (u[:-1], u[1:])):
+        assert abs(np.corrcoef(a.ravel(), b.ravel())[0, 1]) < 5 / np.sqrt(a.size)
+    top, low = (x >> np.uint64(24)).astype(np.float64), (x & np.uint64(0xFFFFFF)).astype(np.float64)
+    assert abs(np.corrcoef(top.ravel(), low.ravel())[0, 1]) < 5 / np.sqrt(n)
+    # the candidate byte (255) marks exactly the words of U >= 255/256
+    assert np.array_equal(x >= np.uint64(0xFF000000), (x >> np.uint64(24)) == 255)
 
 
 def test_uniform_grid_and_ends():
