@@ -170,7 +170,7 @@ def _src_hash() -> str:
 # --------------------------------------------------------------------------------------
 
 
-def time_oracle(scn, steps: int, budget_s: float):
+def time_oracle(scn, steps: int, budget_s: float, temperature: float = 0.0, seed: int = 1):
     """Runs the oracle's whole step on the same workload; returns (steps/s, steps, seconds)."""
     import oracle
     tree = oracle.step_tree_phase(scn.parent_in, scn.tokens_in, scn.score_in,
@@ -189,7 +189,11 @@ def time_oracle(scn, steps: int, budget_s: float):
             n, P = int(tree["n_nodes"][b]), int(scn.prefix_len[b])
             oracle.tree_attn(dec(scn.Q[b]), dec(scn.K[b][:, :P + n]), dec(scn.Vc[b][:, :P + n]),
                              tree["parent"][b], n, P, scn.scale)
-        res = oracle.step_verify_phase(tree, logits, table, scn.prefix_len, scn.k)
+        if temperature > 0:
+            res = oracle.step_verify_sampled(tree, logits, table, scn.prefix_len, scn.k,
+                                             temperature, seed, done)
+        else:
+            res = oracle.step_verify_phase(tree, logits, table, scn.prefix_len, scn.k)
         table = res["table"]
         done += 1
         if time.perf_counter() - t0 > budget_s:
@@ -202,15 +206,17 @@ def run_reference(args, rank: int, world: int):
     if rank != 0:
         return None
     scn = make_scenario(args.config)
-    time_oracle(scn, 1, 0.0)  # one untimed warm-up step (the oracle has no caches to fill)
-    value, done, dt = time_oracle(scn, args.steps, args.ref_budget)
+    # one untimed warm-up step (the oracle has no caches to fill)
+    time_oracle(scn, 1, 0.0, args.temperature, args.seed)
+    value, done, dt = time_oracle(scn, args.steps, args.ref_budget, args.temperature, args.seed)
     cores = os.cpu_count()
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s",
         "n_gpus": world, "steps": done, "warmup": args.warmup, "ms_per_step": 1e3 * dt / done,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded generator; see DESIGN.md input recipe)",
-        "config": {"workload": CONFIGS[args.config]["name"], "config_id": args.config},
+        "config": {"workload": CONFIGS[args.config]["name"], "config_id": args.config,
+                   "temperature": args.temperature},
         "cpu_baseline": {"value": value, "unit": "steps/s", "cores": cores, "kind": "oracle",
                          "sample": f"{done} whole steps of the same workload on the host CPU "
                                    f"(numpy float64; BLAS may use all {cores} cores)"},
@@ -230,7 +236,8 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     from tree_speculative_decoding_parent_gb300 import build, gt
     from tree_speculative_decoding_parent_gb300.step import (StepBuffers, StepShape, run_attn,
                                                              run_step, run_tree_build,
-                                                             run_tree_phase, run_verify_commit)
+                                                             run_tree_phase, run_verify_commit,
+                                                             run_verify_sample_commit)
     build.build()
     gt.load()
     dev = torch.device("cuda", local_rank)
@@ -273,7 +280,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     stream = torch.cuda.current_stream(dev)
 
     # eager warm-up (first calls set kernel attributes), then graphs
-    run_step(buf, sets[0], scale=scn.scale)
+    run_step(buf, sets[0], scale=scn.scale, temperature=args.temperature, seed=args.seed)
     torch.cuda.synchronize()
     if int(buf.err.item()) != 0:
         raise RuntimeError(f"device error {gt.status_string(int(buf.err.item()))}")
@@ -294,7 +301,10 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
                 if timed:
                     gt.gt_event_record_external(e1, s)
                     evs.append((e0, e1))
-                run_verify_commit(buf, inp, s)
+                if args.temperature > 0:
+                    run_verify_sample_commit(buf, inp, args.temperature, args.seed, i, s)
+                else:
+                    run_verify_commit(buf, inp, s)
         return g, evs
 
     # torch creates CUDA events lazily: record each once before capture so it exists
@@ -359,7 +369,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
             inp["K"][b, :, P[b]:P[b] + scn.N].copy_(h_kv[b][0], non_blocking=True)
             inp["V"][b, :, P[b]:P[b] + scn.N].copy_(h_kv[b][1], non_blocking=True)
         inp["logits"].copy_(h_logits, non_blocking=True)
-        run_step(buf, inp, scale=scn.scale)
+        run_step(buf, inp, scale=scn.scale, temperature=args.temperature, seed=args.seed)
         for k in outs:
             h_out[k].copy_(getattr(buf, k), non_blocking=True)
         torch.cuda.synchronize()
@@ -376,7 +386,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
 
     breakdown = None
     if args.breakdown and rank == 0:
-        breakdown = call_breakdown(torch, gt, buf, sets, scn, nsets)
+        breakdown = call_breakdown(torch, gt, buf, sets, scn, nsets, args.temperature, args.seed)
 
     if rank != 0:
         return None
@@ -390,6 +400,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": scn.dtype,
         "data": "synthetic (seeded generator; see DESIGN.md input recipe)",
         "config": {"workload": scn.name, "config_id": args.config, "B": scn.B,
+                   "temperature": args.temperature,
                    "prefix_len": int(max(scn.prefix_len)), "slots": scn.N, "vocab": scn.V,
                    "heads": f"{scn.Hq}/{scn.Hkv}x{scn.d}",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -408,14 +419,14 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
                      "traffic": _traffic_record(f"tree_attn/config{args.config}")},
         "e2e": {"value": job_throughput(world, ne, e2e_s), "unit": "steps/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * KERNELS_PER_STEP,
+        "gpu_launches": args.steps * (KERNELS_PER_STEP + (args.temperature > 0)),
         "clocks": clocks,
         "accepted_len_mean": float(buf.acc_len.float().mean().item()),
     }
     if breakdown is not None:
         line["breakdown_us"] = breakdown
     if not args.no_cpu_baseline:
-        cv, cdone, cdt = time_oracle(scn, 1000, args.cpu_budget)
+        cv, cdone, cdt = time_oracle(scn, 1000, args.cpu_budget, args.temperature, args.seed)
         line["cpu_baseline"] = {
             "value": cv, "unit": "steps/s", "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"{cdone} whole steps of the same workload (~{cdt:.0f} s, numpy float64; "
@@ -423,14 +434,17 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     return line
 
 
-def call_breakdown(torch, gt, buf, sets, scn, nsets, reps: int = 50):
+def call_breakdown(torch, gt, buf, sets, scn, nsets, temperature=0.0, seed=0, reps: int = 50):
     """Average device time of each C-ABI call of the step inside a CUDA graph: one graph
     per input set with an externally visible event between consecutive calls (the events
     also end the programmatic overlap between the calls, so the sum exceeds the step)."""
     from tree_speculative_decoding_parent_gb300.step import (run_attn, run_kv_commit,
-                                                             run_tree_build, run_verify_commit)
+                                                             run_tree_build, run_verify_commit,
+                                                             run_verify_sample_commit)
     # the KV commit (compaction of the accepted rows) is timed too; it is not part of the step
-    names = ["gt_tree_build", "gt_tree_attn", "gt_verify_commit", "gt_kv_commit (not in step)"]
+    names = ["gt_tree_build", "gt_tree_attn",
+             "gt_verify_sample_commit" if temperature > 0 else "gt_verify_commit",
+             "gt_kv_commit (not in step)"]
     graphs = []
     for k in range(nsets):
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
@@ -446,7 +460,10 @@ def call_breakdown(torch, gt, buf, sets, scn, nsets, reps: int = 50):
             gt.gt_event_record_external(evs[1], s)
             run_attn(buf, inp, s, scn.scale)
             gt.gt_event_record_external(evs[2], s)
-            run_verify_commit(buf, inp, s)
+            if temperature > 0:
+                run_verify_sample_commit(buf, inp, temperature, seed, k, s)
+            else:
+                run_verify_commit(buf, inp, s)
             gt.gt_event_record_external(evs[3], s)
             run_kv_commit(buf, inp, s)
             gt.gt_event_record_external(evs[4], s)
@@ -472,6 +489,9 @@ def main():
     ap.add_argument("--breakdown", action="store_true",
                     help="also report the in-graph device time of each C-ABI call")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--temperature", type=float, default=0.0,
+                    help="0: greedy verification; > 0: one target draw per node at this T")
+    ap.add_argument("--seed", type=int, default=1, help="seed of the draws at T > 0")
     ap.add_argument("--ref-budget", type=float, default=60.0)
     args = ap.parse_args()
     if args.warmup < 3:

@@ -284,6 +284,54 @@ int gt_verify_commit(const float *logits, const int32_t *tokens, const int32_t *
                      int32_t *err, gt_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
+ * Verification at temperature T > 0.  [TreeGraft] §三 (the pruned tree goes to tree
+ *     attention and rejection sampling), §七 (rejection sampling keeps the target's output
+ *     distribution).
+ *
+ * The tree's proposals are point masses (drafters' top-m children, retrieved successors).
+ * Rejection sampling of point masses has the distribution of one target draw y_u per node
+ * followed by a walk into the first child (lowest index) whose token is y_u; the walk stops
+ * at the first node with no such child and y_u there is the bonus token. These calls use
+ * that form.
+ *
+ * gt_vocab_sample: sample[r] = argmax_j fl(fl(z[r][j] * fl(1/T)) + G(r, j)), ties to the
+ *   lower index, NaN below -inf, +0.0 equal to -0.0 (a Gumbel-max draw from
+ *   softmax(z[r] / T)). G(r, j) = -log(-log U) with U = ((x >> 9) + 0.5) * 2^-23 and
+ *   x = (A << 24) | (B >> 8): A is byte j % 16 (little-endian) of the Philox-4x32-10 block
+ *   (Salmon et al., SC 2011) at counter (j / 16, r, step mod 2^32, step / 2^32), B is word
+ *   j % 4 of the block at counter (j / 4 + 2^31, r, step mod 2^32, step / 2^32), both with
+ *   key (seed mod 2^32, seed / 2^32). log is the library's own float32
+ *   routine: x = 2^e m, m in [sqrt(2)/2, sqrt(2)), s = (m-1)/(m+1), log m = (s + s) *
+ *   (((( 1/9 z + 1/7) z + 1/5) z + 1/3) z + 1), z = s*s, log x = e * fl(ln 2) + log m, every
+ *   float32 operation rounded to nearest once, so the draw is reproducible bit for bit.
+ *   device in : logits f32 [rows][V]        device out: sample i32 [rows]
+ *   Errors: GT_ERR_ARG for T not finite and > 0 or 1/T overflowing float32.
+ * gt_verify_sample: gt_vocab_sample over the B*N rows (row b*N + v), then the sampled walk
+ *   of each request. Outputs as gt_verify_greedy (acc_len, path, out_tok, kv_src, kv_dst).
+ * gt_verify_sample_commit: gt_verify_sample plus gt_vocab_topk of the unscaled logits and
+ *   the table update of gt_succ_update (the table keeps the target's k most likely tokens
+ *   at every verified node, as at T = 0).
+ *   device in : logits f32 [B][N][V]; tokens, parent i32 [B][N]; n_nodes, prefix_len i32 [B]
+ *   device out: sample i32 [B][N]; topk_id i32 [B][N][k]; topk_val f32 [B][N][k]; the walk
+ *               outputs as gt_verify_greedy; table i32 [V][k] in place.
+ *   Limits: 1 <= N <= 1024, B*N <= 16384, 1 <= k <= 16, k <= V. Device errors: GT_ERR_TREE,
+ *   GT_ERR_RANGE.
+ * ------------------------------------------------------------------------------------- */
+int gt_vocab_sample(const float *logits, int rows, int V, float temperature, uint64_t seed,
+                    uint64_t step, int32_t *sample, gt_stream_t stream);
+int gt_verify_sample(const float *logits, const int32_t *tokens, const int32_t *parent,
+                     const int32_t *n_nodes, const int32_t *prefix_len, int B, int N, int V,
+                     float temperature, uint64_t seed, uint64_t step, int32_t *sample,
+                     int32_t *acc_len, int32_t *path, int32_t *out_tok, int32_t *kv_src,
+                     int32_t *kv_dst, int32_t *err, gt_stream_t stream);
+int gt_verify_sample_commit(const float *logits, const int32_t *tokens, const int32_t *parent,
+                            const int32_t *n_nodes, const int32_t *prefix_len, int B, int N,
+                            int V, int k, float temperature, uint64_t seed, uint64_t step,
+                            int32_t *topk_id, float *topk_val, int32_t *sample, int32_t *acc_len,
+                            int32_t *path, int32_t *out_tok, int32_t *kv_src, int32_t *kv_dst,
+                            int32_t *table, int32_t *err, gt_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
  * Host helpers (host pointers, synchronous, no CUDA calls).
  *
  * gt_stage_budget: draft / retrieved split of `slots` for a prune at stage 0, 1 or 5

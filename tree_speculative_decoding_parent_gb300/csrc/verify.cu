@@ -26,6 +26,7 @@
 
 #include "gt_internal.cuh"
 #include "launch.cuh"
+#include "sample.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -366,12 +367,26 @@ static int topk_launch(const float *logits, int rows, int V, int k, int32_t *ids
 // on each edge; the deepest accepted node (ties: smaller index) wins a block max over
 // (depth << 16 | ~v).
 // ------------------------------------------------------------------------------------
+// With one target draw per node (T > 0) the walk enters only the first child carrying the
+// draw: a later sibling with the same token as an earlier one can never be entered, so its
+// token is replaced by -1 (draws are never negative). Every thread of the block calls this.
+__device__ __forceinline__ void shadow_duplicates(const int *s_par, int *s_tok, int n, int v) {
+  bool shadowed = false;
+  if (v < n && v > 0)
+    for (int w = 1; w < v && !shadowed; ++w)
+      shadowed = s_par[w] == s_par[v] && s_tok[w] == s_tok[v];
+  __syncthreads();
+  if (shadowed) s_tok[v] = -1;
+  __syncthreads();
+}
+
 __global__ void __launch_bounds__(1024)
 walk_kernel(const int32_t *__restrict__ tokens, const int32_t *__restrict__ parent,
             const int32_t *__restrict__ n_nodes, const int32_t *__restrict__ prefix_len, int N,
-            int k, const int32_t *__restrict__ topk_id, int32_t *__restrict__ acc_len,
-            int32_t *__restrict__ path, int32_t *__restrict__ out_tok,
-            int32_t *__restrict__ kv_src, int32_t *__restrict__ kv_dst, int32_t *err) {
+            int k, const int32_t *__restrict__ topk_id, const int32_t *__restrict__ sample,
+            int32_t *__restrict__ acc_len, int32_t *__restrict__ path,
+            int32_t *__restrict__ out_tok, int32_t *__restrict__ kv_src,
+            int32_t *__restrict__ kv_dst, int32_t *err) {
   pdl_enter();
   extern __shared__ int s_w[];
   int *s_par = s_w, *s_tok = s_w + N, *s_am = s_w + 2 * N, *s_path = s_w + 3 * N;
@@ -386,7 +401,7 @@ walk_kernel(const int32_t *__restrict__ tokens, const int32_t *__restrict__ pare
     const int p = parent[row0 + v];
     s_par[v] = p;
     s_tok[v] = tokens[row0 + v];
-    s_am[v] = topk_id[(row0 + v) * k];
+    s_am[v] = sample ? sample[row0 + v] : topk_id[(row0 + v) * k];
     if (v == 0 ? (p != -1) : (p < 0 || p >= v)) code = GT_ERR_TREE;
   }
   __syncthreads();
@@ -395,6 +410,7 @@ walk_kernel(const int32_t *__restrict__ tokens, const int32_t *__restrict__ pare
   const int bad = s_bad;
   int L = 0, vstar = 0;
   if (!bad) {
+    if (sample) shadow_duplicates(s_par, s_tok, n, v);
     uint32_t key = 0u;
     if (v < n) {
       bool acc = true;
@@ -485,7 +501,7 @@ __global__ void __launch_bounds__(1024)
 walk_update_kernel(const int32_t *__restrict__ tokens, const int32_t *__restrict__ parent,
                    const int32_t *__restrict__ n_nodes, const int32_t *__restrict__ prefix_len,
                    int B, int N, int k, const int32_t *__restrict__ topk_id,
-                   int32_t *__restrict__ acc_len, int32_t *__restrict__ path,
+                   const int32_t *__restrict__ sample, int32_t *__restrict__ acc_len, int32_t *__restrict__ path,
                    int32_t *__restrict__ out_tok, int32_t *__restrict__ kv_src,
                    int32_t *__restrict__ kv_dst, int32_t *__restrict__ table, int V, int hs,
                    int32_t *err) {
@@ -522,7 +538,7 @@ walk_update_kernel(const int32_t *__restrict__ tokens, const int32_t *__restrict
     const int p = parent[row0 + v];
     s_par[v] = p;
     s_tok[v] = tokens[row0 + v];
-    s_am[v] = topk_id[(row0 + v) * k];
+    s_am[v] = sample ? sample[row0 + v] : topk_id[(row0 + v) * k];
     if (v == 0 ? (p != -1) : (p < 0 || p >= v)) code = GT_ERR_TREE;
   }
   __syncthreads();
@@ -531,6 +547,7 @@ walk_update_kernel(const int32_t *__restrict__ tokens, const int32_t *__restrict
   const int bad = s_bad;
   int L = 0, vstar = 0;
   if (!bad) {
+    if (sample) shadow_duplicates(s_par, s_tok, n, v);
     uint32_t key = 0u;
     if (v < n) {
       bool acc = true;
@@ -639,8 +656,8 @@ GT_API int gt_verify_greedy(const float *logits, const int32_t *tokens, const in
   if (rc != GT_OK) return rc;
   const int threads = (N + 31) / 32 * 32;
   return launch(walk_kernel, dim3(B), dim3(threads), 4 * sizeof(int) * (size_t)N, s, tokens,
-                parent, n_nodes, prefix_len, N, k, topk_id, acc_len, path, out_tok, kv_src,
-                kv_dst, err);
+                parent, n_nodes, prefix_len, N, k, topk_id, (const int32_t *)nullptr, acc_len, path,
+                out_tok, kv_src, kv_dst, err);
 }
 
 GT_API int gt_succ_update(int32_t *table, int V, int k, const int32_t *tokens,
@@ -662,20 +679,12 @@ GT_API int gt_succ_update(int32_t *table, int V, int k, const int32_t *tokens,
                 tokens, topk_id, n_nodes, N, (int)total, err);
 }
 
-GT_API int gt_verify_commit(const float *logits, const int32_t *tokens, const int32_t *parent,
-                            const int32_t *n_nodes, const int32_t *prefix_len, int B, int N, int V,
-                            int k, int32_t *topk_id, float *topk_val, int32_t *acc_len,
-                            int32_t *path, int32_t *out_tok, int32_t *kv_src, int32_t *kv_dst,
-                            int32_t *table, int32_t *err, gt_stream_t stream) {
-  if (B < 0 || N < 1 || V < 1 || k < 1) return GT_ERR_ARG;
-  if (N > 1024 || k > 16 || k > V || (long long)B * N > 16384) return GT_ERR_SHAPE;
-  if (B == 0) return GT_OK;
-  if (!logits || !tokens || !parent || !n_nodes || !prefix_len || !topk_id || !topk_val ||
-      !acc_len || !path || !out_tok || !kv_src || !kv_dst || !table)
-    return GT_ERR_ARG;
-  cudaStream_t s = (cudaStream_t)stream;
-  int rc = topk_launch(logits, B * N, V, k, topk_id, topk_val, s);
-  if (rc != GT_OK) return rc;
+// walk + table update of a5-a7 once the top-k (and, at T > 0, the draws) are in memory
+static int walk_update_launch(const int32_t *tokens, const int32_t *parent,
+                              const int32_t *n_nodes, const int32_t *prefix_len, int B, int N,
+                              int V, int k, const int32_t *topk_id, const int32_t *sample,
+                              int32_t *acc_len, int32_t *path, int32_t *out_tok, int32_t *kv_src,
+                              int32_t *kv_dst, int32_t *table, int32_t *err, cudaStream_t s) {
   const int threads = (N + 31) / 32 * 32;
   size_t smem = sizeof(int) * (4 * (size_t)N + (size_t)B * N);
   // the token hash: a power of two at least twice B*N, when it fits (else the scan)
@@ -690,6 +699,75 @@ GT_API int gt_verify_commit(const float *logits, const int32_t *tokens, const in
     if (e != cudaSuccess) return launch_status(e, "cudaFuncSetAttribute(walk_update_kernel)");
   }
   return launch(walk_update_kernel, dim3(B), dim3(threads), smem, s, tokens, parent, n_nodes,
-                prefix_len, B, N, k, topk_id, acc_len, path, out_tok, kv_src, kv_dst, table, V,
-                hs, err);
+                prefix_len, B, N, k, topk_id, sample, acc_len, path, out_tok, kv_src, kv_dst,
+                table, V, hs, err);
+}
+
+GT_API int gt_verify_commit(const float *logits, const int32_t *tokens, const int32_t *parent,
+                            const int32_t *n_nodes, const int32_t *prefix_len, int B, int N, int V,
+                            int k, int32_t *topk_id, float *topk_val, int32_t *acc_len,
+                            int32_t *path, int32_t *out_tok, int32_t *kv_src, int32_t *kv_dst,
+                            int32_t *table, int32_t *err, gt_stream_t stream) {
+  if (B < 0 || N < 1 || V < 1 || k < 1) return GT_ERR_ARG;
+  if (N > 1024 || k > 16 || k > V || (long long)B * N > 16384) return GT_ERR_SHAPE;
+  if (B == 0) return GT_OK;
+  if (!logits || !tokens || !parent || !n_nodes || !prefix_len || !topk_id || !topk_val ||
+      !acc_len || !path || !out_tok || !kv_src || !kv_dst || !table)
+    return GT_ERR_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  int rc = topk_launch(logits, B * N, V, k, topk_id, topk_val, s);
+  if (rc != GT_OK) return rc;
+  return walk_update_launch(tokens, parent, n_nodes, prefix_len, B, N, V, k, topk_id, nullptr,
+                            acc_len, path, out_tok, kv_src, kv_dst, table, err, s);
+}
+
+GT_API int gt_vocab_sample(const float *logits, int rows, int V, float temperature,
+                           uint64_t seed, uint64_t step, int32_t *sample, gt_stream_t stream) {
+  if (rows < 0 || V < 1) return GT_ERR_ARG;
+  if (rows == 0) return GT_OK;
+  if (!logits || !sample) return GT_ERR_ARG;
+  return sample_launch(logits, rows, V, temperature, seed, step, sample, (cudaStream_t)stream);
+}
+
+GT_API int gt_verify_sample(const float *logits, const int32_t *tokens, const int32_t *parent,
+                            const int32_t *n_nodes, const int32_t *prefix_len, int B, int N,
+                            int V, float temperature, uint64_t seed, uint64_t step,
+                            int32_t *sample, int32_t *acc_len, int32_t *path, int32_t *out_tok,
+                            int32_t *kv_src, int32_t *kv_dst, int32_t *err, gt_stream_t stream) {
+  if (B < 0 || N < 1 || V < 1) return GT_ERR_ARG;
+  if (N > 1024 || (long long)B * N > 16384) return GT_ERR_SHAPE;
+  if (B == 0) return GT_OK;
+  if (!logits || !tokens || !parent || !n_nodes || !prefix_len || !sample || !acc_len ||
+      !path || !out_tok || !kv_src || !kv_dst)
+    return GT_ERR_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  int rc = sample_launch(logits, B * N, V, temperature, seed, step, sample, s);
+  if (rc != GT_OK) return rc;
+  const int threads = (N + 31) / 32 * 32;
+  return launch(walk_kernel, dim3(B), dim3(threads), 4 * sizeof(int) * (size_t)N, s, tokens,
+                parent, n_nodes, prefix_len, N, 1, (const int32_t *)nullptr, (const int32_t *)sample,
+                acc_len, path, out_tok, kv_src, kv_dst, err);
+}
+
+GT_API int gt_verify_sample_commit(const float *logits, const int32_t *tokens,
+                                   const int32_t *parent, const int32_t *n_nodes,
+                                   const int32_t *prefix_len, int B, int N, int V, int k,
+                                   float temperature, uint64_t seed, uint64_t step,
+                                   int32_t *topk_id, float *topk_val, int32_t *sample,
+                                   int32_t *acc_len, int32_t *path, int32_t *out_tok,
+                                   int32_t *kv_src, int32_t *kv_dst, int32_t *table, int32_t *err,
+                                   gt_stream_t stream) {
+  if (B < 0 || N < 1 || V < 1 || k < 1) return GT_ERR_ARG;
+  if (N > 1024 || k > 16 || k > V || (long long)B * N > 16384) return GT_ERR_SHAPE;
+  if (B == 0) return GT_OK;
+  if (!logits || !tokens || !parent || !n_nodes || !prefix_len || !topk_id || !topk_val ||
+      !sample || !acc_len || !path || !out_tok || !kv_src || !kv_dst || !table)
+    return GT_ERR_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  int rc = sample_launch(logits, B * N, V, temperature, seed, step, sample, s);
+  if (rc != GT_OK) return rc;
+  rc = topk_launch(logits, B * N, V, k, topk_id, topk_val, s);
+  if (rc != GT_OK) return rc;
+  return walk_update_launch(tokens, parent, n_nodes, prefix_len, B, N, V, k, topk_id, sample,
+                            acc_len, path, out_tok, kv_src, kv_dst, table, err, s);
 }

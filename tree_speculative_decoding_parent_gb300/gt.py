@@ -19,6 +19,7 @@ GT_F32, GT_BF16 = 0, 1
 GT_ATTN_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024  # size of the static scratch in libgt
 
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_u64 = ctypes.c_uint64
 _SIGS = {
     "gt_prune_topB": (_i, [_vp, _vp, _vp, _vp, _i, _i, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp,
                            _vp, _vp]),
@@ -39,6 +40,11 @@ _SIGS = {
                            _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "gt_verify_commit": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp,
                               _vp, _vp, _vp, _vp, _vp]),
+    "gt_vocab_sample": (_i, [_vp, _i, _i, _f, _u64, _u64, _vp, _vp]),
+    "gt_verify_sample": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _f, _u64, _u64, _vp, _vp, _vp,
+                              _vp, _vp, _vp, _vp, _vp]),
+    "gt_verify_sample_commit": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _u64, _u64,
+                                     _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "gt_stage_budget": (_i, [_i, _i, _vp, _vp]),
     "gt_default_template": (_i, [_i, _i, _i, _vp, _vp]),
     "gt_status_string": (ctypes.c_char_p, [_i]),
@@ -192,6 +198,28 @@ def gt_verify_commit(logits, tokens, parent, n_nodes, prefix_len, B, N, V, k, to
         _p(logits), _p(tokens), _p(parent), _p(n_nodes), _p(prefix_len), B, N, V, k, _p(topk_id),
         _p(topk_val), _p(acc_len), _p(path), _p(out_tok), _p(kv_src), _p(kv_dst), _p(table),
         _p(err), _s(stream)))
+
+
+def gt_vocab_sample(logits, rows, V, temperature, seed, step, sample, stream=None):
+    _check("gt_vocab_sample", load().gt_vocab_sample(
+        _p(logits), rows, V, temperature, seed, step, _p(sample), _s(stream)))
+
+
+def gt_verify_sample(logits, tokens, parent, n_nodes, prefix_len, B, N, V, temperature, seed,
+                     step, sample, acc_len, path, out_tok, kv_src, kv_dst, err, stream=None):
+    _check("gt_verify_sample", load().gt_verify_sample(
+        _p(logits), _p(tokens), _p(parent), _p(n_nodes), _p(prefix_len), B, N, V, temperature,
+        seed, step, _p(sample), _p(acc_len), _p(path), _p(out_tok), _p(kv_src), _p(kv_dst),
+        _p(err), _s(stream)))
+
+
+def gt_verify_sample_commit(logits, tokens, parent, n_nodes, prefix_len, B, N, V, k,
+                            temperature, seed, step, topk_id, topk_val, sample, acc_len, path,
+                            out_tok, kv_src, kv_dst, table, err, stream=None):
+    _check("gt_verify_sample_commit", load().gt_verify_sample_commit(
+        _p(logits), _p(tokens), _p(parent), _p(n_nodes), _p(prefix_len), B, N, V, k,
+        temperature, seed, step, _p(topk_id), _p(topk_val), _p(sample), _p(acc_len), _p(path),
+        _p(out_tok), _p(kv_src), _p(kv_dst), _p(table), _p(err), _s(stream)))
 
 
 def gt_stage_budget(stage: int, slots: int = 60):

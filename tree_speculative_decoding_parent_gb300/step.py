@@ -57,6 +57,7 @@ class StepBuffers:
         self.O = torch.empty((s.B, s.N, s.Hq, s.d), dtype=odt, device=dev)
         self.topk_id = torch.empty((s.B, s.N, s.k), dtype=i32, device=dev)
         self.topk_val = torch.empty((s.B, s.N, s.k), dtype=torch.float32, device=dev)
+        self.sample = torch.empty((s.B, s.N), dtype=i32, device=dev)  # draws at T > 0
         self.acc_len = torch.empty((s.B,), dtype=i32, device=dev)
         self.path = torch.empty((s.B, s.N), dtype=i32, device=dev)
         self.out_tok = torch.empty((s.B, s.N + 1), dtype=i32, device=dev)
@@ -127,6 +128,16 @@ def run_verify_commit(buf: StepBuffers, inp: dict, stream=None):
                         buf.out_tok, buf.kv_src, buf.kv_dst, inp["table"], buf.err, stream)
 
 
+def run_verify_sample_commit(buf: StepBuffers, inp: dict, temperature: float, seed: int,
+                             step: int, stream=None):
+    """a5+a6+a7 at temperature T > 0: per-node draws, top-k, sampled walk + table update."""
+    s = buf.shape
+    gt.gt_verify_sample_commit(inp["logits"], buf.tokens, buf.parent, buf.n_nodes,
+                               inp["prefix_len"], s.B, s.N, s.V, s.k, temperature, seed, step,
+                               buf.topk_id, buf.topk_val, buf.sample, buf.acc_len, buf.path,
+                               buf.out_tok, buf.kv_src, buf.kv_dst, inp["table"], buf.err, stream)
+
+
 def run_kv_commit(buf: StepBuffers, inp: dict, stream=None):
     """Move the accepted path's K/V rows to their committed positions (in place)."""
     s = buf.shape
@@ -134,9 +145,15 @@ def run_kv_commit(buf: StepBuffers, inp: dict, stream=None):
                     s.d, s.Lcap, s.dtype, buf.err, stream)
 
 
-def run_step(buf: StepBuffers, inp: dict, stream=None, scale=None, fused: bool = True):
-    """The whole verify-and-graft step (a1..a7) on one stream, no host synchronisation."""
-    if fused:
+def run_step(buf: StepBuffers, inp: dict, stream=None, scale=None, fused: bool = True,
+             temperature: float = 0.0, seed: int = 0, step: int = 0):
+    """The whole verify-and-graft step (a1..a7) on one stream, no host synchronisation.
+    temperature > 0 verifies by one target draw per node (seed, step pick the draws)."""
+    if temperature > 0:
+        run_tree_build(buf, inp, stream)
+        run_attn(buf, inp, stream, scale)
+        run_verify_sample_commit(buf, inp, temperature, seed, step, stream)
+    elif fused:
         run_tree_build(buf, inp, stream)
         run_attn(buf, inp, stream, scale)
         run_verify_commit(buf, inp, stream)
