@@ -27,3 +27,8 @@ from .sampling import (  # noqa: F401
     verify_sampled,
     vocab_sample,
 )
+from .drafting import (  # noqa: F401
+    frontier_select,
+    ngram_children,
+    tree_attach,
+)
