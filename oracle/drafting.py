@@ -18,7 +18,8 @@ Sources (page title, then section):
               context n-gram index).
 
 Readings where the pages are silent (each one is also listed in the design doc):
-  * Frontier: the top-W pool nodes by (score desc, index asc). The small drafter's pool is
+  * Frontier: the top-W pool nodes by (score desc, index asc; NaN last, as in the prune).
+    The small drafter's pool is
     the nodes added by the previous step, [first_new, n); the mid drafter's pool is every
     node not yet visited, and afterwards every node of the tree counts as visited.
   * Attach: children are appended after the existing nodes, frontier by frontier in
@@ -56,7 +57,11 @@ def frontier_select(score, n: int, W: int, pool_lo: Optional[int] = None,
         pool = list(range(max(0, int(pool_lo)), n))
     else:
         pool = [v for v in range(n) if not visited[v]]
-    order = sorted(pool, key=lambda v: (-float(np.float32(score[v])), v))
+    def key(v):  # score descending, NaN last, +0.0 equal to -0.0, then index ascending
+        x = float(np.float32(score[v]))
+        return (x != x, 0.0 if x != x else -x, v)
+
+    order = sorted(pool, key=key)
     front = order[:W]
     new_visited = None
     if visited is not None:
