@@ -332,6 +332,61 @@ int gt_verify_sample_commit(const float *logits, const int32_t *tokens, const in
                             int32_t *table, int32_t *err, gt_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
+ * Drafting side of a tree step.  [TreeGraft] §一 (an n-gram small drafter and a neural mid
+ *     drafter grow one shared tree), §三 (top-W frontier of a candidate pool by cumulative
+ *     path score, top-m children per frontier node), §四 Where / How (pools; attach without
+ *     overwriting), §七 item 6 (the n-gram drafter: the target's top-m cache of prefill and a
+ *     context n-gram index).
+ *
+ * gt_frontier_select: frontier[b][0..n_frontier[b]) = the top-W pool nodes of request b by
+ *   (score desc, index asc; NaN last, +0.0 equal to -0.0). Pool: nodes [pool_lo[b], n) (the
+ *   small drafter's newest nodes) when pool_lo is given; else the nodes with
+ *   visited[b][v] == 0 (the mid drafter), after which visited[b][v] = 1 for every v < n.
+ *   Exactly one of pool_lo and visited is non-NULL.
+ *   device in : score f32 [B][Nmax]; n_nodes i32 [B]; pool_lo i32 [B] | visited u8 [B][Nmax]
+ *   device out: frontier i32 [B][W] (-1 padded); n_frontier i32 [B]
+ *   Limits: Nmax <= 1024, 1 <= W <= 64. Device errors: GT_ERR_RANGE (n outside [1, Nmax]).
+ * gt_ngram_draft: children of every frontier node from the n-gram drafter. The key of
+ *   node f is the last q tokens of hist[b][0..hist_len[b]) followed by the tokens of the
+ *   root-to-f path; the drafter finds the most recent position i with
+ *   hist[i-q+1..i] = key, trying q = q_max first and backing off to 1, and returns row i of
+ *   the top-m cache (the target's m most likely tokens for position i+1, with
+ *   probabilities). No match: ids -1, probabilities 0.
+ *   device in : hist i32 [B][Lh]; hist_len i32 [B]; cache_id i32 [B][Lh][m];
+ *               cache_p f32 [B][Lh][m]; parent, tokens i32 [B][Nmax]; n_nodes i32 [B];
+ *               frontier i32 [B][W]; n_frontier i32 [B]
+ *   device out: child_id i32 [B][W][m]; child_p f32 [B][W][m]; match i32 [B][W][2]
+ *               (nullable: matched position or -1, matched length q or 0)
+ *   Limits: Nmax <= 1024, W <= 64, m <= 32, q_max <= 8. Device errors: GT_ERR_RANGE (n,
+ *   hist_len, n_frontier or a frontier node out of range), GT_ERR_TREE (a parent not
+ *   earlier than its child).
+ * gt_tree_attach: non-destructive attach. The children with id >= 0 take the slots n, n+1,
+ *   ... in (frontier order, child order) until Nmax; child score = fl(score(f) * p);
+ *   existing nodes never change; slots past the new count are set to -1 / -1 / 0.
+ *   n_nodes[b] becomes the new count and first_new[b] the old one (the next small step's
+ *   pool).
+ *   device in/out: parent, tokens i32 [B][Nmax]; score f32 [B][Nmax]; n_nodes i32 [B]
+ *   device in    : frontier i32 [B][W]; n_frontier i32 [B]; child_id i32 [B][W][m];
+ *                  child_p f32 [B][W][m]          device out: first_new i32 [B]
+ *   Limits: Nmax <= 1024, W <= 64, m <= 32, W*m <= 1024. Device errors: GT_ERR_RANGE (n,
+ *   n_frontier or a frontier node out of range), GT_ERR_TREE (a child id outside [-1, V));
+ *   such a request keeps its tree.
+ * ------------------------------------------------------------------------------------- */
+int gt_frontier_select(const float *score, const int32_t *n_nodes, int B, int Nmax,
+                       const int32_t *pool_lo, uint8_t *visited, int W, int32_t *frontier,
+                       int32_t *n_frontier, int32_t *err, gt_stream_t stream);
+int gt_ngram_draft(const int32_t *hist, const int32_t *hist_len, int B, int Lh,
+                   const int32_t *cache_id, const float *cache_p, int m, const int32_t *parent,
+                   const int32_t *tokens, const int32_t *n_nodes, int Nmax,
+                   const int32_t *frontier, const int32_t *n_frontier, int W, int q_max,
+                   int32_t *child_id, float *child_p, int32_t *match, int32_t *err,
+                   gt_stream_t stream);
+int gt_tree_attach(int32_t *parent, int32_t *tokens, float *score, int32_t *n_nodes, int B,
+                   int Nmax, const int32_t *frontier, const int32_t *n_frontier, int W,
+                   const int32_t *child_id, const float *child_p, int m, int V,
+                   int32_t *first_new, int32_t *err, gt_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
  * Host helpers (host pointers, synchronous, no CUDA calls).
  *
  * gt_stage_budget: draft / retrieved split of `slots` for a prune at stage 0, 1 or 5

@@ -45,6 +45,11 @@ _SIGS = {
                               _vp, _vp, _vp, _vp, _vp]),
     "gt_verify_sample_commit": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _u64, _u64,
                                      _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "gt_frontier_select": (_i, [_vp, _vp, _i, _i, _vp, _vp, _i, _vp, _vp, _vp, _vp]),
+    "gt_ngram_draft": (_i, [_vp, _vp, _i, _i, _vp, _vp, _i, _vp, _vp, _vp, _i, _vp, _vp, _i, _i,
+                            _vp, _vp, _vp, _vp, _vp]),
+    "gt_tree_attach": (_i, [_vp, _vp, _vp, _vp, _i, _i, _vp, _vp, _i, _vp, _vp, _i, _i, _vp, _vp,
+                            _vp]),
     "gt_stage_budget": (_i, [_i, _i, _vp, _vp]),
     "gt_default_template": (_i, [_i, _i, _i, _vp, _vp]),
     "gt_status_string": (ctypes.c_char_p, [_i]),
@@ -220,6 +225,28 @@ def gt_verify_sample_commit(logits, tokens, parent, n_nodes, prefix_len, B, N, V
         _p(logits), _p(tokens), _p(parent), _p(n_nodes), _p(prefix_len), B, N, V, k,
         temperature, seed, step, _p(topk_id), _p(topk_val), _p(sample), _p(acc_len), _p(path),
         _p(out_tok), _p(kv_src), _p(kv_dst), _p(table), _p(err), _s(stream)))
+
+
+def gt_frontier_select(score, n_nodes, B, Nmax, pool_lo, visited, W, frontier, n_frontier, err,
+                       stream=None):
+    _check("gt_frontier_select", load().gt_frontier_select(
+        _p(score), _p(n_nodes), B, Nmax, _p(pool_lo), _p(visited), W, _p(frontier),
+        _p(n_frontier), _p(err), _s(stream)))
+
+
+def gt_ngram_draft(hist, hist_len, B, Lh, cache_id, cache_p, m, parent, tokens, n_nodes, Nmax,
+                   frontier, n_frontier, W, q_max, child_id, child_p, match, err, stream=None):
+    _check("gt_ngram_draft", load().gt_ngram_draft(
+        _p(hist), _p(hist_len), B, Lh, _p(cache_id), _p(cache_p), m, _p(parent), _p(tokens),
+        _p(n_nodes), Nmax, _p(frontier), _p(n_frontier), W, q_max, _p(child_id), _p(child_p),
+        _p(match), _p(err), _s(stream)))
+
+
+def gt_tree_attach(parent, tokens, score, n_nodes, B, Nmax, frontier, n_frontier, W, child_id,
+                   child_p, m, V, first_new, err, stream=None):
+    _check("gt_tree_attach", load().gt_tree_attach(
+        _p(parent), _p(tokens), _p(score), _p(n_nodes), B, Nmax, _p(frontier), _p(n_frontier), W,
+        _p(child_id), _p(child_p), m, V, _p(first_new), _p(err), _s(stream)))
 
 
 def gt_stage_budget(stage: int, slots: int = 60):

@@ -9,6 +9,9 @@ from .synth import (  # noqa: F401
     eagle_tree,
     f32_to_bf16_bits,
     make_scenario,
+    DraftScenario,
+    make_draft_scenario,
+    topm_cache,
     plant_logits,
     static_tree_widths,
     stream_table,

@@ -272,6 +272,67 @@ def stream_table(rng: np.random.Generator, V: int, k: int, length: int = 1 << 20
 
 
 # ----------------------------------------------------------------------------------------
+# Inputs of the n-gram drafter: a token history and the target's top-m cache of prefill
+# ----------------------------------------------------------------------------------------
+
+
+def topm_cache(rng: np.random.Generator, seq: np.ndarray, V: int, m: int,
+               p_hit: float = 0.6):
+    """A stand-in for the target's top-m cache of prefill over the history ``seq[:-1]``.
+
+    Row i lists m token ids for position i+1 with float32 probabilities in descending
+    order (a softmax of m N(0, 1.5^2) draws scaled by a mass in [0.5, 0.95]). With
+    probability p_hit the true next token seq[i+1] sits at a uniform rank; the other ids
+    are tokens of uniformly drawn stream positions (plausible alternatives, distributed
+    like the stream itself).
+    """
+    L = len(seq) - 1
+    ids = np.asarray(seq, np.int32)[rng.integers(0, L + 1, size=(L, m))]
+    hit = rng.random(L) < p_hit
+    rank = rng.integers(0, m, size=L)
+    rows = np.nonzero(hit)[0]
+    ids[rows, rank[rows]] = seq[1:][rows]
+    z = rng.standard_normal((L, m)) * 1.5
+    w = np.exp(z - z.max(axis=1, keepdims=True))
+    probs = -np.sort(-(w / w.sum(axis=1, keepdims=True)), axis=1)
+    mass = rng.uniform(0.5, 0.95, size=(L, 1))
+    return ids, (probs * mass).astype(np.float32)
+
+
+@dataclasses.dataclass
+class DraftScenario:
+    """Inputs of n-gram drafting steps for B requests (numpy, host memory)."""
+    hist: np.ndarray       # int32 [B][L] committed tokens before the root
+    hist_len: np.ndarray   # int32 [B]
+    cache_id: np.ndarray   # int32 [B][L][m]
+    cache_p: np.ndarray    # float32 [B][L][m]
+    root: np.ndarray       # int32 [B] the current token (tree node 0)
+    V: int
+    m: int
+    W: int
+    q_max: int
+    Nmax: int
+
+
+def make_draft_scenario(B: int = 1, L: int = 32768, V: int = 151936, m: int = 10, W: int = 10,
+                        q_max: int = 4, Nmax: int = 256, seed: int = 7) -> DraftScenario:
+    """Code-like histories (the repetitive stream of the successor tables) with their
+    top-m caches; the tree starts as the root alone (TreeGraft write-up §五: D = 5,
+    W = 10, m = 10; growth capped at Nmax nodes before the prune)."""
+    rngs = _rngs(seed, 2 * B)
+    hist = np.zeros((B, L), np.int32)
+    cid = np.zeros((B, L, m), np.int32)
+    cp = np.zeros((B, L, m), np.float32)
+    root = np.zeros(B, np.int32)
+    for b in range(B):
+        seq = repetitive_stream(rngs[2 * b], V, L + 1).astype(np.int32)
+        hist[b], root[b] = seq[:L], seq[L]
+        cid[b], cp[b] = topm_cache(rngs[2 * b + 1], seq, V, m)
+    return DraftScenario(hist=hist, hist_len=np.full(B, L, np.int32), cache_id=cid, cache_p=cp,
+                         root=root, V=V, m=m, W=W, q_max=q_max, Nmax=Nmax)
+
+
+# ----------------------------------------------------------------------------------------
 # Target stand-in: logits with a planted peak per node
 # ----------------------------------------------------------------------------------------
 
