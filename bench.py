@@ -425,6 +425,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     }
     if breakdown is not None:
         line["breakdown_us"] = breakdown
+        line["drafter_us"] = draft_timing(torch, gt)
     if not args.no_cpu_baseline:
         cv, cdone, cdt = time_oracle(scn, 1000, args.cpu_budget, args.temperature, args.seed)
         line["cpu_baseline"] = {
@@ -432,6 +433,71 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
             "sample": f"{cdone} whole steps of the same workload (~{cdt:.0f} s, numpy float64; "
                       "BLAS may use every core, the tree and top-k loops use one)"}
     return line
+
+
+def draft_timing(torch, gt, reps: int = 20):
+    """Device time of n-gram drafting steps (frontier select, n-gram draft, attach; three
+    launches each), growing D = 5 steps from the root in a CUDA graph (schedule small,
+    mid, small, mid, small; W = 10, m = 10, keys of up to 4 tokens) over 32,768-token
+    histories. Returns microseconds per step for B = 1 and B = 16."""
+    from workload import make_draft_scenario
+    res = {}
+    for B in (1, 16):
+        ds = make_draft_scenario(B=B, L=32768, V=151936)
+        N = ds.Nmax
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+        par0 = np.full((B, N), -1, np.int32)
+        tok0 = np.full((B, N), -1, np.int32)
+        tok0[:, 0] = ds.root
+        sc0 = np.zeros((B, N), np.float32)
+        sc0[:, 0] = 1.0
+        init = dict(parent=t(par0), tokens=t(tok0), score=t(sc0), n=t(np.ones(B, np.int32)),
+                    first_new=t(np.zeros(B, np.int32)),
+                    visited=torch.zeros((B, N), dtype=torch.uint8, device="cuda"))
+        cur = {k: v.clone() for k, v in init.items()}
+        hist, hlen, cid, cp = t(ds.hist), t(ds.hist_len), t(ds.cache_id), t(ds.cache_p)
+        fr = torch.empty((B, ds.W), dtype=torch.int32, device="cuda")
+        nfr = torch.empty(B, dtype=torch.int32, device="cuda")
+        kid = torch.empty((B, ds.W, ds.m), dtype=torch.int32, device="cuda")
+        kp = torch.empty((B, ds.W, ds.m), dtype=torch.float32, device="cuda")
+        match = torch.empty((B, ds.W, 2), dtype=torch.int32, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+        def grow(s):
+            for mid in (0, 1, 0, 1, 0):
+                gt.gt_frontier_select(cur["score"], cur["n"], B, N,
+                                      None if mid else cur["first_new"],
+                                      cur["visited"] if mid else None, ds.W, fr, nfr, err, s)
+                gt.gt_ngram_draft(hist, hlen, B, hist.shape[1], cid, cp, ds.m, cur["parent"],
+                                  cur["tokens"], cur["n"], N, fr, nfr, ds.W, ds.q_max, kid, kp,
+                                  match, err, s)
+                gt.gt_tree_attach(cur["parent"], cur["tokens"], cur["score"], cur["n"], B, N, fr,
+                                  nfr, ds.W, kid, kp, ds.m, ds.V, cur["first_new"], err, s)
+
+        grow(torch.cuda.current_stream())  # eager warm-up
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for e in (e0, e1):
+            e.record()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            s = torch.cuda.current_stream()
+            for k in cur:
+                cur[k].copy_(init[k])
+            gt.gt_event_record_external(e0, s)
+            grow(s)
+            gt.gt_event_record_external(e1, s)
+        tot = 0.0
+        for _ in range(reps):
+            g.replay()
+            torch.cuda.synchronize()
+            tot += e0.elapsed_time(e1) * 1e3
+        if int(err.item()) != 0:
+            raise RuntimeError(f"drafting device error {gt.status_string(int(err.item()))}")
+        res[f"B{B}"] = {"us_per_step": round(tot / reps / 5, 2),
+                        "nodes_after_5_steps": int(cur["n"].float().mean().item())}
+    return res
 
 
 def call_breakdown(torch, gt, buf, sets, scn, nsets, temperature=0.0, seed=0, reps: int = 50):

@@ -356,7 +356,8 @@ int gt_verify_sample_commit(const float *logits, const int32_t *tokens, const in
  *               cache_p f32 [B][Lh][m]; parent, tokens i32 [B][Nmax]; n_nodes i32 [B];
  *               frontier i32 [B][W]; n_frontier i32 [B]
  *   device out: child_id i32 [B][W][m]; child_p f32 [B][W][m]; match i32 [B][W][2]
- *               (nullable: matched position or -1, matched length q or 0)
+ *               (matched position or -1, matched length q or 0; 8-byte aligned, also the
+ *               call's scratch: the scan merges each key's best match into it)
  *   Limits: Nmax <= 1024, W <= 64, m <= 32, q_max <= 8. Device errors: GT_ERR_RANGE (n,
  *   hist_len, n_frontier or a frontier node out of range), GT_ERR_TREE (a parent not
  *   earlier than its child).

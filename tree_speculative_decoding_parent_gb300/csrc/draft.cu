@@ -68,41 +68,44 @@ frontier_kernel(const float *__restrict__ score, const int32_t *__restrict__ n_n
 // the history, read backwards (key[0] = token(f)), at most q_max long. Position i of the
 // history matches to length ell(i) = the number of leading key tokens equal to
 // H[i], H[i-1], ...; the drafter takes the largest ell, then the largest i (the longest
-// key with a match, at its most recent position), and copies the top-m cache row i. The
-// scan compares every position with every key's first token and walks back only on a
-// hit; the best (ell, i) per key meets in a shared-memory atomic max.
+// key with a match, at its most recent position), and copies the top-m cache row i.
+// The scan is split over a grid of (history chunk, request) CTAs: each compares its
+// positions with every key's first token, walks back only on a hit, and merges its best
+// (ell << 32 | i) per key into the caller's match array with one global atomic max.
 // ------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(NGRAM_THREADS)
-ngram_kernel(const int32_t *__restrict__ hist, const int32_t *__restrict__ hist_len, int Lh,
-             const int32_t *__restrict__ cache_id, const float *__restrict__ cache_p, int m,
-             const int32_t *__restrict__ parent, const int32_t *__restrict__ tokens,
-             const int32_t *__restrict__ n_nodes, int Nmax, const int32_t *__restrict__ frontier,
-             const int32_t *__restrict__ n_frontier, int W, int q_max,
-             int32_t *__restrict__ child_id, float *__restrict__ child_p,
-             int32_t *__restrict__ match, int32_t *err) {
+ngram_scan_kernel(const int32_t *__restrict__ hist, const int32_t *__restrict__ hist_len, int Lh,
+                  int chunk, const int32_t *__restrict__ parent,
+                  const int32_t *__restrict__ tokens, const int32_t *__restrict__ n_nodes,
+                  int Nmax, const int32_t *__restrict__ frontier,
+                  const int32_t *__restrict__ n_frontier, int W, int q_max,
+                  unsigned long long *__restrict__ best_out, int32_t *err) {
   pdl_enter();
   __shared__ int s_key[DRAFT_MAX_W][DRAFT_MAX_Q];
   __shared__ int s_klen[DRAFT_MAX_W];
   __shared__ unsigned long long s_best[DRAFT_MAX_W];
-  const int b = blockIdx.x, tid = threadIdx.x;
+  const int b = blockIdx.y, tid = threadIdx.x;
+  const bool report = blockIdx.x == 0;  // one CTA per request reports data errors
   const size_t row0 = (size_t)b * Nmax;
   const int32_t *H = hist + (size_t)b * Lh;
   const int n = n_nodes[b], L = hist_len[b], nf = n_frontier[b];
   const bool ok = n >= 1 && n <= Nmax && L >= 0 && L <= Lh && nf >= 0 && nf <= W;
-  if (!ok && tid == 0) set_err(err, GT_ERR_RANGE);
+  if (!ok && tid == 0 && report) set_err(err, GT_ERR_RANGE);
   const int nk = ok ? nf : 0;
+  const int i0 = blockIdx.x * chunk, i1 = min(L, i0 + chunk);
+  if (i0 >= i1 && !report) return;  // no positions of this request in this chunk
   if (tid < nk) {
     int t = 0;
     const int f = frontier[(size_t)b * W + tid];
     if (f < 0 || f >= n) {
-      set_err(err, GT_ERR_RANGE);
+      if (report) set_err(err, GT_ERR_RANGE);
     } else {
       // the path from f up to the root (at most q_max steps; parents precede children)
       for (int u = f; u != -1 && t < q_max; ++t) {
         s_key[tid][t] = tokens[row0 + u];
         const int p = parent[row0 + u];
         if (p >= u || p < -1) {
-          set_err(err, GT_ERR_TREE);
+          if (report) set_err(err, GT_ERR_TREE);
           t = 0;
           break;
         }
@@ -115,7 +118,7 @@ ngram_kernel(const int32_t *__restrict__ hist, const int32_t *__restrict__ hist_
     s_best[tid] = 0ull;
   }
   __syncthreads();
-  for (int i = tid; i < L; i += NGRAM_THREADS) {
+  for (int i = i0 + tid; i < i1; i += NGRAM_THREADS) {
     const int h0 = H[i];
     for (int w = 0; w < nk; ++w) {
       if (s_klen[w] == 0 || h0 != s_key[w][0]) continue;
@@ -125,17 +128,36 @@ ngram_kernel(const int32_t *__restrict__ hist, const int32_t *__restrict__ hist_
     }
   }
   __syncthreads();
-  for (int e = tid; e < W * m; e += NGRAM_THREADS) {
+  if (tid < nk && s_best[tid] != 0ull) atomicMax(&best_out[(size_t)b * W + tid], s_best[tid]);
+}
+
+// The children: row `pos` of the top-m cache for every key with a match; the match array
+// becomes (position, length), position -1 without a match.
+__global__ void __launch_bounds__(256)
+ngram_children_kernel(int Lh, const int32_t *__restrict__ cache_id,
+                      const float *__restrict__ cache_p, int m,
+                      const int32_t *__restrict__ n_frontier, int W,
+                      int32_t *__restrict__ child_id, float *__restrict__ child_p,
+                      int32_t *__restrict__ match) {
+  pdl_enter();
+  const int b = blockIdx.x;
+  const int nf = n_frontier[b];
+  const int nk = (nf >= 0 && nf <= W) ? nf : 0;
+  const unsigned long long *best = reinterpret_cast<const unsigned long long *>(match);
+  for (int e = threadIdx.x; e < W * m; e += blockDim.x) {
     const int w = e / m, c = e - w * m;
-    const unsigned long long best = w < nk ? s_best[w] : 0ull;
-    const int ell = (int)(best >> 32), pos = (int)(best & 0xFFFFFFFFull);
+    const unsigned long long bw = w < nk ? best[(size_t)b * W + w] : 0ull;
+    const int ell = (int)(bw >> 32), pos = (int)(bw & 0xFFFFFFFFull);
     const size_t src = ((size_t)b * Lh + pos) * m + c;
     child_id[(size_t)b * W * m + e] = ell ? cache_id[src] : -1;
     child_p[(size_t)b * W * m + e] = ell ? cache_p[src] : 0.0f;
-    if (match && c == 0) {
-      match[((size_t)b * W + w) * 2] = ell ? pos : -1;
-      match[((size_t)b * W + w) * 2 + 1] = ell;
-    }
+  }
+  __syncthreads();  // every read of the packed bests is done before they are rewritten
+  for (int w = threadIdx.x; w < W; w += blockDim.x) {
+    const unsigned long long bw = w < nk ? best[(size_t)b * W + w] : 0ull;
+    const int ell = (int)(bw >> 32);
+    match[((size_t)b * W + w) * 2] = ell ? (int)(bw & 0xFFFFFFFFull) : -1;
+    match[((size_t)b * W + w) * 2 + 1] = ell;
   }
 }
 
@@ -213,15 +235,34 @@ GT_API int gt_ngram_draft(const int32_t *hist, const int32_t *hist_len, int B, i
                           int q_max, int32_t *child_id, float *child_p, int32_t *match,
                           int32_t *err, gt_stream_t stream) {
   if (B < 0 || Lh < 0 || m < 1 || Nmax < 1 || W < 1 || q_max < 1) return GT_ERR_ARG;
-  if (Nmax > 1024 || W > DRAFT_MAX_W || m > DRAFT_MAX_M || q_max > DRAFT_MAX_Q)
+  if (Nmax > 1024 || W > DRAFT_MAX_W || m > DRAFT_MAX_M || q_max > DRAFT_MAX_Q || B > 65535)
     return GT_ERR_SHAPE;
   if (B == 0) return GT_OK;
   if (!hist_len || !parent || !tokens || !n_nodes || !frontier || !n_frontier || !child_id ||
-      !child_p || (Lh > 0 && (!hist || !cache_id || !cache_p)))
+      !child_p || !match || ((uintptr_t)match & 7) ||
+      (Lh > 0 && (!hist || !cache_id || !cache_p)))
     return GT_ERR_ARG;
-  return launch(ngram_kernel, dim3(B), dim3(NGRAM_THREADS), 0, (cudaStream_t)stream, hist,
-                hist_len, Lh, cache_id, cache_p, m, parent, tokens, n_nodes, Nmax, frontier,
-                n_frontier, W, q_max, child_id, child_p, match, err);
+  cudaStream_t s = (cudaStream_t)stream;
+  // the match array holds each key's packed best (length << 32 | position) during the scan
+  cudaError_t e = cudaMemsetAsync(match, 0, sizeof(int32_t) * 2 * (size_t)B * W, s);
+  if (e != cudaSuccess) return launch_status(e, "cudaMemsetAsync(match)");
+  // history chunks per request: enough CTAs for about two per SM, each at least 1024
+  // positions long
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    sms = 148;
+  }
+  const int want = max(1, (2 * sms + B - 1) / B);
+  const int C = max(1, min(want, (Lh + 1023) / 1024));
+  const int chunk = max(1, (Lh + C - 1) / C);
+  int rc = launch(ngram_scan_kernel, dim3(C, B), dim3(NGRAM_THREADS), 0, s, hist, hist_len, Lh,
+                  chunk, parent, tokens, n_nodes, Nmax, frontier, n_frontier, W, q_max,
+                  reinterpret_cast<unsigned long long *>(match), err);
+  if (rc != GT_OK) return rc;
+  return launch(ngram_children_kernel, dim3(B), dim3(256), 0, s, Lh, cache_id, cache_p, m,
+                n_frontier, W, child_id, child_p, match);
 }
 
 GT_API int gt_tree_attach(int32_t *parent, int32_t *tokens, float *score, int32_t *n_nodes,
