@@ -363,9 +363,13 @@ GT_API int gt_tree_attn(const void *Q, const void *K, const void *V, const uint6
   // the tcgen05 kernel runs one cluster per piece: aim for one wave of clusters
   const int Gs = tc ? attn_tc_pieces(g, N) : G;
   const SchedArgs sa{prefix_len, n_nodes, B, Hkv, N, Lcap, TK, Gs};
+  // pieces the schedule can make: at most Gs while the segments are fewer than Gs (the
+  // piece length is then searched so that they fit), else at most Gs + S. CTAs of pieces
+  // past the schedule's count would only wait for an SM, find no work and exit.
+  const int grid_pieces = S < Gs ? Gs : Gs + S;
   int rc;
   if (tc) {
-    rc = attn_tc_launch(Q, K, V, mask, sa, B, N, Hq, Hkv, Lcap, scale, ws, err, s);
+    rc = attn_tc_launch(Q, K, V, mask, sa, B, N, Hq, Hkv, Lcap, scale, ws, grid_pieces, err, s);
   } else if (dtype == GT_F32) {
     static bool attr_f32 = false;
     if (!attr_f32) {
@@ -374,7 +378,7 @@ GT_API int gt_tree_attn(const void *Q, const void *K, const void *V, const uint6
       if (e != cudaSuccess) return launch_status(e, "cudaFuncSetAttribute(attn_simt_kernel)");
       attr_f32 = true;
     }
-    rc = launch(attn_simt_kernel<float>, dim3(ws.maxp, ceil_div(g * N, SIMT_ROWS)), dim3(256),
+    rc = launch(attn_simt_kernel<float>, dim3(grid_pieces, ceil_div(g * N, SIMT_ROWS)), dim3(256),
                 SIMT_SMEM, s, (const float *)Q, (const float *)K, (const float *)V, mask,
                 prefix_len, n_nodes, N, Hq, Hkv, Lcap, scale, sa, ws, err);
   } else {
@@ -386,7 +390,7 @@ GT_API int gt_tree_attn(const void *Q, const void *K, const void *V, const uint6
       if (e != cudaSuccess) return launch_status(e, "cudaFuncSetAttribute(attn_simt_kernel)");
       attr_bf16 = true;
     }
-    rc = launch(attn_simt_kernel<__nv_bfloat16>, dim3(ws.maxp, ceil_div(g * N, SIMT_ROWS)),
+    rc = launch(attn_simt_kernel<__nv_bfloat16>, dim3(grid_pieces, ceil_div(g * N, SIMT_ROWS)),
                 dim3(256), SIMT_SMEM, s, (const __nv_bfloat16 *)Q, (const __nv_bfloat16 *)K,
                 (const __nv_bfloat16 *)V, mask, prefix_len, n_nodes, N, Hq, Hkv, Lcap, scale,
                 sa, ws, err);

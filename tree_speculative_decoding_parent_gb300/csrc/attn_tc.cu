@@ -628,7 +628,7 @@ int attn_tc_pieces(int g, int N) {
 
 int attn_tc_launch(const void *Q, const void *K, const void *V, const uint64_t *mask,
                    const SchedArgs &sa, int B, int N, int Hq, int Hkv, int Lcap, float scale,
-                   const AttnWs &ws, int32_t *err, cudaStream_t s) {
+                   const AttnWs &ws, int pieces, int32_t *err, cudaStream_t s) {
   const int g = Hq / Hkv;
   const int C = cluster_of(g, N), L = loaders_of(C);
   CUtensorMap mK, mV;
@@ -644,8 +644,8 @@ int attn_tc_launch(const void *Q, const void *K, const void *V, const uint64_t *
     return GT_ERR_CUDA;
   }
   if (!set_attributes()) return GT_ERR_CUDA;
-  // one cluster of C CTAs per piece; the schedule never makes more than ws.maxp pieces
-  return launch_cluster(attn_tc_kernel, dim3(C * ws.maxp), dim3(TC_THREADS), dim3(C, 1, 1),
+  // one cluster of C CTAs per piece; the schedule never makes more than `pieces`
+  return launch_cluster(attn_tc_kernel, dim3(C * pieces), dim3(TC_THREADS), dim3(C, 1, 1),
                         TC_SMEM, s, (const __nv_bfloat16 *)Q, mK, mV, mask, sa.prefix_len, sa.n_nodes, N, Hq, Hkv,
                         scale, C, L, sa, ws, err);
 }

@@ -18,9 +18,10 @@ bool attn_tc_supported(int g, int N);
 int attn_tc_pieces(int g, int N);
 
 // Runs every split-KV piece of the schedule (tiles of ATTN_TC_KEYS keys, computed in the
-// kernel from `sa`) and writes the partial O / LSE rows of every piece.
+// kernel from `sa`) and writes the partial O / LSE rows of every piece. `pieces` bounds the
+// schedule's piece count (one cluster is launched per possible piece).
 int attn_tc_launch(const void *Q, const void *K, const void *V, const uint64_t *mask,
                    const SchedArgs &sa, int B, int N, int Hq, int Hkv, int Lcap, float scale,
-                   const AttnWs &ws, int32_t *err, cudaStream_t s);
+                   const AttnWs &ws, int pieces, int32_t *err, cudaStream_t s);
 
 }  // namespace gt
