@@ -87,6 +87,71 @@ __device__ __forceinline__ int4 schedule_piece(const SchedArgs &a, int p, AttnWs
     if (!ok && publisher && (s % a.Hkv) == 0 && err) atomicCAS(err, 0, GT_ERR_RANGE);
     return ok ? (P + n + a.TK - 1) / a.TK : 0;
   };
+  if (S <= 32 * CH) {
+    // few segments: warp 0 computes the whole schedule with shuffles (lane l holds segments
+    // l, l + 32, ...), the same tau and pieces as the block version below, and the CTA
+    // meets it at one barrier
+    if (warp == 0) {
+      if (lane == 0) s_piece = make_int4(-1, 0, 0, 0);
+      __syncwarp();
+      int wt[CH];
+      long long local = 0;
+#pragma unroll
+      for (int i = 0; i < CH; ++i) {
+        const int s = lane + 32 * i;
+        wt[i] = s < S ? tiles_of(s) : 0;
+        local += wt[i] + ((long long)(wt[i] > 0) << 44);
+      }
+      auto warp_sum = [&](long long v) {
+#pragma unroll
+        for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        return v;
+      };
+      const long long both = warp_sum(local);
+      const long long T = both & ((1ll << 44) - 1), Sn = both >> 44;
+      int tau = (int)max(1ll, (T + a.G - 1) / a.G);
+      if (Sn > 0 && a.G > Sn) {
+        int lo = tau, hi = (int)max((long long)tau, (T + (a.G - Sn) - 1) / (a.G - Sn));
+        while (lo < hi) {
+          const int mid = lo + (hi - lo) / 2;
+          long long c = 0;
+#pragma unroll
+          for (int i = 0; i < CH; ++i) c += (wt[i] + mid - 1) / mid;
+          if (warp_sum(c) <= a.G)
+            hi = mid;
+          else
+            lo = mid + 1;
+        }
+        tau = lo;
+      }
+      // pieces in segment order: segments lane + 32 i for i = 0, 1, ...
+      int base = 0;
+#pragma unroll
+      for (int i = 0; i < CH; ++i) {
+        const int s = lane + 32 * i;
+        const int cnt = (wt[i] + tau - 1) / tau;
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const int off = base + incl - cnt;
+        if (s < S) {
+          if (publisher) ws.seg[s] = make_int2(off, cnt);
+          if (p >= off && p < off + cnt) {
+            const int j = p - off, t = wt[i];
+            s_piece = make_int4(s, (int)((long long)t * j / cnt),
+                                (int)((long long)t * (j + 1) / cnt), 0);
+          }
+        }
+        base += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (publisher && lane == 0) ws.hdr[0] = base;
+    }
+    __syncthreads();
+    return s_piece;
+  }
   int tl[CH];  // tiles of this thread's first CH segments
 #pragma unroll
   for (int i = 0; i < CH; ++i) tl[i] = c0 + i < c1 ? tiles_of(c0 + i) : 0;
