@@ -90,7 +90,8 @@ int gt_prune_topB(const float *score, const int32_t *parent, const int32_t *toke
 
 /* ---------------------------------------------------------------------------------------
  * a2. Graft retrieved nodes into the freed slots.  [Graft] §二 (second gear), §四;
- *     Graft-TAIL: [Graft] §一 (the suffix of a drafter's chain is extended by retrieval).
+ *     Graft-TAIL: [Graft] §七 (the low-confidence tail of a block draft is replaced by
+ *     retrieved candidates).
  *
  * In place on the kept trees. For request b with n = n_nodes[b] kept nodes, the
  * retrieved tree hangs from the anchor node a = anchor[b] (anchor NULL: a = 0, the root;

@@ -147,7 +147,7 @@ def treegraft_tree(rng_small: np.random.Generator, rng_mid: np.random.Generator,
 
 
 def dflash_chain(rng: np.random.Generator, V: int, L: int = 16):
-    """One block draft of L tokens as a chain below the root (Graft write-up §五, DFlash).
+    """One block draft of L tokens as a chain below the root (Graft write-up §七, DFlash).
 
     A block drafter proposes L tokens at once, each with its own confidence. The tokens
     are uniform draws; the confidence c_i of position i is a Beta(8, 2) draw scaled by
