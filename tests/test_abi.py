@@ -63,3 +63,33 @@ def test_status_strings_and_arg_errors(lib):
                             None, None, None, None) == lib.GT_ERR_SHAPE
     assert so.gt_prune_topB(None, None, None, None, 0, 10, None, None, 60, None, None, None,
                             None, None, None, None) == lib.GT_OK
+
+
+def test_sampling_and_drafting_calls_validate_arguments_without_gpu(lib):
+    so = lib.load()
+    P = 4096  # a stand-in address: these calls must return before any CUDA work
+    ARG, SHAPE, OK = lib.GT_ERR_ARG, lib.GT_ERR_SHAPE, lib.GT_OK
+    for T in (0.0, -1.0, float("inf"), float("nan"), 1e-39):
+        assert so.gt_vocab_sample(P, 2, 100, T, 1, 1, P, None) == ARG
+    assert so.gt_vocab_sample(None, 0, 100, 1.0, 1, 1, None, None) == OK
+    assert so.gt_vocab_sample(P, 2, 0, 1.0, 1, 1, P, None) == ARG
+    assert so.gt_verify_sample(P, P, P, P, P, 1, 2000, 10, 1.0, 1, 1, P, P, P, P, P, P, P,
+                               None) == SHAPE
+    assert so.gt_verify_sample(None, None, None, None, None, 0, 60, 10, 1.0, 1, 1, None, None,
+                               None, None, None, None, None, None) == OK
+    assert so.gt_verify_sample_commit(P, P, P, P, P, 1, 60, 100, 17, 1.0, 1, 1, P, P, P, P, P, P,
+                                      P, P, P, P, None) == SHAPE
+    # drafting: frontier width, both pools, key length, match alignment, children per CTA
+    assert so.gt_frontier_select(P, P, 1, 256, P, None, 65, P, P, P, None) == SHAPE
+    assert so.gt_frontier_select(P, P, 1, 256, P, P, 10, P, P, P, None) == ARG
+    assert so.gt_frontier_select(P, P, 1, 256, None, None, 10, P, P, P, None) == ARG
+    assert so.gt_ngram_draft(P, P, 1, 100, P, P, 10, P, P, P, 256, P, P, 10, 9, P, P, P, P,
+                             None) == SHAPE
+    assert so.gt_ngram_draft(P, P, 1, 100, P, P, 10, P, P, P, 256, P, P, 10, 4, P, P, P + 4, P,
+                             None) == ARG
+    assert so.gt_ngram_draft(P, P, 1, 100, P, P, 10, P, P, P, 256, P, P, 10, 4, P, P, None, P,
+                             None) == ARG
+    assert so.gt_tree_attach(P, P, P, P, 1, 256, P, P, 64, P, P, 32, 100, P, P, None) == SHAPE
+    assert so.gt_tree_attach(P, P, P, P, 1, 256, P, P, 10, P, P, 10, 0, P, P, None) == ARG
+    # KV commit: rows must be whole 16-byte chunks
+    assert so.gt_kv_commit(P, P, P, P, P, 1, 8, 8, 100, 1000, lib.GT_BF16, P, None) == SHAPE
