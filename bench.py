@@ -144,8 +144,8 @@ def job_throughput(world: int, steps_per_rank: int, seconds: float) -> float:
 
 
 def _traffic_record(kernel_key: str):
-    """DRAM bytes per launch from a committed ncu summary, if the kernel source it was taken
-    on is unchanged (sha256 of the CUDA sources), else None."""
+    """DRAM bytes per launch from a committed ncu summary, if the kernel's sources are
+    unchanged since the capture (sha256 of ATTN_SOURCES), else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -156,10 +156,16 @@ def _traffic_record(kernel_key: str):
     return rec["bytes_per_launch"] if rec.get("src_sha256") == _src_hash() else None
 
 
-def _src_hash() -> str:
+# the sources the attention kernels (tcgen05, SIMT, combine) are compiled from
+ATTN_SOURCES = ("attn.cu", "attn_tc.cu", "attn_tc.cuh", "attn_common.cuh", "tc_ptx.cuh",
+                "gt_internal.cuh", "launch.cuh")
+
+
+def _src_hash(names=ATTN_SOURCES) -> str:
+    """sha256 over the named CUDA sources (name and content, in the given order)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "tree_speculative_decoding_parent_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in names:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()
