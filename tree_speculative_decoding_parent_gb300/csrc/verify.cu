@@ -685,7 +685,9 @@ static int walk_update_launch(const int32_t *tokens, const int32_t *parent,
                               int V, int k, const int32_t *topk_id, const int32_t *sample,
                               int32_t *acc_len, int32_t *path, int32_t *out_tok, int32_t *kv_src,
                               int32_t *kv_dst, int32_t *table, int32_t *err, cudaStream_t s) {
-  const int threads = (N + 31) / 32 * 32;
+  // a thread per node for the walk; up to 512 threads so that the B*N verified tokens every
+  // CTA stages and hashes take a few load rounds instead of B rounds
+  const int threads = (max(N, min(B * N, 512)) + 31) / 32 * 32;
   size_t smem = sizeof(int) * (4 * (size_t)N + (size_t)B * N);
   // the token hash: a power of two at least twice B*N, when it fits (else the scan)
   int hs = 1;
