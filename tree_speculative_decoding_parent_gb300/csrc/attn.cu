@@ -371,25 +371,18 @@ GT_API int gt_tree_attn(const void *Q, const void *K, const void *V, const uint6
   if (tc) {
     rc = attn_tc_launch(Q, K, V, mask, sa, B, N, Hq, Hkv, Lcap, scale, ws, grid_pieces, err, s);
   } else if (dtype == GT_F32) {
-    static bool attr_f32 = false;
-    if (!attr_f32) {
-      const cudaError_t e = cudaFuncSetAttribute(
-          attn_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SIMT_SMEM);
-      if (e != cudaSuccess) return launch_status(e, "cudaFuncSetAttribute(attn_simt_kernel)");
-      attr_f32 = true;
-    }
+    static SmemAttr attr_f32;
+    rc = ensure_smem(attn_simt_kernel<float>, (int)SIMT_SMEM, attr_f32,
+                     "cudaFuncSetAttribute(attn_simt_kernel)");
+    if (rc != GT_OK) return rc;
     rc = launch(attn_simt_kernel<float>, dim3(grid_pieces, ceil_div(g * N, SIMT_ROWS)), dim3(256),
                 SIMT_SMEM, s, (const float *)Q, (const float *)K, (const float *)V, mask,
                 prefix_len, n_nodes, N, Hq, Hkv, Lcap, scale, sa, ws, err);
   } else {
-    static bool attr_bf16 = false;
-    if (!attr_bf16) {
-      const cudaError_t e =
-          cudaFuncSetAttribute(attn_simt_kernel<__nv_bfloat16>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SIMT_SMEM);
-      if (e != cudaSuccess) return launch_status(e, "cudaFuncSetAttribute(attn_simt_kernel)");
-      attr_bf16 = true;
-    }
+    static SmemAttr attr_bf16;
+    rc = ensure_smem(attn_simt_kernel<__nv_bfloat16>, (int)SIMT_SMEM, attr_bf16,
+                     "cudaFuncSetAttribute(attn_simt_kernel)");
+    if (rc != GT_OK) return rc;
     rc = launch(attn_simt_kernel<__nv_bfloat16>, dim3(grid_pieces, ceil_div(g * N, SIMT_ROWS)),
                 dim3(256), SIMT_SMEM, s, (const __nv_bfloat16 *)Q, (const __nv_bfloat16 *)K,
                 (const __nv_bfloat16 *)V, mask, prefix_len, n_nodes, N, Hq, Hkv, Lcap, scale,

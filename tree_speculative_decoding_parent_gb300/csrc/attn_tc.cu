@@ -571,16 +571,9 @@ int cluster_of(int g, int N) { return ceil_div(g * N, 128); }
 int loaders_of(int C) { return C >= 4 ? 4 : (C >= 2 ? 2 : 1); }
 
 bool set_attributes() {
-  static bool done = false;
-  if (done) return true;
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)TC_SMEM);
-  if (e != cudaSuccess) {
-    launch_status(e, "cudaFuncSetAttribute(attn_tc_kernel)");
-    return false;
-  }
-  done = true;
-  return true;
+  static SmemAttr attr;
+  return ensure_smem(attn_tc_kernel, (int)TC_SMEM, attr, "cudaFuncSetAttribute(attn_tc_kernel)") ==
+         GT_OK;
 }
 
 }  // namespace

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "gt.h"
 
 #define GT_API extern "C" __attribute__((visibility("default")))
@@ -37,6 +39,30 @@ static inline int launch_status(cudaError_t e, const char *what = "kernel launch
     note_error(what, e);
     (void)cudaGetLastError();  // clear a non-sticky launch error
     return GT_ERR_CUDA;
+  }
+  return GT_OK;
+}
+
+// Raises a kernel's dynamic shared-memory limit to at least `bytes` on the current device.
+// The runtime keeps the attribute per device, so each call site remembers, per device, the
+// largest limit it has set (a static SmemAttr); repeated calls then cost no driver call.
+struct SmemAttr {
+  std::atomic<int> bytes[64];  // zero-initialised when declared static
+};
+template <typename Kernel>
+static inline int ensure_smem(Kernel kernel, int bytes, SmemAttr &a, const char *what) {
+  int dev = 0;
+  const cudaError_t ge = cudaGetDevice(&dev);
+  if (ge != cudaSuccess) return launch_status(ge, "cudaGetDevice");
+  const bool cached = dev >= 0 && dev < 64;
+  if (cached && a.bytes[dev].load(std::memory_order_relaxed) >= bytes) return GT_OK;
+  const cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return launch_status(e, what);
+  if (cached) {
+    int cur = a.bytes[dev].load(std::memory_order_relaxed);
+    while (cur < bytes && !a.bytes[dev].compare_exchange_weak(cur, bytes)) {
+    }
   }
   return GT_OK;
 }

@@ -90,14 +90,10 @@ GT_API int gt_kv_commit(void *K, void *V, const int32_t *kv_src, const int32_t *
   if (!K || !V || !kv_src || !kv_dst || !acc_len) return GT_ERR_ARG;
   if (((uintptr_t)K | (uintptr_t)V) & 15) return GT_ERR_ARG;
   const size_t smem = (size_t)N * row_bytes;
-  static bool attr = false;
-  if (!attr) {  // up to 64 KB of staged rows
-    const cudaError_t e = cudaFuncSetAttribute(
-        kv_commit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        (int)((size_t)KVC_MAX_N * KVC_MAX_ROW));
-    if (e != cudaSuccess) return launch_status(e, "cudaFuncSetAttribute(kv_commit_kernel)");
-    attr = true;
-  }
+  static SmemAttr attr;  // up to 64 KB of staged rows
+  const int rc = ensure_smem(kv_commit_kernel, (int)((size_t)KVC_MAX_N * KVC_MAX_ROW), attr,
+                             "cudaFuncSetAttribute(kv_commit_kernel)");
+  if (rc != GT_OK) return rc;
   return launch(kv_commit_kernel, dim3(Hkv, B), dim3(KVC_THREADS), smem, (cudaStream_t)stream,
                 (uint8_t *)K, (uint8_t *)V, kv_src, kv_dst, acc_len, N, Hkv, Lcap,
                 (int)row_bytes, err);

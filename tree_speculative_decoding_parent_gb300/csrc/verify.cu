@@ -670,9 +670,9 @@ GT_API int gt_succ_update(int32_t *table, int V, int k, const int32_t *tokens,
   if (!table || !tokens || !topk_id || !n_nodes) return GT_ERR_ARG;
   const size_t smem = sizeof(int) * (size_t)total;
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(update_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return launch_status(e);
+    static SmemAttr attr;
+    const int rc = ensure_smem(update_kernel, (int)smem, attr, "cudaFuncSetAttribute(update_kernel)");
+    if (rc != GT_OK) return rc;
   }
   const int blocks = (int)((total + 255) / 256);
   return launch(update_kernel, dim3(blocks), dim3(256), smem, (cudaStream_t)stream, table, V, k,
@@ -696,9 +696,10 @@ static int walk_update_launch(const int32_t *tokens, const int32_t *parent,
     hs = 0;
   smem += 2 * sizeof(int) * (size_t)hs;
   if (smem > 48 * 1024) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        walk_update_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return launch_status(e, "cudaFuncSetAttribute(walk_update_kernel)");
+    static SmemAttr attr;
+    const int rc = ensure_smem(walk_update_kernel, (int)smem, attr,
+                               "cudaFuncSetAttribute(walk_update_kernel)");
+    if (rc != GT_OK) return rc;
   }
   return launch(walk_update_kernel, dim3(B), dim3(threads), smem, s, tokens, parent, n_nodes,
                 prefix_len, B, N, k, topk_id, sample, acc_len, path, out_tok, kv_src, kv_dst,
