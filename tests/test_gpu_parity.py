@@ -381,7 +381,8 @@ def test_kv_commit_random_paths_and_bad_requests(dtype):
 def test_tree_attn_edge_shapes(dtype):
     """Random trees through gt_tree_attn alone, masks from the oracle: a full 64-node mask
     word, single-node trees, zero prefixes, prefixes on and next to 128-key tile edges,
-    and 8 query heads per KV head (512 query rows of one KV head)."""
+    8 query heads per KV head (512 query rows of one KV head), and more segments than one
+    wave of clusters (both schedule paths)."""
     from workload import f32_to_bf16_bits
     rng = np.random.default_rng(21)
     cases = [  # B, N, Hq, Hkv, prefixes, nodes per request (None: N)
@@ -389,6 +390,10 @@ def test_tree_attn_edge_shapes(dtype):
         (2, 1, 32, 8, [0, 5], None),
         (3, 64, 16, 2, [127, 128, 129], [64, 33, 1]),
         (2, 40, 4, 4, [1000, 255], [40, 17]),
+        # 160 segments: the block-wide schedule
+        (20, 9, 16, 8, rng.integers(0, 700, size=20).tolist(), rng.integers(1, 10, size=20).tolist()),
+        # 96 segments over 38 clusters of 4 CTAs: the one-warp schedule in several waves
+        (12, 49, 64, 8, rng.integers(0, 900, size=12).tolist(), rng.integers(1, 50, size=12).tolist()),
     ]
     for B, N, Hq, Hkv, P, nn in cases:
         d = 128

@@ -61,11 +61,12 @@ attn_simt_kernel(const T *__restrict__ Q, const T *__restrict__ K, const T *__re
   __shared__ uint64_t s_mask[SIMT_ROWS];
 
   const int p = blockIdx.x;
-  const int4 pc = schedule_piece(sa, p, ws, err);
+  int2 np;
+  const int4 pc = schedule_piece(sa, p, ws, err, &np);
   if (pc.x < 0) return;
   const int seg = pc.x, b = seg / Hkv, h = seg - b * Hkv;
   const int g = Hq / Hkv;
-  const int n = n_nodes[b], P = prefix_len[b], keys = P + n;
+  const int n = np.x, P = np.y, keys = P + n;  // from the schedule: no second load
   const int r0 = blockIdx.y * SIMT_ROWS;
   if (r0 >= g * n) return;
   const int tid = threadIdx.x;

@@ -66,11 +66,12 @@ struct SchedArgs {
 // of non-empty segments, tau is raised to the smallest value whose pieces all fit in one
 // wave of G (sum_s cnt_s <= G), so that no piece waits for a second wave. Returns piece p
 // as (segment, tile_begin,
-// tile_end, 0), or segment -1 when p is past the last piece. The CTA at blockIdx (0,0)
+// tile_end, 0), or segment -1 when p is past the last piece, and (when np_out is given)
+// the node count and prefix length of the piece's request. The CTA at blockIdx (0,0)
 // also publishes (first piece, count) of every segment and the piece total into `ws`, and
 // reports invalid requests. Every thread of the CTA must call it (it synchronises).
 __device__ __forceinline__ int4 schedule_piece(const SchedArgs &a, int p, AttnWs ws,
-                                               int32_t *err) {
+                                               int32_t *err, int2 *np_out = nullptr) {
   constexpr int CH = 4;  // segments per thread kept in registers; more are recomputed
   __shared__ long long s_red[2][32];
   __shared__ int s_scan[32];
@@ -87,37 +88,42 @@ __device__ __forceinline__ int4 schedule_piece(const SchedArgs &a, int p, AttnWs
     if (!ok && publisher && (s % a.Hkv) == 0 && err) atomicCAS(err, 0, GT_ERR_RANGE);
     return ok ? (P + n + a.TK - 1) / a.TK : 0;
   };
+  __shared__ int2 s_np;  // (n, P) of the piece's request
   if (S <= 32 * CH) {
-    // few segments: warp 0 computes the whole schedule with shuffles (lane l holds segments
-    // l, l + 32, ...), the same tau and pieces as the block version below, and the CTA
-    // meets it at one barrier
+    // few segments: warp 0 computes the whole schedule with 32-bit shuffles and reductions
+    // (lane l holds segments l, l + 32, ...), the same tau and pieces as the block version
+    // below, and the CTA meets it at one barrier
     if (warp == 0) {
       if (lane == 0) s_piece = make_int4(-1, 0, 0, 0);
       __syncwarp();
-      int wt[CH];
-      long long local = 0;
+      int wt[CH], wn[CH], wP[CH], tsum = 0, nsum = 0;
 #pragma unroll
       for (int i = 0; i < CH; ++i) {
         const int s = lane + 32 * i;
-        wt[i] = s < S ? tiles_of(s) : 0;
-        local += wt[i] + ((long long)(wt[i] > 0) << 44);
+        wt[i] = wn[i] = wP[i] = 0;
+        if (s < S) {
+          const int b = s / a.Hkv;
+          const int n = a.n_nodes[b], P = a.prefix_len[b];
+          const bool ok = n >= 1 && n <= a.N && P >= 0 && (long long)P + n <= (long long)a.Lcap;
+          if (!ok && publisher && (s % a.Hkv) == 0 && err) atomicCAS(err, 0, GT_ERR_RANGE);
+          wt[i] = ok ? (P + n + a.TK - 1) / a.TK : 0;
+          wn[i] = n;
+          wP[i] = P;
+        }
+        tsum += wt[i];
+        nsum += wt[i] > 0;
       }
-      auto warp_sum = [&](long long v) {
-#pragma unroll
-        for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        return v;
-      };
-      const long long both = warp_sum(local);
-      const long long T = both & ((1ll << 44) - 1), Sn = both >> 44;
-      int tau = (int)max(1ll, (T + a.G - 1) / a.G);
+      const int T = (int)__reduce_add_sync(0xffffffffu, (unsigned)tsum);
+      const int Sn = (int)__reduce_add_sync(0xffffffffu, (unsigned)nsum);
+      int tau = max(1, (T + a.G - 1) / a.G);
       if (Sn > 0 && a.G > Sn) {
-        int lo = tau, hi = (int)max((long long)tau, (T + (a.G - Sn) - 1) / (a.G - Sn));
+        int lo = tau, hi = max(tau, (T + (a.G - Sn) - 1) / (a.G - Sn));
         while (lo < hi) {
           const int mid = lo + (hi - lo) / 2;
-          long long c = 0;
+          int c = 0;
 #pragma unroll
           for (int i = 0; i < CH; ++i) c += (wt[i] + mid - 1) / mid;
-          if (warp_sum(c) <= a.G)
+          if ((int)__reduce_add_sync(0xffffffffu, (unsigned)c) <= a.G)
             hi = mid;
           else
             lo = mid + 1;
@@ -140,9 +146,10 @@ __device__ __forceinline__ int4 schedule_piece(const SchedArgs &a, int p, AttnWs
         if (s < S) {
           if (publisher) ws.seg[s] = make_int2(off, cnt);
           if (p >= off && p < off + cnt) {
-            const int j = p - off, t = wt[i];
-            s_piece = make_int4(s, (int)((long long)t * j / cnt),
-                                (int)((long long)t * (j + 1) / cnt), 0);
+            // floor(t * j / cnt) = (t / cnt) * j + floor((t % cnt) * j / cnt), in 32 bits
+            const int j = p - off, t = wt[i], q = t / cnt, r = t - q * cnt;
+            s_piece = make_int4(s, q * j + r * j / cnt, q * (j + 1) + r * (j + 1) / cnt, 0);
+            s_np = make_int2(wn[i], wP[i]);
           }
         }
         base += __shfl_sync(0xffffffffu, incl, 31);
@@ -150,6 +157,7 @@ __device__ __forceinline__ int4 schedule_piece(const SchedArgs &a, int p, AttnWs
       if (publisher && lane == 0) ws.hdr[0] = base;
     }
     __syncthreads();
+    if (np_out) *np_out = s_np;
     return s_piece;
   }
   int tl[CH];  // tiles of this thread's first CH segments
@@ -226,11 +234,14 @@ __device__ __forceinline__ int4 schedule_piece(const SchedArgs &a, int p, AttnWs
     if (p >= off && p < off + cnt) {
       const int j = p - off;
       s_piece = make_int4(s, (int)((long long)t * j / cnt), (int)((long long)t * (j + 1) / cnt), 0);
+      const int b = s / a.Hkv;
+      s_np = make_int2(a.n_nodes[b], a.prefix_len[b]);
     }
     off += cnt;
   }
   if (publisher && tid == 0) ws.hdr[0] = total;
   __syncthreads();
+  if (np_out) *np_out = s_np;
   return s_piece;
 }
 #endif

@@ -197,14 +197,15 @@ attn_tc_kernel(const __nv_bfloat16 *__restrict__ Qg, const __grid_constant__ CUt
   pdl_enter();
   // every CTA of a cluster gets the same piece, so a cluster leaves here as a whole
   const int p = blockIdx.x / C;
-  const int4 pc = schedule_piece(sa, p, ws, err);
+  int2 np;
+  const int4 pc = schedule_piece(sa, p, ws, err, &np);
   if (pc.x < 0) {
     if (warp == 5) tc::tmem_dealloc(tmem, TMEM_COLS);
     return;
   }
   const int seg = pc.x, b = seg / Hkv, h = seg - b * Hkv;
   const int g = Hq / Hkv;
-  const int n = n_nodes[b], P = prefix_len[b], keys = P + n;
+  const int n = np.x, P = np.y, keys = P + n;  // from the schedule: no second load
   const int row0 = rank * 128;  // first segment row of this CTA (may lie past g*n)
   const int t0 = pc.y, nt = pc.z - pc.y;
   const int total = 2 * nt;
