@@ -408,6 +408,14 @@ const char *gt_status_string(int status);
  * pointer stays valid until the next libgt call on this thread. */
 const char *gt_last_error(void);
 
+/* Self-test of the bounded waits (no counterpart in the pages). One CTA waits on an
+ * mbarrier that nothing arrives on, through the same bounded-wait helper the tcgen05 kernels
+ * use, with a limit of limit_ns (1 ns .. 1 s); it sets GT_ERR_TIMEOUT in *err and, when
+ * waited_ns (device, nullable) is given, stores the time it waited. The GPU context stays
+ * usable afterwards. Host errors: GT_ERR_ARG (limit out of range, err NULL). */
+int gt_selftest_wait_timeout(int64_t limit_ns, int32_t *err, int64_t *waited_ns,
+                             gt_stream_t stream);
+
 /* Records `event` (a cudaEvent_t) on `stream` as an externally visible node when the
  * stream is being captured into a CUDA graph (cudaEventRecordExternal), so a replayed
  * graph can time the work between two such records. Not part of the step. */

@@ -93,3 +93,10 @@ def test_sampling_and_drafting_calls_validate_arguments_without_gpu(lib):
     assert so.gt_tree_attach(P, P, P, P, 1, 256, P, P, 10, P, P, 10, 0, P, P, None) == ARG
     # KV commit: rows must be whole 16-byte chunks
     assert so.gt_kv_commit(P, P, P, P, P, 1, 8, 8, 100, 1000, lib.GT_BF16, P, None) == SHAPE
+
+
+def test_wait_selftest_rejects_bad_limits_without_gpu(lib):
+    so = lib.load()
+    for ns in (0, -5, 2_000_000_000):
+        assert so.gt_selftest_wait_timeout(ns, 4096, None, None) == lib.GT_ERR_ARG
+    assert so.gt_selftest_wait_timeout(1000, None, None, None) == lib.GT_ERR_ARG

@@ -53,15 +53,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 // Waits for the phase of parity `parity` to complete. Returns false if the CTA was
-// aborted (by this wait timing out or by another role).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+// aborted (by this wait timing out after limit_ns, or by another role).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                          uint64_t limit_ns = GT_WAIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0u) {
       if (*abort) return false;
-      if (globaltimer() - t0 > GT_WAIT_NS) {
+      if (globaltimer() - t0 > limit_ns) {
         *abort = 1;
         return false;
       }

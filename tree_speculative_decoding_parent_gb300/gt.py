@@ -50,6 +50,7 @@ _SIGS = {
                             _vp, _vp, _vp, _vp, _vp]),
     "gt_tree_attach": (_i, [_vp, _vp, _vp, _vp, _i, _i, _vp, _vp, _i, _vp, _vp, _i, _i, _vp, _vp,
                             _vp]),
+    "gt_selftest_wait_timeout": (_i, [ctypes.c_int64, _vp, _vp, _vp]),
     "gt_stage_budget": (_i, [_i, _i, _vp, _vp]),
     "gt_default_template": (_i, [_i, _i, _i, _vp, _vp]),
     "gt_status_string": (ctypes.c_char_p, [_i]),
@@ -247,6 +248,11 @@ def gt_tree_attach(parent, tokens, score, n_nodes, B, Nmax, frontier, n_frontier
     _check("gt_tree_attach", load().gt_tree_attach(
         _p(parent), _p(tokens), _p(score), _p(n_nodes), B, Nmax, _p(frontier), _p(n_frontier), W,
         _p(child_id), _p(child_p), m, V, _p(first_new), _p(err), _s(stream)))
+
+
+def gt_selftest_wait_timeout(limit_ns, err, waited_ns=None, stream=None):
+    _check("gt_selftest_wait_timeout", load().gt_selftest_wait_timeout(
+        int(limit_ns), _p(err), _p(waited_ns), _s(stream)))
 
 
 def gt_stage_budget(stage: int, slots: int = 60):
