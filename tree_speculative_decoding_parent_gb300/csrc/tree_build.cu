@@ -55,11 +55,19 @@ tree_build_kernel(const float *__restrict__ score, const int32_t *__restrict__ p
 
   // ---------------------------------------------------------------- phase A: prune
   int code = (n < 1 || n > Nin) ? GT_ERR_RANGE : 0;
-  int p = -1;
+  int p = -1, tok = -1;
   float s = 0.f;
+  // every global read of the prune and of the graft set-up is issued here, before the
+  // first barrier, so that none of them waits for a phase before it
+  const float th = thresh ? thresh[b] : -INFINITY;
+  const int anchor_b = anchor ? anchor[b] : 0;
+  const int R_b = R[b];
+  const int tpar_t = t < T ? tpar[t] : -1;
+  const int trank_t = t < T ? trank[t] : 0;
   if (!code && t < n) {
     p = parent_in[in0 + t];
     s = score[in0 + t];
+    tok = tokens_in[in0 + t];
     s_score[t] = s;
   }
   __syncthreads();
@@ -92,7 +100,6 @@ tree_build_kernel(const float *__restrict__ score, const int32_t *__restrict__ p
     }
     return;
   }
-  const float th = thresh ? thresh[b] : -INFINITY;
   // the root is always kept; the other nodes compete for the remaining ke - 1 slots
   const bool cand = t > 0 && t < n && s >= th;
   const bool sel = topk_keys_keep(cand ? order_key(s) : 0u, ke - 1, s_hist, s_sel, warp_tot);
@@ -103,7 +110,7 @@ tree_build_kernel(const float *__restrict__ score, const int32_t *__restrict__ p
   __syncthreads();
   if (kept) {
     s_par[newi] = (t == 0) ? -1 : s_new[p];
-    s_tok[newi] = tokens_in[in0 + t];
+    s_tok[newi] = tok;
     if (out_score) out_score[row0 + newi] = s;
     if (out_old) out_old[row0 + newi] = t;
   }
@@ -118,7 +125,7 @@ tree_build_kernel(const float *__restrict__ score, const int32_t *__restrict__ p
   int a = 0;
   code = 0;
   if (anchor) {
-    a = anchor[b] == -1 ? nk - 1 : anchor[b];
+    a = anchor_b == -1 ? nk - 1 : anchor_b;
     if (a < 0 || a >= nk) {
       code = GT_ERR_RANGE;
       a = 0;
@@ -126,12 +133,12 @@ tree_build_kernel(const float *__restrict__ score, const int32_t *__restrict__ p
   }
   const int root_tok = s_tok[a];
   if (!code && (root_tok < 0 || root_tok >= V)) code = GT_ERR_TREE;
-  const int r = code ? 0 : max(0, min(min(R[b], N - nk), T));
+  const int r = code ? 0 : max(0, min(min(R_b, N - nk), T));
   const bool active = t < r;
   int tp = -1, rk = 0;
   if (active) {
-    tp = tpar[t];
-    rk = trank[t];
+    tp = tpar_t;
+    rk = trank_t;
     if (tp < -1 || tp >= t || rk < 0 || rk >= k) code = GT_ERR_TREE;
     s_tpar[t] = tp;
   }
