@@ -516,6 +516,17 @@ walk_update_kernel(const int32_t *__restrict__ tokens, const int32_t *__restrict
   const int b = blockIdx.x, v = threadIdx.x;
   const int total = B * N;
   const size_t row0 = (size_t)b * N;
+  // node v's own reads are in bounds for any v < N: they are issued together with the
+  // node count, not after it, and the node's top-k row waits in registers for the table
+  int p_v = -1, tok_v = -1, am_v = -1;
+  int krow[16];
+  if (v < N) {
+    p_v = parent[row0 + v];
+    tok_v = tokens[row0 + v];
+    am_v = sample ? sample[row0 + v] : topk_id[(row0 + v) * k];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) krow[c] = c < k ? topk_id[(row0 + v) * k + c] : -1;
+  }
   const int n = n_nodes[b], P = prefix_len[b];
   if (v == 0) s_bad = 0;
   for (int i = v; i < total; i += blockDim.x) {
@@ -535,10 +546,10 @@ walk_update_kernel(const int32_t *__restrict__ tokens, const int32_t *__restrict
   }
   int code = (n < 1 || n > N) ? GT_ERR_RANGE : 0;
   if (!code && v < n) {
-    const int p = parent[row0 + v];
+    const int p = p_v;
     s_par[v] = p;
-    s_tok[v] = tokens[row0 + v];
-    s_am[v] = sample ? sample[row0 + v] : topk_id[(row0 + v) * k];
+    s_tok[v] = tok_v;
+    s_am[v] = am_v;
     if (v == 0 ? (p != -1) : (p < 0 || p >= v)) code = GT_ERR_TREE;
   }
   __syncthreads();
@@ -621,9 +632,15 @@ walk_update_kernel(const int32_t *__restrict__ tokens, const int32_t *__restrict
         }
     }
     if (!last) continue;
-    const int32_t *src = topk_id + (size_t)i * k;
     int32_t *dst = table + (size_t)t * k;
-    for (int c = 0; c < k; ++c) dst[c] = src[c];
+    if (vv == v) {  // the launch gives every node its own thread (blockDim >= N)
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        if (c < k) dst[c] = krow[c];
+    } else {
+      const int32_t *src = topk_id + (size_t)i * k;
+      for (int c = 0; c < k; ++c) dst[c] = src[c];
+    }
   }
 }
 
