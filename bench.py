@@ -404,7 +404,11 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
             inp["V"][b, :, P[b]:P[b] + scn.N].copy_(h_kv[b][1], non_blocking=True)
         side.wait_stream(main)
         with torch.cuda.stream(side):
-            inp["logits"].copy_(h_logits, non_blocking=True)
+            # in copies of at most 32 MB: one large copy replays slower from a graph
+            dl, hl = inp["logits"].view(-1), h_logits.view(-1)
+            step = 8 << 20  # floats
+            for o in range(0, dl.numel(), step):
+                dl[o:o + step].copy_(hl[o:o + step], non_blocking=True)
             logits_in.record(side)
         run_tree_build(buf, inp, main)
         run_attn(buf, inp, main, scn.scale)
