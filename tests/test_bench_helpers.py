@@ -1,0 +1,37 @@
+"""The bench's byte and FLOP accounting and its roofline bound, checked by hand counts."""
+import json
+import os
+
+import bench
+from workload import make_scenario
+
+
+def test_attention_bytes_and_flops_by_hand():
+    scn = make_scenario(3, V=1000, stream_len=5000)  # B=1, Hq=32, Hkv=8, d=128, N=60, bf16
+    P = int(scn.prefix_len[0])
+    kv = (P + 60) * 8 * 128 * 2 * 2          # K and V rows of every KV head, bf16
+    qo = 2 * 1 * 60 * 32 * 128 * 2           # Q read and O written
+    assert bench.attn_bytes(scn) == kv + qo
+    assert bench.attn_flops(scn) == 4 * 4 * 60 * (P + 60) * 128 * 8   # 4 g N (P+n) d per head
+    scn4 = make_scenario(4, V=1000, P=(100, 900), B=3, stream_len=5000)
+    keys = sum(int(p) + 60 for p in scn4.prefix_len)
+    assert bench.attn_bytes(scn4) == keys * 8 * 128 * 2 * 2 + 2 * 3 * 60 * 64 * 128 * 2
+
+
+def test_roofline_bound_follows_the_measured_ridge():
+    hbm, _ = bench._peaks()
+    tpeak, _ = bench._tensor_peak()
+    ridge = tpeak * 1e12 / (hbm * 1e9)
+    peaks = os.path.join(bench.ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(peaks):  # written per machine; the fallback figures apply otherwise
+        with open(peaks) as f:
+            assert json.load(f)["hbm_gbs"] == hbm
+    # workload 3 sits below the ridge (HBM-bound), workloads 4 and 5 above it (tensor-bound)
+    for cid, tensor in ((3, False), (4, True), (5, True)):
+        scn = make_scenario(cid, V=1000, stream_len=5000)
+        assert (bench.attn_flops(scn) / bench.attn_bytes(scn) > ridge) == tensor, cid
+
+
+def test_throughput_counts_every_rank():
+    assert bench.job_throughput(1, 200, 0.5) == 400.0
+    assert bench.job_throughput(4, 200, 0.5) == 1600.0
