@@ -32,7 +32,7 @@ KERNELS_PER_STEP = 5  # tree build, attention + combine, top-k, walk + table upd
 L2_BYTES = 129 * 2 ** 20
 # Event record nodes end the programmatic overlap of the calls around them, so the timed
 # graph brackets the attention call with events in one step out of ATTN_EVENT_EVERY only.
-ATTN_EVENT_EVERY = 4
+ATTN_EVENT_EVERY = 8  # one step in 8 has its attention call bracketed by events
 
 
 def _peaks():
