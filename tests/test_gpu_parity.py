@@ -440,3 +440,60 @@ def test_tree_attn_edge_shapes(dtype):
             e = float(np.abs(got[b, :n[b]] - ref).max())
             assert e <= TOL[dtype], (B, N, Hq, Hkv, b, e)
             assert np.all(got[b, n[b]:] == 0.0)
+
+
+def test_tree_attn_two_cta_cluster_shapes():
+    """bf16 shapes with 129..256 query rows per KV head (two-CTA clusters sharing every
+    K/V tile by multicast): prefixes on and next to tile edges, a one-node tree whose
+    second CTA has no rows, zero prefixes (the tail tile is the only tile), a single
+    segment cut into one-tile pieces, and more segments than one wave (long pieces that
+    wrap the ring). Cache rows past each request hold NaN."""
+    from workload import f32_to_bf16_bits
+    rng = np.random.default_rng(33)
+    cases = [  # B, N, Hq, Hkv, prefixes, nodes per request (None: N)
+        (3, 60, 32, 8, [127, 128, 129], [60, 33, 1]),
+        (2, 64, 8, 2, [0, 3], None),
+        (1, 17, 8, 1, [4000], None),
+        (16, 40, 16, 4, rng.integers(1000, 5000, size=16).tolist(),
+         rng.integers(1, 41, size=16).tolist()),
+        (24, 33, 32, 8, rng.integers(0, 3500, size=24).tolist(),
+         rng.integers(1, 34, size=24).tolist()),
+    ]
+    for B, N, Hq, Hkv, P, nn in cases:
+        assert 128 < (Hq // Hkv) * N <= 256
+        d = 128
+        n = np.array(nn if nn else [N] * B, np.int32)
+        P = np.array(P, np.int32)
+        Lcap = int((P + N).max() + 64) // 64 * 64
+        parent = np.full((B, N), -1, np.int32)
+        for b in range(B):
+            parent[b, 1:n[b]] = [rng.integers(0, v) for v in range(1, n[b])]
+        mask = np.zeros((B, N, 1), np.uint64)
+        for b in range(B):
+            _, _, mask[b] = oracle.tree_mask(parent[b], int(n[b]), int(P[b]), N)
+        Q = rng.standard_normal((B, N, Hq, d), dtype=np.float32)
+        K = rng.standard_normal((B, Hkv, Lcap, d), dtype=np.float32)
+        Vv = rng.standard_normal((B, Hkv, Lcap, d), dtype=np.float32)
+        for b in range(B):
+            K[b, :, P[b] + n[b]:] = np.nan
+            Vv[b, :, P[b] + n[b]:] = np.nan
+        hq, hk, hv = (f32_to_bf16_bits(x) for x in (Q, K, Vv))
+        dev = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).cuda() for x in (hq, hk, hv)]
+        O = torch.empty((B, N, Hq, d), dtype=torch.bfloat16, device="cuda")
+        wsb = gt.gt_tree_attn_workspace(B, N, Hq, Hkv, d, Lcap)
+        ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        scale = 1.0 / np.sqrt(d)
+        gt.gt_tree_attn(dev[0], dev[1], dev[2], _t(mask), _t(P), _t(n), B, N, Hq, Hkv, d, Lcap,
+                        gt.GT_BF16, scale, O, ws, wsb, err)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        got = O.float().cpu().numpy().astype(np.float64)
+        for b in range(B):
+            L = int(P[b] + n[b])
+            ref = oracle.tree_attn(oracle.bf16_to_f64(hq[b]), oracle.bf16_to_f64(hk[b][:, :L]),
+                                   oracle.bf16_to_f64(hv[b][:, :L]), parent[b], int(n[b]),
+                                   int(P[b]), scale)
+            e = float(np.abs(got[b, :n[b]] - ref).max())
+            assert e <= TOL["bf16"], (B, N, Hq, Hkv, b, e)
+            assert np.all(got[b, n[b]:] == 0.0)

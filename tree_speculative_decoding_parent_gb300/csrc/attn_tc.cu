@@ -16,11 +16,15 @@
 //   warp 4      TMA producer: the K/V items in consumption order, through a ring of 7
 //               slots of 32 KB: K(0), K(1), K(2), V(0), K(3), V(1), ... (K runs two tiles
 //               ahead of V). A slot is refilled once the MMA threads of all C CTAs released
-//               its previous item (multicast tcgen05.commit).
-//   warp 5      MMA issuer (one thread) and tensor-memory owner. S(t) = Q K(t)^T goes to one
-//               of two S buffers (Q from tensor memory, K from shared memory); S(j+2) is
-//               issued as soon as the softmax has read S(j) into registers, so Q K^T stays
-//               two tiles ahead. O += P(j) V(j) as soon as the softmax published P(j).
+//               its previous item (multicast tcgen05.commit). Past the first three items
+//               the producer waits until this CTA's softmax threads hold their Q rows and
+//               ancestor masks, so that those small loads are not queued behind the ring's
+//               burst of loads at the start.
+//   warp 5      MMA issuer (one thread) and tensor-memory owner.
+//               S(t) = Q K(t)^T goes to one of two S buffers (Q from tensor memory, K from
+//               shared memory); S(j+2) is issued as soon as the softmax has read S(j) into
+//               registers, so Q K^T stays two tiles ahead. O += P(j) V(j) as soon as the
+//               softmax published P(j).
 //   warps 0-3   softmax: thread = query row = tensor-memory lane. First the thread copies
 //               its Q row into tensor memory. Per tile: read the S row (and free its
 //               buffer), mask, p = 2^(s*scale*log2e - m) with a lazily moved reference max
@@ -50,11 +54,9 @@ namespace {
 
 constexpr int TC_THREADS = 192;     // 4 softmax warps + producer + MMA
 constexpr int TK = ATTN_TC_KEYS;    // keys per tile (128)
-constexpr int SLOTS = 7;            // ring slots, each one K or one V tile
 constexpr int NSBUF = 2;            // S buffers in tensor memory
 constexpr int KLEAD = 2;            // K tiles loaded ahead of V (= NSBUF)
 constexpr int HALF_BYTES = 16384;   // 128 rows x 64 d x bf16 (one 128B-swizzled box)
-constexpr int SLOT_BYTES = 2 * HALF_BYTES;  // one tile: 128 keys x 128 d
 constexpr int MAX_CLUSTER = 4;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t O_COL = 256;
@@ -62,19 +64,26 @@ constexpr uint32_t Q_COL = 384;
 constexpr uint32_t P_COL = 448;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
+constexpr int STAGE_PITCH = ATTN_D * 4 + 16;  // bytes per staged partial row
 static_assert(TK == 128, "the tile shape above assumes 128-key tiles");
 static_assert(KLEAD == NSBUF, "S(t + NSBUF) reuses the buffer of P(t)");
 
+// Ring and barriers of one CTA; a slot holds one whole K or V tile.
 struct Smem {
+  static constexpr int SLOTS = 7;
+  static constexpr int SLOT_BYTES = 2 * HALF_BYTES;
   // offsets from the 1024-aligned base
-  static constexpr int RING = 0;                       // [SLOTS] x 32 KB
+  static constexpr int RING = 0;
   static constexpr int BAR = RING + SLOTS * SLOT_BYTES;
-  static constexpr int NBAR = 1 + 2 * SLOTS + 2 * NSBUF + 1 + 1 + 1 + 1;
+  // q_full, full[SLOTS], empty[SLOTS], s_full[NSBUF], s_free[NSBUF], p_full, o_ready,
+  // o_done, drain
+  static constexpr int NBAR = 1 + 2 * SLOTS + 2 * NSBUF + 4;
   static constexpr int END = BAR + NBAR * 8;
+  static constexpr size_t BYTES = END + 1024;  // + alignment slack
+  static_assert(BYTES + 768 <= 232448, "shared memory of one CTA (dynamic + static)");
+  static_assert(128 * STAGE_PITCH <= SLOTS * SLOT_BYTES, "partial rows are staged in the ring");
 };
-constexpr size_t TC_SMEM = Smem::END + 1024;  // + alignment slack
-static_assert(TC_SMEM + 768 <= 232448, "shared memory of one CTA (dynamic + static)");
-static_assert(128 * (ATTN_D * 4 + 16) <= SLOTS * SLOT_BYTES, "partial rows are staged in the ring");
+constexpr int RING_GATE = 3;  // ring items issued before the producer waits for q_full
 
 struct Bars {
   uint64_t *q_full, *full, *empty, *s_full, *s_free, *p_full, *o_ready, *o_done, *drain;
@@ -85,8 +94,8 @@ __device__ __forceinline__ Bars bars_at(uint8_t *base) {
   Bars r;
   r.q_full = b;
   r.full = b + 1;
-  r.empty = r.full + SLOTS;
-  r.s_full = r.empty + SLOTS;
+  r.empty = r.full + Smem::SLOTS;
+  r.s_full = r.empty + Smem::SLOTS;
   r.s_free = r.s_full + NSBUF;
   r.p_full = r.s_free + NSBUF;
   r.o_ready = r.p_full + 1;
@@ -98,7 +107,7 @@ __device__ __forceinline__ Bars bars_at(uint8_t *base) {
 // Item sequence of a piece of nt tiles, the order in which the MMA thread consumes them:
 // K(0..P0-1) with P0 = min(KLEAD, nt), then for j = 0..nt-1: K(j+KLEAD) while
 // j+KLEAD < nt, followed by V(j). Item q sits in slot q % SLOTS as that slot's use number
-// q / SLOTS.
+// q / SLOTS. The last item is V(nt-1).
 __device__ __forceinline__ int pos_v(int j, int nt) {
   const int p0 = min(KLEAD, nt), e = max(0, nt - KLEAD);
   return p0 + j + min(j + 1, e);
@@ -123,8 +132,6 @@ __device__ __forceinline__ void item_at(int q, int nt, bool &is_v, int &tile) {
   is_v = true;
   tile = e + (r - 2 * e);
 }
-__device__ __forceinline__ int slot_of(int q) { return q % SLOTS; }
-__device__ __forceinline__ uint32_t use_parity(int q) { return (uint32_t)((q / SLOTS) & 1); }
 
 // AND of `pred` over the four softmax warps (128 threads), through named barrier 1.
 __device__ __forceinline__ int __syncthreads_and_named(bool pred) {
@@ -144,12 +151,177 @@ __device__ __forceinline__ bool drain_wait(uint64_t *bar, uint32_t parity) {
   return tc::mbar_wait(bar, parity, &never);
 }
 
+// ------------------------------------------------------------------ softmax pieces
+// Q row r = node * g + head-in-group of the segment (b, h) into tensor memory at tQ (this
+// warp's lanes), as 64 bf16 pairs (low half = even element), the tensor-memory layout of an
+// M-tile operand; rows past the tree are zero. Returns once the stores completed.
+__device__ __forceinline__ void q_row_to_tmem(const __nv_bfloat16 *__restrict__ Qg, int b, int N,
+                                              int Hq, int h, int g, int r, uint32_t tQ) {
+  const int node = r / g;
+  uint32_t qw[64];
+  if (node < N) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(
+        Qg + (((size_t)b * N + node) * Hq + (size_t)h * g + (r - node * g)) * ATTN_D);
+#pragma unroll
+    for (int v = 0; v < 16; ++v) {
+      const uint4 x = __ldg(src + v);
+      qw[4 * v] = x.x;
+      qw[4 * v + 1] = x.y;
+      qw[4 * v + 2] = x.z;
+      qw[4 * v + 3] = x.w;
+    }
+  } else {
+#pragma unroll
+    for (int v = 0; v < 64; ++v) qw[v] = 0u;
+  }
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t w[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) w[q] = qw[c * 16 + q];
+    tc::tmem_st16(tQ + c * 16, w);
+  }
+  tc::tmem_wait_st();
+}
+
+// Softmax of one tile for this thread's row: s holds the row's 128 raw scores of keys
+// kb .. kb+127 (masked in place), P the committed prefix length, keys = P + n, mrow the
+// row's ancestor mask over the tree keys. Produces the P words (bf16 pairs) in pk, the
+// factor alpha by which the running O and sum must be scaled, and updates the reference
+// max m_used (log2 units) and the row sum l. `later` is true for every tile after the
+// piece's first. Warp-collective (its votes keep the paths warp-uniform).
+//
+// p = 2^(s*scale*log2e - m_used) against a lazily moved reference max. A tile wholly inside
+// the committed prefix, once the row has a finite reference, goes straight to the
+// exponentials with the tile's sum as the overflow test: sum <= 2^15 = 128 * 2^8 means no p
+// exceeded the lazy-rescale bound 2^8, so the result is what a max pass first would give
+// (up to summation order). Otherwise (the first tile, a masked tile, or the rare growth of
+// the row's max by more than 8 in log2 units) a max pass moves the reference first. Both
+// cases run the same exponential loop, which keeps the code small.
+__device__ __forceinline__ void softmax_tile(uint32_t (&s)[4][32], int kb, int P, int keys,
+                                             uint64_t mrow, float sl2, bool later,
+                                             float &m_used, float &l, float &alpha,
+                                             uint32_t (&pk)[4][16]) {
+  alpha = 1.f;
+  if (kb + TK > P) {  // keys of the tree: the ancestor mask decides visibility
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int q = 0; q < 32; ++q) {
+        const int key = kb + c * 32 + q;
+        const bool vis = key < P || (key < keys && ((mrow >> (unsigned)(key - P)) & 1ull));
+        if (!vis) s[c][q] = __float_as_uint(-INFINITY);
+      }
+  }
+  bool need_max = __any_sync(0xffffffffu, !later || kb + TK > P || m_used == -INFINITY);
+  float lt;
+  for (int pass = 0;; ++pass) {
+    if (need_max) {
+      // 8 independent partial maxima of the raw scores keep the dependent chain short
+      float mxa[8];
+#pragma unroll
+      for (int a = 0; a < 8; ++a) mxa[a] = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int q = 0; q < 32; ++q) mxa[q & 7] = fmaxf(mxa[q & 7], __uint_as_float(s[c][q]));
+      const float mx = sl2 * fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
+                                   fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
+      // lazy rescale: move the reference max only when it grows by more than 8 (x256)
+      if (mx > m_used + 8.f) {
+        alpha = (m_used == -INFINITY) ? 0.f : tc::ex2_approx(m_used - mx);
+        m_used = mx;
+      }
+    }
+    // a row with no visible key so far has m = -inf and every s = -inf: its p are 0
+    const float msub = m_used == -INFINITY ? 0.f : m_used;
+    const uint64_t a2 = tc::f32x2_pack(sl2, sl2), c2 = tc::f32x2_pack(-msub, -msub);
+    uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        float p0, p1;
+        tc::ex2_fma_x2(__uint_as_float(s[c][2 * q]), __uint_as_float(s[c][2 * q + 1]), a2, c2,
+                       p0, p1);
+        tc::add_x2(acc[q & 3], p0, p1);
+        pk[c][q] = tc::pack_bf16x2(p0, p1);
+      }
+    lt = (tc::f32x2_sum(acc[0]) + tc::f32x2_sum(acc[1])) +
+         (tc::f32x2_sum(acc[2]) + tc::f32x2_sum(acc[3]));
+    // after a max pass every p <= 2^8 by construction; without one, the sum tests it
+    // (false for inf and NaN too)
+    if (need_max || pass > 0 || __all_sync(0xffffffffu, lt <= 32768.f)) break;
+    need_max = true;
+  }
+  l = l * alpha + lt;
+}
+
+// O row (tensor memory at tO, this warp's lanes) *= alpha.
+__device__ __forceinline__ void rescale_o(uint32_t tO, float alpha) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t o[32];
+    tc::tmem_ld32(tO + c * 32, o);
+    tc::tmem_wait_ld();
+    uint32_t w[16];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+#pragma unroll
+      for (int q = 0; q < 16; ++q) w[q] = __float_as_uint(__uint_as_float(o[half * 16 + q]) * alpha);
+      tc::tmem_st16(tO + c * 32 + half * 16, w);
+    }
+  }
+}
+
+// The normalised partial rows and their log-sum-exps. They leave through shared memory
+// (`stage`, idle once O is complete) so that every warp store covers a whole 512-byte row;
+// rows are staged at a 528-byte pitch, which keeps the threads' 16-byte writes free of bank
+// conflicts. ok: this thread's waits all succeeded. Called by the 128 softmax threads.
+__device__ __forceinline__ void write_partial(uint8_t *stage, uint32_t tO, bool ok, float l,
+                                              float m_used, int p, int row0, int rows,
+                                              const AttnWs &ws) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, rl = warp * 32 + lane;
+  const int r = row0 + rl;
+  const bool wok = __all_sync(0xffffffffu, ok);
+  if (wok) {
+    tc::tc_fence_after();
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    uint8_t *srow = stage + rl * STAGE_PITCH;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t o[32];
+      tc::tmem_ld32(tO + c * 32, o);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int q = 0; q < 32; q += 4)
+        *reinterpret_cast<float4 *>(srow + (c * 32 + q) * 4) =
+            make_float4(__uint_as_float(o[q]) * inv, __uint_as_float(o[q + 1]) * inv,
+                        __uint_as_float(o[q + 2]) * inv, __uint_as_float(o[q + 3]) * inv);
+    }
+    if (r < rows)
+      ws.lse[(size_t)p * ws.rows_pad + r] = l > 0.f ? (m_used + log2f(l)) * LN2 : -INFINITY;
+  }
+  // the four softmax warps meet (named barrier 1, 128 threads); each then writes 32 rows
+  const int wall = __syncthreads_and_named(wok);
+  if (wall) {
+    float *dst0 = ws.opart + ((size_t)p * ws.rows_pad + row0) * ATTN_D;
+    for (int rr = warp * 32; rr < warp * 32 + 32; ++rr) {
+      if (row0 + rr >= rows) break;  // rows past the tree are never read
+      const float4 v = *reinterpret_cast<const float4 *>(stage + rr * STAGE_PITCH + lane * 16);
+      *reinterpret_cast<float4 *>(dst0 + (size_t)rr * ATTN_D + lane * 4) = v;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(TC_THREADS, 1)
 attn_tc_kernel(const __nv_bfloat16 *__restrict__ Qg, const __grid_constant__ CUtensorMap mapK,
                const __grid_constant__ CUtensorMap mapV, const uint64_t *__restrict__ mask,
                const int32_t *__restrict__ prefix_len, const int32_t *__restrict__ n_nodes,
                int N, int Hq, int Hkv, float scale, int C, int L, SchedArgs sa, AttnWs ws,
                int32_t *err) {
+  using Lay = Smem;
+  constexpr int SLOTS = Lay::SLOTS, SLOT_BYTES = Lay::SLOT_BYTES;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint32_t tmem_sh;
   __shared__ int abort_sh;
@@ -209,6 +381,8 @@ attn_tc_kernel(const __nv_bfloat16 *__restrict__ Qg, const __grid_constant__ CUt
   const int row0 = rank * 128;  // first segment row of this CTA (may lie past g*n)
   const int t0 = pc.y, nt = pc.z - pc.y;
   const int total = 2 * nt;
+  auto slot_of = [](int q) { return q % SLOTS; };
+  auto use_parity = [](int q) { return (uint32_t)((q / SLOTS) & 1); };
 
   if (warp == 4) {
     if (lane == 0) {
@@ -220,6 +394,7 @@ attn_tc_kernel(const __nv_bfloat16 *__restrict__ Qg, const __grid_constant__ CUt
       const bool loader = rank < L;
       for (int q = 0; q < total; ++q) {
         const int s = slot_of(q);
+        if (q == RING_GATE && !tc::mbar_wait(bar.q_full, 0, abort)) break;
         if (q >= SLOTS && !tc::mbar_wait(bar.empty + s, use_parity(q - SLOTS), abort)) break;
         if (*abort) break;
         tc::mbar_expect_tx(bar.full + s, SLOT_BYTES);  // both halves of the whole tile
@@ -229,7 +404,7 @@ attn_tc_kernel(const __nv_bfloat16 *__restrict__ Qg, const __grid_constant__ CUt
           item_at(q, nt, is_v, tile);
           const CUtensorMap *map = is_v ? &mapV : &mapK;
           const int kb = (t0 + tile) * TK + rank * box_rows;
-          uint8_t *dst = base + Smem::RING + s * SLOT_BYTES + rank * box_rows * 128;
+          uint8_t *dst = base + Lay::RING + s * SLOT_BYTES + rank * box_rows * 128;
           for (int hf = 0; hf < 2; ++hf) {
             if (multicast)
               tc::tma_load_3d_mc(dst + hf * HALF_BYTES, map, bar.full + s, hf * 64, kb, plane,
@@ -246,7 +421,7 @@ attn_tc_kernel(const __nv_bfloat16 *__restrict__ Qg, const __grid_constant__ CUt
       // ------------------------------------------------------------- MMA issuer
       constexpr uint32_t idS = tc::idesc_bf16(128, TK, false, false);
       constexpr uint32_t idO = tc::idesc_bf16(128, 128, false, true);
-      const uint32_t ring = tc::smem_u32(base + Smem::RING);
+      const uint32_t ring = tc::smem_u32(base + Lay::RING);
       // Descriptors are built once; a K step moves the start address, which sits in the
       // low 14 bits (address >> 4) and never carries out of them inside shared memory.
       const uint64_t dK = tc::sdesc_sw128(ring, 16, 1024);
@@ -310,44 +485,15 @@ attn_tc_kernel(const __nv_bfloat16 *__restrict__ Qg, const __grid_constant__ CUt
     // ------------------------------------------------------------------- softmax
     const int rl = warp * 32 + lane;                // row within the M-tile = TMEM lane
     const int r = row0 + rl;                        // row within the segment
-    const bool row_ok = r < g * n;
-    const uint64_t mrow = row_ok ? mask[(size_t)b * N + r / g] : 0ull;
+    const uint64_t mrow = r < g * n ? mask[(size_t)b * N + r / g] : 0ull;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const uint32_t tO = tmem + lane_base + O_COL;
     const float sl2 = scale * LOG2E;  // scale > 0: the max of raw scores gives the max
     float m_used = -INFINITY, l = 0.f;  // reference max (log2 units) and sum of this row
-    {
-      // Q row r = node * g + head-in-group, as 64 bf16 pairs (low half = even element),
-      // the tensor-memory layout of an M-tile operand; rows past the tree are zero
-      const int node = r / g;
-      uint32_t qw[64];
-      if (node < N) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(
-            Qg + (((size_t)b * N + node) * Hq + (size_t)h * g + (r - node * g)) * ATTN_D);
-#pragma unroll
-        for (int v = 0; v < 16; ++v) {
-          const uint4 x = __ldg(src + v);
-          qw[4 * v] = x.x;
-          qw[4 * v + 1] = x.y;
-          qw[4 * v + 2] = x.z;
-          qw[4 * v + 3] = x.w;
-        }
-      } else {
-#pragma unroll
-        for (int v = 0; v < 64; ++v) qw[v] = 0u;
-      }
-      const uint32_t tQ = tmem + lane_base + Q_COL;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t w[16];
-#pragma unroll
-        for (int q = 0; q < 16; ++q) w[q] = qw[c * 16 + q];
-        tc::tmem_st16(tQ + c * 16, w);
-      }
-      tc::tmem_wait_st();
-      tc::tc_fence_before();
-      tc::mbar_arrive(bar.q_full);
-    }
+    q_row_to_tmem(Qg, b, N, Hq, h, g, r, tmem + lane_base + Q_COL);
+    asm volatile("" ::"l"(mrow));  // the mask word has arrived before the arrival below
+    tc::tc_fence_before();
+    tc::mbar_arrive(bar.q_full);
     bool ok = true;
     for (int j = 0; ok && j < nt; ++j) {
       const uint32_t tS = tmem + lane_base + (uint32_t)((j % NSBUF) * 128);
@@ -365,81 +511,9 @@ attn_tc_kernel(const __nv_bfloat16 *__restrict__ Qg, const __grid_constant__ CUt
       tc::tc_fence_before();
       tc::mbar_arrive(bar.s_free + j % NSBUF);  // S(j) is in registers: S(j+2) may follow
       const int kb = (t0 + j) * TK;
-      float alpha = 1.f;
+      float alpha;
       uint32_t pk[4][16];  // P(j) as bf16 pairs, stored once the previous P is consumed
-      // Fast path, for a tile wholly inside the committed prefix once the row has a finite
-      // reference max: no max pass. p = 2^(s*scale*log2e - m_used) straight away, with the
-      // tile's sum as the overflow test: sum <= 2^15 = 128 * 2^8 means no p exceeded the
-      // lazy-rescale bound 2^8, so the result is what the general path below computes
-      // (up to summation order). Otherwise (rare: the row's max grew by more than 8 in
-      // log2 units) the warp falls back to the general path, which recomputes every P word
-      // of this tile with a rescaled reference.
-      bool done = false;
-      if (__all_sync(0xffffffffu, kb + TK <= P && j > 0 && m_used > -INFINITY)) {
-        const uint64_t a2 = tc::f32x2_pack(sl2, sl2), c2 = tc::f32x2_pack(-m_used, -m_used);
-        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            float p0, p1;
-            tc::ex2_fma_x2(__uint_as_float(s[c][2 * q]), __uint_as_float(s[c][2 * q + 1]), a2,
-                           c2, p0, p1);
-            tc::add_x2(acc[q & 3], p0, p1);
-            pk[c][q] = tc::pack_bf16x2(p0, p1);
-          }
-        const float lt = (tc::f32x2_sum(acc[0]) + tc::f32x2_sum(acc[1])) +
-                         (tc::f32x2_sum(acc[2]) + tc::f32x2_sum(acc[3]));
-        done = __all_sync(0xffffffffu, lt <= 32768.f);  // false for inf and NaN too
-        if (done) l += lt;
-      }
-      if (!done) {
-        // 8 independent partial maxima of the raw scores keep the dependent chain short
-        float mxa[8];
-#pragma unroll
-        for (int a = 0; a < 8; ++a) mxa[a] = -INFINITY;
-        if (kb + TK <= P) {  // whole tile inside the committed prefix: every key visible
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int q = 0; q < 32; ++q) mxa[q & 7] = fmaxf(mxa[q & 7], __uint_as_float(s[c][q]));
-        } else {
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int q = 0; q < 32; ++q) {
-              const int key = kb + c * 32 + q;
-              const bool vis =
-                  key < P || (key < keys && ((mrow >> (unsigned)(key - P)) & 1ull));
-              if (!vis) s[c][q] = __float_as_uint(-INFINITY);
-              mxa[q & 7] = fmaxf(mxa[q & 7], __uint_as_float(s[c][q]));
-            }
-        }
-        const float mx = sl2 * fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
-                                     fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
-        // lazy rescale: move the reference max only when it grows by more than 8 (x256)
-        if (mx > m_used + 8.f) {
-          alpha = (m_used == -INFINITY) ? 0.f : tc::ex2_approx(m_used - mx);
-          m_used = mx;
-        }
-        l *= alpha;
-        // p = 2^(s * scale * log2 e - m); a row with no visible key so far has m = -inf
-        // and every s = -inf: its p are 0 (not NaN)
-        const float msub = m_used == -INFINITY ? 0.f : m_used;
-        float la[8];
-#pragma unroll
-        for (int a = 0; a < 8; ++a) la[a] = 0.f;
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            const float p0 = tc::ex2_approx(fmaf(__uint_as_float(s[c][2 * q]), sl2, -msub));
-            const float p1 = tc::ex2_approx(fmaf(__uint_as_float(s[c][2 * q + 1]), sl2, -msub));
-            la[q & 7] += p0 + p1;
-            pk[c][q] = tc::pack_bf16x2(p0, p1);
-          }
-        l += ((la[0] + la[1]) + (la[2] + la[3])) + ((la[4] + la[5]) + (la[6] + la[7]));
-      }
+      softmax_tile(s, kb, P, keys, mrow, sl2, j > 0, m_used, l, alpha, pk);
       // O += P(j-1) V(j-1) must have completed before O is rescaled here and before P(j)
       // overwrites P(j-1)
       if (j > 0 && !__all_sync(0xffffffffu, tc::mbar_wait(bar.o_ready, (uint32_t)((j - 1) & 1), abort))) {
@@ -448,20 +522,7 @@ attn_tc_kernel(const __nv_bfloat16 *__restrict__ Qg, const __grid_constant__ CUt
       }
       if (__any_sync(0xffffffffu, alpha != 1.f && j > 0)) {
         tc::tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tc::tmem_ld32(tO + c * 32, o);
-          tc::tmem_wait_ld();
-          uint32_t w[16];
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-#pragma unroll
-            for (int q = 0; q < 16; ++q)
-              w[q] = __float_as_uint(__uint_as_float(o[half * 16 + q]) * alpha);
-            tc::tmem_st16(tO + c * 32 + half * 16, w);
-          }
-        }
+        rescale_o(tO, alpha);
       }
       const uint32_t tP = tmem + lane_base + P_COL;
 #pragma unroll
@@ -474,7 +535,7 @@ attn_tc_kernel(const __nv_bfloat16 *__restrict__ Qg, const __grid_constant__ CUt
           ok = false;
           break;
         }
-        uint8_t *vt = base + Smem::RING + slot_of(qv) * SLOT_BYTES;
+        uint8_t *vt = base + Lay::RING + slot_of(qv) * SLOT_BYTES;
         const int first = keys - kb > 0 ? keys - kb : 0;
         for (int e = rl; e < (TK - first) * 16; e += 128) {
           const int row = first + e / 16, chunk = e % 16;  // 2 halves x 8 chunks of 16 B
@@ -487,40 +548,7 @@ attn_tc_kernel(const __nv_bfloat16 *__restrict__ Qg, const __grid_constant__ CUt
       tc::mbar_arrive(bar.p_full);
     }
     if (ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(bar.o_done, 0, abort));
-    // The normalised partial rows leave through shared memory so that every warp store
-    // covers a whole 512-byte row: the ring is idle once O is complete (every item was
-    // consumed, so no copy is in flight into it). Rows are staged at a 528-byte pitch,
-    // which keeps the threads' 16-byte writes free of bank conflicts.
-    constexpr int PITCH = ATTN_D * 4 + 16;
-    const bool wok = __all_sync(0xffffffffu, ok);
-    if (wok) {
-      tc::tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint8_t *srow = base + Smem::RING + rl * PITCH;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t o[32];
-        tc::tmem_ld32(tO + c * 32, o);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int q = 0; q < 32; q += 4)
-          *reinterpret_cast<float4 *>(srow + (c * 32 + q) * 4) =
-              make_float4(__uint_as_float(o[q]) * inv, __uint_as_float(o[q + 1]) * inv,
-                          __uint_as_float(o[q + 2]) * inv, __uint_as_float(o[q + 3]) * inv);
-      }
-      if (row_ok)
-        ws.lse[(size_t)p * ws.rows_pad + r] = l > 0.f ? (m_used + log2f(l)) * LN2 : -INFINITY;
-    }
-    // the four softmax warps meet (named barrier 1, 128 threads); each then writes 32 rows
-    const int wall = __syncthreads_and_named(wok);
-    if (wall) {
-      float *dst0 = ws.opart + ((size_t)p * ws.rows_pad + row0) * ATTN_D;
-      for (int rr = warp * 32; rr < warp * 32 + 32; ++rr) {
-        if (row0 + rr >= g * n) break;  // rows past the tree are never read
-        const float4 v = *reinterpret_cast<const float4 *>(base + Smem::RING + rr * PITCH + lane * 16);
-        *reinterpret_cast<float4 *>(dst0 + (size_t)rr * ATTN_D + lane * 4) = v;
-      }
-    }
+    write_partial(base + Lay::RING, tO, ok, l, m_used, p, row0, g * n, ws);
   }
 
   tc::tc_fence_before();
@@ -570,11 +598,10 @@ bool encode(CUtensorMap *map, const void *ptr, int rank, const cuuint64_t *dims,
 
 int cluster_of(int g, int N) { return ceil_div(g * N, 128); }
 int loaders_of(int C) { return C >= 4 ? 4 : (C >= 2 ? 2 : 1); }
-
 bool set_attributes() {
   static SmemAttr attr;
-  return ensure_smem(attn_tc_kernel, (int)TC_SMEM, attr, "cudaFuncSetAttribute(attn_tc_kernel)") ==
-         GT_OK;
+  return ensure_smem(attn_tc_kernel, (int)Smem::BYTES, attr,
+                     "cudaFuncSetAttribute(attn_tc_kernel)") == GT_OK;
 }
 
 }  // namespace
@@ -602,7 +629,7 @@ int attn_tc_pieces(int g, int N) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(C * clusters);
     cfg.blockDim = dim3(TC_THREADS);
-    cfg.dynamicSmemBytes = TC_SMEM;
+    cfg.dynamicSmemBytes = Smem::BYTES;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = C;
@@ -640,8 +667,8 @@ int attn_tc_launch(const void *Q, const void *K, const void *V, const uint64_t *
   if (!set_attributes()) return GT_ERR_CUDA;
   // one cluster of C CTAs per piece; the schedule never makes more than `pieces`
   return launch_cluster(attn_tc_kernel, dim3(C * pieces), dim3(TC_THREADS), dim3(C, 1, 1),
-                        TC_SMEM, s, (const __nv_bfloat16 *)Q, mK, mV, mask, sa.prefix_len, sa.n_nodes, N, Hq, Hkv,
-                        scale, C, L, sa, ws, err);
+                        Smem::BYTES, s, (const __nv_bfloat16 *)Q, mK, mV, mask, sa.prefix_len,
+                        sa.n_nodes, N, Hq, Hkv, scale, C, L, sa, ws, err);
 }
 
 }  // namespace gt
