@@ -12,7 +12,7 @@
 // 1/L of every tile with a cluster-multicast TMA, so every tile leaves L2 once and lands
 // in all C shared memories.
 //
-// Roles (192 threads, one CTA per SM):
+// Roles (224 threads, one CTA per SM):
 //   warp 4      TMA producer: the K/V items in consumption order, through a ring of 7
 //               slots of 32 KB: K(0), K(1), K(2), V(0), K(3), V(1), ... (K runs two tiles
 //               ahead of V). A slot is refilled once the MMA threads of all C CTAs released
@@ -20,11 +20,16 @@
 //               the producer waits until this CTA's softmax threads hold their Q rows and
 //               ancestor masks, so that those small loads are not queued behind the ring's
 //               burst of loads at the start.
-//   warp 5      MMA issuer (one thread) and tensor-memory owner.
-//               S(t) = Q K(t)^T goes to one of two S buffers (Q from tensor memory, K from
-//               shared memory); S(j+2) is issued as soon as the softmax has read S(j) into
-//               registers, so Q K^T stays two tiles ahead. O += P(j) V(j) as soon as the
-//               softmax published P(j).
+//   warp 5      Q K^T issuer (one thread) and tensor-memory owner. S(t) = Q K(t)^T goes to
+//               one of two S buffers (Q from tensor memory, K from shared memory); S(j+2)
+//               is issued as soon as the softmax has read S(j) into registers, so Q K^T
+//               stays two tiles ahead.
+//   warp 6      P V issuer (one thread): O += P(j) V(j) as soon as the softmax published
+//               P(j). The two streams touch disjoint tensor and shared memory, so each
+//               thread commits only its own MMAs. With one issuer, P V(j) would wait behind
+//               the Q K^T(j+2) instructions (an MMA issue blocks for about the MMA's
+//               execution time), and the softmax, which stores P(j+1) only after P V(j),
+//               would wait with it.
 //   warps 0-3   softmax: thread = query row = tensor-memory lane. First the thread copies
 //               its Q row into tensor memory. Per tile: read the S row (and free its
 //               buffer), mask, p = 2^(s*scale*log2e - m) with a lazily moved reference max
@@ -52,7 +57,7 @@ namespace gt {
 
 namespace {
 
-constexpr int TC_THREADS = 192;     // 4 softmax warps + producer + MMA
+constexpr int TC_THREADS = 224;     // 4 softmax warps + producer + two MMA issuers
 constexpr int TK = ATTN_TC_KEYS;    // keys per tile (128)
 constexpr int NSBUF = 2;            // S buffers in tensor memory
 constexpr int KLEAD = 2;            // K tiles loaded ahead of V (= NSBUF)
@@ -76,8 +81,8 @@ struct Smem {
   static constexpr int RING = 0;
   static constexpr int BAR = RING + SLOTS * SLOT_BYTES;
   // q_full, full[SLOTS], empty[SLOTS], s_full[NSBUF], s_free[NSBUF], p_full, o_ready,
-  // o_done, drain
-  static constexpr int NBAR = 1 + 2 * SLOTS + 2 * NSBUF + 4;
+  // o_done, drain[2] (one per MMA issuer)
+  static constexpr int NBAR = 1 + 2 * SLOTS + 2 * NSBUF + 5;
   static constexpr int END = BAR + NBAR * 8;
   static constexpr size_t BYTES = END + 1024;  // + alignment slack
   static_assert(BYTES + 768 <= 232448, "shared memory of one CTA (dynamic + static)");
@@ -352,6 +357,7 @@ attn_tc_kernel(const __nv_bfloat16 *__restrict__ Qg, const __grid_constant__ CUt
     tc::mbar_init(bar.o_ready, 1);
     tc::mbar_init(bar.o_done, 1);
     tc::mbar_init(bar.drain, 1);
+    tc::mbar_init(bar.drain + 1, 1);
     tc::fence_mbar_init();
   }
   if (warp == 5) {
@@ -416,9 +422,10 @@ attn_tc_kernel(const __nv_bfloat16 *__restrict__ Qg, const __grid_constant__ CUt
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 5 || warp == 6) {
     if (lane == 0) {
-      // ------------------------------------------------------------- MMA issuer
+      // ------------------------------------------------------------- MMA issuers
+      const bool qk = warp == 5;  // warp 5: Q K^T; warp 6: P V
       constexpr uint32_t idS = tc::idesc_bf16(128, TK, false, false);
       constexpr uint32_t idO = tc::idesc_bf16(128, 128, false, true);
       const uint32_t ring = tc::smem_u32(base + Lay::RING);
@@ -427,7 +434,8 @@ attn_tc_kernel(const __nv_bfloat16 *__restrict__ Qg, const __grid_constant__ CUt
       const uint64_t dK = tc::sdesc_sw128(ring, 16, 1024);
       const uint64_t dV = tc::sdesc_sw128(ring, HALF_BYTES, 1024);
       // a slot's release is only sent when a later item will refill it, so every release
-      // that reaches a peer is awaited by that peer's producer
+      // that reaches a peer is awaited by that peer's producer; it follows the issuing
+      // thread's own MMAs, the ones that read the slot
       auto release = [&](int q) {
         if (q + SLOTS >= total) return;
         if (multicast)
@@ -435,51 +443,57 @@ attn_tc_kernel(const __nv_bfloat16 *__restrict__ Qg, const __grid_constant__ CUt
         else
           tc::mma_commit(bar.empty + slot_of(q));
       };
-      auto issue_s = [&](int t) {  // S(t) = Q K(t)^T over d = 128 (8 steps of 16)
-        const int q = pos_k(t, nt);
-        if (!tc::mbar_wait(bar.full + slot_of(q), use_parity(q), abort)) return false;
-        tc::tc_fence_after();
-        const uint64_t b0 = dK + ((slot_of(q) * SLOT_BYTES) >> 4);
-        const uint32_t dS = tmem + (uint32_t)((t % NSBUF) * 128);
+      bool ok = true;
+      if (qk) {
+        auto issue_s = [&](int t) {  // S(t) = Q K(t)^T over d = 128 (8 steps of 16)
+          const int q = pos_k(t, nt);
+          if (!tc::mbar_wait(bar.full + slot_of(q), use_parity(q), abort)) return false;
+          tc::tc_fence_after();
+          const uint64_t b0 = dK + ((slot_of(q) * SLOT_BYTES) >> 4);
+          const uint32_t dS = tmem + (uint32_t)((t % NSBUF) * 128);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = ((kk >> 2) * HALF_BYTES + (kk & 3) * 32) >> 4;
-          tc::mma_ts(dS, tmem + Q_COL + kk * 8, b0 + off, idS, kk > 0);
-        }
-        tc::mma_commit(bar.s_full + t % NSBUF);
-        release(q);
-        return true;
-      };
-      bool ok = tc::mbar_wait(bar.q_full, 0, abort);
-      for (int t = 0; ok && t < min(KLEAD, nt); ++t) ok = issue_s(t);
-      for (int j = 0; ok && j < nt; ++j) {
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = ((kk >> 2) * HALF_BYTES + (kk & 3) * 32) >> 4;
+            tc::mma_ts(dS, tmem + Q_COL + kk * 8, b0 + off, idS, kk > 0);
+          }
+          tc::mma_commit(bar.s_full + t % NSBUF);
+          release(q);
+          return true;
+        };
+        ok = tc::mbar_wait(bar.q_full, 0, abort);
+        for (int t = 0; ok && t < min(KLEAD, nt); ++t) ok = issue_s(t);
         // S(j+2) into the buffer of S(j) once every softmax thread has read S(j)
-        if (j + KLEAD < nt) {
+        for (int j = 0; ok && j + KLEAD < nt; ++j) {
           if (!tc::mbar_wait(bar.s_free + j % NSBUF, (uint32_t)((j / NSBUF) & 1), abort)) {
             ok = false;
             break;
           }
           tc::tc_fence_after();
-          if (!(ok = issue_s(j + KLEAD))) break;
+          ok = issue_s(j + KLEAD);
         }
-        const int qv = pos_v(j, nt);
-        if (!tc::mbar_wait(bar.p_full, j & 1, abort) ||
-            !tc::mbar_wait(bar.full + slot_of(qv), use_parity(qv), abort)) {
-          ok = false;
-          break;
-        }
-        tc::tc_fence_after();
-        const uint64_t v0 = dV + ((slot_of(qv) * SLOT_BYTES) >> 4);
+      } else {
+        for (int j = 0; ok && j < nt; ++j) {
+          const int qv = pos_v(j, nt);
+          if (!tc::mbar_wait(bar.p_full, j & 1, abort) ||
+              !tc::mbar_wait(bar.full + slot_of(qv), use_parity(qv), abort)) {
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+          const uint64_t v0 = dV + ((slot_of(qv) * SLOT_BYTES) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // O += P V over 128 keys (steps of 16)
-          tc::mma_ts(tmem + O_COL, tmem + P_COL + kk * 8, v0 + ((kk * 2048) >> 4), idO,
-                     (j > 0) || (kk > 0));
-        tc::mma_commit(bar.o_ready);
-        release(qv);
+          for (int kk = 0; kk < 8; ++kk)  // O += P V over 128 keys (steps of 16)
+            tc::mma_ts(tmem + O_COL, tmem + P_COL + kk * 8, v0 + ((kk * 2048) >> 4), idO,
+                       (j > 0) || (kk > 0));
+          tc::mma_commit(bar.o_ready);
+          release(qv);
+        }
+        if (ok) tc::mma_commit(bar.o_done);
       }
-      if (ok) tc::mma_commit(bar.o_done);
-      tc::mma_commit(bar.drain);  // every MMA issued above completes before teardown
-      drain_wait(bar.drain, 0);
+      // every MMA this thread issued completes before teardown
+      uint64_t *drain = bar.drain + (qk ? 0 : 1);
+      tc::mma_commit(drain);
+      drain_wait(drain, 0);
     }
   } else {
     // ------------------------------------------------------------------- softmax
