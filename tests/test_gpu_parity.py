@@ -484,16 +484,22 @@ def test_tree_attn_two_cta_cluster_shapes():
         ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
         err = torch.zeros(1, dtype=torch.int32, device="cuda")
         scale = 1.0 / np.sqrt(d)
-        gt.gt_tree_attn(dev[0], dev[1], dev[2], _t(mask), _t(P), _t(n), B, N, Hq, Hkv, d, Lcap,
-                        gt.GT_BF16, scale, O, ws, wsb, err)
-        torch.cuda.synchronize()
-        assert err.item() == 0
-        got = O.float().cpu().numpy().astype(np.float64)
+        refs = []
         for b in range(B):
             L = int(P[b] + n[b])
-            ref = oracle.tree_attn(oracle.bf16_to_f64(hq[b]), oracle.bf16_to_f64(hk[b][:, :L]),
-                                   oracle.bf16_to_f64(hv[b][:, :L]), parent[b], int(n[b]),
-                                   int(P[b]), scale)
-            e = float(np.abs(got[b, :n[b]] - ref).max())
-            assert e <= TOL["bf16"], (B, N, Hq, Hkv, b, e)
-            assert np.all(got[b, n[b]:] == 0.0)
+            refs.append(oracle.tree_attn(oracle.bf16_to_f64(hq[b]), oracle.bf16_to_f64(hk[b][:, :L]),
+                                         oracle.bf16_to_f64(hv[b][:, :L]), parent[b], int(n[b]),
+                                         int(P[b]), scale))
+        # twice on one workspace (the second call finds what the first left there) and into
+        # an output filled with NaN: every output element is written
+        for _ in range(2):
+            O.fill_(float("nan"))
+            gt.gt_tree_attn(dev[0], dev[1], dev[2], _t(mask), _t(P), _t(n), B, N, Hq, Hkv, d,
+                            Lcap, gt.GT_BF16, scale, O, ws, wsb, err)
+            torch.cuda.synchronize()
+            assert err.item() == 0
+            got = O.float().cpu().numpy().astype(np.float64)
+            for b in range(B):
+                e = float(np.abs(got[b, :n[b]] - refs[b]).max())
+                assert e <= TOL["bf16"], (B, N, Hq, Hkv, b, e)
+                assert np.all(got[b, n[b]:] == 0.0)
