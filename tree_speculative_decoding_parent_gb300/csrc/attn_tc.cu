@@ -109,7 +109,7 @@ __device__ __forceinline__ Bars bars_at(uint8_t *base) {
   return r;
 }
 
-// Item sequence of a piece of nt tiles, the order in which the MMA thread consumes them:
+// Item sequence of a piece of nt tiles, the order in which the MMA threads consume them:
 // K(0..P0-1) with P0 = min(KLEAD, nt), then for j = 0..nt-1: K(j+KLEAD) while
 // j+KLEAD < nt, followed by V(j). Item q sits in slot q % SLOTS as that slot's use number
 // q / SLOTS. The last item is V(nt-1).
@@ -347,7 +347,7 @@ attn_tc_kernel(const __nv_bfloat16 *__restrict__ Qg, const __grid_constant__ CUt
     tc::mbar_init(bar.q_full, 128);  // every softmax thread stored its Q row
     for (int s = 0; s < SLOTS; ++s) {
       tc::mbar_init(bar.full + s, 1);
-      tc::mbar_init(bar.empty + s, C);  // one release from each CTA's MMA thread
+      tc::mbar_init(bar.empty + s, C);  // one release per CTA, by the thread whose MMAs read it
     }
     for (int s = 0; s < NSBUF; ++s) {
       tc::mbar_init(bar.s_full + s, 1);
