@@ -35,3 +35,23 @@ def test_roofline_bound_follows_the_measured_ridge():
 def test_throughput_counts_every_rank():
     assert bench.job_throughput(1, 200, 0.5) == 400.0
     assert bench.job_throughput(4, 200, 0.5) == 1600.0
+
+
+def test_reference_arm_line_carries_the_contract_keys():
+    """The reference arm times the oracle on the host: one JSON-ready line with the GPU arm's
+    metric and unit, impl "reference", a CPU baseline describing the run and an e2e object
+    that moves no bytes; ranks other than 0 return nothing."""
+    import argparse
+    args = argparse.Namespace(config=1, steps=1, warmup=3, ref_budget=0.0, temperature=0.0,
+                              seed=1)
+    line = bench.run_reference(args, 0, 1)
+    json.dumps(line)  # serialisable as printed
+    assert line["impl"] == "reference"
+    assert line["metric"] == bench.METRIC and line["unit"] == "steps/s"
+    assert line["higher_is_better"] is True and line["steps"] >= 1 and line["value"] > 0
+    assert line["config"]["workload"] == bench.CONFIGS[1]["name"]
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1
+    assert line["e2e"] == {"value": line["value"], "unit": "steps/s",
+                           "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert bench.run_reference(args, 1, 2) is None
