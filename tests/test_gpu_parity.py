@@ -382,7 +382,7 @@ def test_tree_attn_edge_shapes(dtype):
     """Random trees through gt_tree_attn alone, masks from the oracle: a full 64-node mask
     word, single-node trees, zero prefixes, prefixes on and next to 128-key tile edges,
     8 query heads per KV head (512 query rows of one KV head), and more segments than one
-    wave of clusters (both schedule paths)."""
+    wave of clusters (both schedule paths), and clusters of two, three and four CTAs."""
     from workload import f32_to_bf16_bits
     rng = np.random.default_rng(21)
     cases = [  # B, N, Hq, Hkv, prefixes, nodes per request (None: N)
@@ -394,6 +394,11 @@ def test_tree_attn_edge_shapes(dtype):
         (20, 9, 16, 8, rng.integers(0, 700, size=20).tolist(), rng.integers(1, 10, size=20).tolist()),
         # 96 segments over 38 clusters of 4 CTAs: the one-warp schedule in several waves
         (12, 49, 64, 8, rng.integers(0, 900, size=12).tolist(), rng.integers(1, 50, size=12).tolist()),
+        # three-CTA clusters (257..384 rows), whose third CTA loads nothing and receives every
+        # tile by multicast: ragged trees over two requests, and one segment cut into
+        # one-tile pieces
+        (2, 33, 64, 8, [130, 7], [33, 20]),
+        (1, 24, 16, 1, [3000], None),
     ]
     for B, N, Hq, Hkv, P, nn in cases:
         d = 128
