@@ -7,7 +7,9 @@ host synchronisation. The timed region replays a CUDA graph of K such steps; the
 rotate over several device copies whose total size is a multiple of the 129 MB L2, so
 every step streams its K/V cache and logits from HBM.
 
-Prints ONE JSON line (rank 0). `--impl reference` times the CPU oracle instead.
+Prints ONE JSON line. The GPU arm runs on exactly one GPU (it refuses WORLD_SIZE > 1
+before touching CUDA); `--impl reference` times the CPU oracle instead (under torchrun,
+rank 0 alone runs and prints it).
 """
 from __future__ import annotations
 
@@ -33,6 +35,7 @@ L2_BYTES = 129 * 2 ** 20
 # Event record nodes end the programmatic overlap of the calls around them, so the timed
 # graph brackets the attention call with events in one step out of ATTN_EVENT_EVERY only.
 ATTN_EVENT_EVERY = 8  # one step in 8 has its attention call bracketed by events
+ATTN_MIN_TIMED = 10   # bracketed attention calls per run, however few steps are timed
 
 
 def _peaks():
@@ -82,6 +85,27 @@ def step_bytes(scn) -> int:
     table = B * N * scn.k * 4 * 2 + len(scn.tpar) * 8       # graft reads + update writes
     verify = B * N * scn.k * 8 + B * N * 16
     return attn_bytes(scn) + logits + tree + table + verify
+
+
+def rotation(scn):
+    """(bytes of one input set, number of device copies the timed graph rotates over): the
+    K/V cache, Q, the logits and the table of one set; enough sets that four L2 sizes pass
+    between two uses of the same set."""
+    es = 2 if scn.dtype == "bf16" else 4
+    per_set = (2 * scn.K.size + scn.Q.size) * es + scn.B * scn.N * scn.V * 4 + \
+        scn.table.size * 4
+    return per_set, max(2, -(-4 * L2_BYTES // per_set))
+
+
+def workload_config(scn, cid: int, temperature: float) -> dict:
+    """The `config` object both arms print: what the workload is, nothing measured."""
+    per_set, nsets = rotation(scn)
+    return {"workload": scn.name, "config_id": cid, "B": scn.B, "temperature": temperature,
+            "prefix_len": int(max(scn.prefix_len)), "slots": scn.N, "vocab": scn.V,
+            "heads": f"{scn.Hq}/{scn.Hkv}x{scn.d}", "parallelism": "single GPU",
+            "l2": f"inputs rotate over {nsets} device copies of {per_set / 1e6:.1f} MB "
+                  f"(> L2 of {L2_BYTES / 2**20:.0f} MiB)",
+            "step_bytes": step_bytes(scn)}
 
 
 class ClockSampler:
@@ -144,23 +168,6 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
                 "reasons": sorted(self.reasons), "samples": len(self.samples),
                 "source": "nvml"}
-
-
-def max_over_ranks(x: float, dist, device) -> float:
-    """The largest x over all ranks (the slowest rank sets the job's time); x itself when
-    there is no process group."""
-    if dist is None:
-        return x
-    import torch
-    t = torch.tensor([x], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
-
-
-def job_throughput(world: int, steps_per_rank: int, seconds: float) -> float:
-    """Whole-job steps/s: every rank ran its own replica of `steps_per_rank` steps, and the
-    job took as long as its slowest rank."""
-    return world * steps_per_rank / seconds
 
 
 def _traffic_record(kernel_key: str):
@@ -240,9 +247,8 @@ def run_reference(args, rank: int, world: int):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s",
         "n_gpus": world, "steps": done, "warmup": args.warmup, "ms_per_step": 1e3 * dt / done,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded generator; see DESIGN.md input recipe)",
-        "config": {"workload": CONFIGS[args.config]["name"], "config_id": args.config,
-                   "temperature": args.temperature},
+        "data": "synthetic (seeded generator of the five workload shapes)",
+        "config": workload_config(scn, args.config, args.temperature),
         "cpu_baseline": {"value": value, "unit": "steps/s", "cores": cores, "kind": "oracle",
                          "sample": f"{done} whole steps of the same workload on the host CPU "
                                    f"(numpy float64; BLAS may use all {cores} cores)"},
@@ -257,7 +263,7 @@ def run_reference(args, rank: int, world: int):
 # --------------------------------------------------------------------------------------
 
 
-def run_gpu(args, rank: int, world: int, local_rank: int):
+def run_gpu(args):
     import torch
     from tree_speculative_decoding_parent_gb300 import build, gt
     from tree_speculative_decoding_parent_gb300.step import (StepBuffers, StepShape, run_attn,
@@ -266,9 +272,9 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
                                                              run_verify_sample_commit)
     build.build()
     gt.load()
-    dev = torch.device("cuda", local_rank)
+    dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    scn = make_scenario(args.config, seed=args.config + 1000 * rank)
+    scn = make_scenario(args.config)
     shape = StepShape(B=scn.B, Nin=scn.Nin, N=scn.N, V=scn.V, k=scn.k, Hq=scn.Hq, Hkv=scn.Hkv,
                       d=scn.d, Lcap=scn.Lcap, T=len(scn.tpar),
                       dtype=gt.GT_BF16 if scn.dtype == "bf16" else gt.GT_F32)
@@ -299,9 +305,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     logits_np = scn.logits(buf.parent.cpu().numpy(), buf.tokens.cpu().numpy(),
                            buf.n_nodes.cpu().numpy())
     base["logits"] = to_dev(logits_np)
-    per_set = sum(base[k].numel() * base[k].element_size()
-                  for k in ("K", "V", "logits", "Q", "table"))
-    nsets = max(2, -(-4 * L2_BYTES // per_set))
+    per_set, nsets = rotation(scn)
     sets = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(nsets - 1)]
     stream = torch.cuda.current_stream(dev)
 
@@ -311,7 +315,9 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     if int(buf.err.item()) != 0:
         raise RuntimeError(f"device error {gt.status_string(int(buf.err.item()))}")
 
-    def capture(nsteps: int, with_events: bool):
+    def capture(nsteps: int, event_every: int = 0):
+        """A graph of nsteps whole steps rotating over the input sets; with event_every > 0
+        the attention call of every event_every-th step is bracketed by event records."""
         g = torch.cuda.CUDAGraph()
         evs = []
         with torch.cuda.graph(g):
@@ -319,9 +325,9 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
             for i in range(nsteps):
                 inp = sets[i % nsets]
                 run_tree_build(buf, inp, s)
-                timed = with_events and i % ATTN_EVENT_EVERY == 0
+                timed = event_every > 0 and i % event_every == 0
                 if timed:
-                    e0, e1 = ev_pool[2 * i], ev_pool[2 * i + 1]
+                    e0, e1 = ev_pool[2 * len(evs)], ev_pool[2 * len(evs) + 1]
                     gt.gt_event_record_external(e0, s)
                 run_attn(buf, inp, s, scn.scale)
                 if timed:
@@ -333,36 +339,36 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
                     run_verify_commit(buf, inp, s)
         return g, evs
 
-    # torch creates CUDA events lazily: record each once before capture so it exists
-    ev_pool = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
-    for e in ev_pool:
+    # the timed graph has no event nodes (an event record ends the programmatic overlap of
+    # the calls around it); the attention's per-call time comes from a second graph of the
+    # same steps in which one attention call in ATTN_EVENT_EVERY is bracketed, with at least
+    # ATTN_MIN_TIMED bracketed calls
+    attn_steps = max(args.steps, ATTN_EVENT_EVERY * ATTN_MIN_TIMED)
+    ev_pool = [torch.cuda.Event(enable_timing=True) for _ in range(2 * attn_steps)]
+    for e in ev_pool:  # torch creates CUDA events lazily: record each once before capture
         e.record(stream)
     torch.cuda.synchronize()
-    g_warm, _ = capture(max(args.warmup, 1), False)
-    g_timed, evs = capture(args.steps, True)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
+    g_warm, _ = capture(max(args.warmup, 1))
+    g_timed, _ = capture(args.steps)
+    g_attn, evs = capture(attn_steps, ATTN_EVENT_EVERY)
     g_warm.replay()
     torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    clk = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    clk = ClockSampler(torch.cuda.current_device())
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    replay_ms = []
+    clk.start()
+    for _ in range(args.reps):
+        torch.cuda.synchronize()
+        t0.record(stream)
+        g_timed.replay()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        replay_ms.append(t0.elapsed_time(t1))
+    g_attn.replay()
     torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    if clk:
-        clk.start()
-    t0.record(stream)
-    g_timed.replay()
-    t1.record(stream)
-    torch.cuda.synchronize()
-    clocks = clk.stop() if clk else None
-    if dist:
-        dist.barrier()
-    ms = max_over_ranks(t0.elapsed_time(t1), dist, dev)
+    clocks = clk.stop()
+    ms = statistics.median(replay_ms)
     errc = int(buf.err.item())
     if errc != 0:
         raise RuntimeError(f"device error {gt.status_string(errc)}")
@@ -429,12 +435,11 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     ne = max(5, min(args.steps, 50))
 
     def time_e2e(step_fn):
-        if dist:
-            dist.barrier()
+        torch.cuda.synchronize()
         te = time.perf_counter()
         for _ in range(ne):
             step_fn()
-        return max_over_ranks(time.perf_counter() - te, dist, dev)
+        return time.perf_counter() - te
 
     e2e_eager_s = time_e2e(e2e_step)
     # the same step (host-to-device copies, the calls, the read-back) captured once and
@@ -453,11 +458,9 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     e2e_s = time_e2e(e2e_graph_step)
 
     breakdown = None
-    if args.breakdown and rank == 0:
+    if args.breakdown:
         breakdown = call_breakdown(torch, gt, buf, sets, scn, nsets, args.temperature, args.seed)
 
-    if rank != 0:
-        return None
     peak, peak_kind = _peaks()
     ab = attn_bytes(scn)
     achieved = ab / (attn_avg_ms * 1e-3) / 1e9
@@ -474,31 +477,28 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
     else:
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_kind": peak_kind}
-    value = job_throughput(world, args.steps, ms * 1e-3)
+    value = args.steps / (ms * 1e-3)
+    sb = step_bytes(scn)
     line = {
-        "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
+        "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": scn.dtype,
-        "data": "synthetic (seeded generator; see DESIGN.md input recipe)",
-        "config": {"workload": scn.name, "config_id": args.config, "B": scn.B,
-                   "temperature": args.temperature,
-                   "prefix_len": int(max(scn.prefix_len)), "slots": scn.N, "vocab": scn.V,
-                   "heads": f"{scn.Hq}/{scn.Hkv}x{scn.d}",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": f"inputs rotate over {nsets} device copies of {per_set / 1e6:.1f} MB "
-                         f"(> L2 of {L2_BYTES / 2**20:.0f} MiB)",
-                   "step_bytes": step_bytes(scn),
-                   "step_byte_roofline_frac": step_bytes(scn) / (ms / args.steps * 1e-3) / 1e9
-                   / peak},
-        "roofline": {**roof, "kernel": "gt_tree_attn (sched + tcgen05/SIMT + combine)",
+        "data": "synthetic (seeded generator of the five workload shapes)",
+        "config": workload_config(scn, args.config, args.temperature),
+        "value_spread": {"replays": len(replay_ms), "statistic": "median",
+                         "steps_per_s": sorted(args.steps / (t * 1e-3) for t in replay_ms)},
+        "step_byte_roofline_frac": sb / (ms / args.steps * 1e-3) / 1e9 / peak,
+        "roofline": {**roof, "kernel": "gt_tree_attn (tcgen05/SIMT attention + combine)",
                      "flop_per_byte": af / ab,
                      "algorithmic_bytes_per_launch": ab,
                      "avg_launch_ms": attn_avg_ms,
-                     "timed_launches": f"{len(evs)} of {args.steps} (every {ATTN_EVENT_EVERY}th "
-                                       "step's call, bracketed by CUDA events in the timed graph)",
+                     "launch_ms_min_max": [min(attn_ms), max(attn_ms)],
+                     "timed_launches": f"{len(evs)} calls, each bracketed by CUDA events, one per "
+                                       f"{ATTN_EVENT_EVERY} steps of a {attn_steps}-step graph of "
+                                       "the same step (replayed after the timed replays)",
                      "traffic": _traffic_record(f"tree_attn/config{args.config}")},
-        "e2e": {"value": job_throughput(world, ne, e2e_s), "unit": "steps/s",
-                "eager_value": job_throughput(world, ne, e2e_eager_s),
+        "e2e": {"value": ne / e2e_s, "unit": "steps/s",
+                "eager_value": ne / e2e_eager_s,
                 "how": "pinned host inputs copied in (the logits on a side stream, overlapping "
                        "the tree build and the attention), the step's calls, results read back "
                        "and a host sync every step, replayed from one captured graph "
@@ -517,8 +517,40 @@ def run_gpu(args, rank: int, world: int, local_rank: int):
         line["cpu_baseline"] = {
             "value": cv, "unit": "steps/s", "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"{cdone} whole steps of the same workload (~{cdt:.0f} s, numpy float64; "
-                      "BLAS may use every core, the tree and top-k loops use one)"}
+                      "BLAS may use every core, the tree and top-k loops use one)",
+            "single_thread": oracle_single_thread(args.config, args.cpu_budget,
+                                                  args.temperature, args.seed)}
     return line
+
+
+def _single_thread_child(cid, budget, temperature, seed, out):
+    scn = make_scenario(cid)
+    out.put(time_oracle(scn, 1000, budget, temperature, seed))
+
+
+def oracle_single_thread(cid: int, budget: float, temperature: float, seed: int) -> dict:
+    """The same oracle timing in a fresh process whose BLAS and OpenMP pools have one thread
+    (the variables are read when numpy loads, so they are set for a spawned child)."""
+    import multiprocessing as mp
+    names = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+    saved = {n: os.environ.get(n) for n in names}
+    try:
+        for n in names:
+            os.environ[n] = "1"
+        ctx = mp.get_context("spawn")
+        q = ctx.Queue()
+        p = ctx.Process(target=_single_thread_child, args=(cid, budget, temperature, seed, q))
+        p.start()
+        value, done, dt = q.get(timeout=budget + 600)
+        p.join(timeout=60)
+    finally:
+        for n, v in saved.items():
+            if v is None:
+                os.environ.pop(n, None)
+            else:
+                os.environ[n] = v
+    return {"value": value, "unit": "steps/s", "cores": 1,
+            "sample": f"{done} whole steps (~{dt:.0f} s) with one BLAS/OpenMP thread"}
 
 
 def draft_timing(torch, gt, reps: int = 20):
@@ -632,15 +664,18 @@ def call_breakdown(torch, gt, buf, sets, scn, nsets, temperature=0.0, seed=0, re
 
 def main():
     ap = argparse.ArgumentParser(description=__doc__)
-    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--gpus", type=int, default=1,
+                    help="GPUs of the run; the GPU arm runs on exactly one")
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--reps", type=int, default=5,
+                    help="replays of the timed graph; the line reports their median")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=sorted(CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--breakdown", action="store_true",
                     help="also report the in-graph device time of each C-ABI call")
-    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--temperature", type=float, default=0.0,
                     help="0: greedy verification; > 0: one target draw per node at this T")
     ap.add_argument("--seed", type=int, default=1, help="seed of the draws at T > 0")
@@ -648,21 +683,19 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    args.reps = max(1, args.reps)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         line = run_reference(args, rank, world)
     else:
-        if world > 1:
-            import torch
-            import torch.distributed as dist
-            torch.cuda.set_device(local_rank)
-            dist.init_process_group("nccl")
-        line = run_gpu(args, rank, world, local_rank)
-        if world > 1:
-            import torch.distributed as dist
-            dist.destroy_process_group()
+        # The attention kernel streams K/V through cluster-multicast TMA loads, which this
+        # library runs only in single-GPU processes; the step is measured on one GPU.
+        if world != 1 or args.gpus != 1:
+            sys.stderr.write(f"bench.py: the GPU arm runs on exactly one GPU (got --gpus "
+                             f"{args.gpus}, WORLD_SIZE {world}); nothing was run\n")
+            sys.exit(2)
+        line = run_gpu(args)
     if line is not None:
         print(json.dumps(line), flush=True)
 

@@ -20,8 +20,9 @@
  *
  * Conventions shared by every entry point
  *   - Pointers named in the "device" list are caller-owned CUDA device pointers (or
- *     managed memory); the library never allocates, frees or keeps them. Host helpers
- *     at the end of the file take host pointers.
+ *     managed memory, except where an entry point says otherwise); the library never
+ *     allocates, frees or keeps them. Host helpers at the end of the file take host
+ *     pointers.
  *   - Trees are flattened in topological order: node 0 is the root (the current token),
  *     parent[0] = -1 and 0 <= parent[v] < v for v >= 1. Per-request arrays are
  *     row-major [B][stride]; entries at or beyond a request's node count are padding.
@@ -144,6 +145,11 @@ int gt_tree_mask(const int32_t *parent, const int32_t *n_nodes, const int32_t *p
  *               256-byte aligned; contents need no initialisation and are clobbered.
  * dtype GT_BF16 runs on the tcgen05 tensor cores (bf16 operands, fp32 accumulators in
  * tensor memory, K/V tiles staged by TMA); GT_F32 runs on FP32 FMA units.
+ * Q, K, V and O must be device memory of the current device (a cudaMalloc-family
+ * allocation made there; the first and last byte of each are checked). Host, managed and
+ * peer-device memory is refused with GT_ERR_ARG before anything is launched: the bf16
+ * kernel streams K and V through cluster-multicast TMA loads, which this library issues
+ * only over the memory of the GPU that runs them.
  * Limits: d = 128, 1 <= N <= 64, Hq % Hkv == 0, (Hq/Hkv)*N <= 512, Lcap >= 1, scale a
  * finite value > 0 (else GT_ERR_ARG); Q, K, V, O 16-byte aligned. Device errors: GT_ERR_RANGE (prefix_len + n_nodes > Lcap,
  * n_nodes outside [1, N], prefix_len < 0). Keys past a request's length are never read
@@ -170,9 +176,14 @@ int gt_tree_attn(const void *Q, const void *K, const void *V, const uint64_t *ma
  *     GT_ERR_SHAPE before anything is launched, with the sizes in gt_last_error(). With
  *     d = 128 the need is about 4*(SMs + B*Hkv)*ceil((Hq/Hkv)*N / 128)*128*128 bytes:
  *     e.g. B = 1, Hkv = 8, Hq/Hkv = 4, N = 60 needs about 21 MB and fits.
- *   - Set-up: the first call on each device (with that device current) looks up the
+ *   - Memory held: every device that loads libgt's module holds the array until the
+ *     process exits. Under lazy module loading (the CUDA default) that is every device on
+ *     which any libgt kernel has run; under CUDA_MODULE_LOADING=EAGER it is every device
+ *     with a context, whether or not this entry point is ever called.
+ *   - Set-up: the first call in each context (with that device current) looks up the
  *     array's device address with cudaGetSymbolAddress, which may load the module, and
- *     caches it. Make that first call before any stream capture. A failed look-up returns
+ *     caches it with the context's id; after cudaDeviceReset the next call looks it up
+ *     again. Make that first call before any stream capture. A failed look-up returns
  *     GT_ERR_CUDA.
  *   - Sharing: every call on a device uses the same array. Nothing in it needs to start at
  *     zero; each call writes what it later reads. Calls ordered on one stream are

@@ -17,7 +17,7 @@ Sources (page title, then section):
               n-gram drafter drafts from the target's top-m cache produced at prefill and a
               context n-gram index).
 
-Readings where the pages are silent (each one is also listed in the design doc):
+Readings where the pages are silent:
   * Frontier: the top-W pool nodes by (score desc, index asc; NaN last, as in the prune).
     The small drafter's pool is
     the nodes added by the previous step, [first_new, n); the mid drafter's pool is every

@@ -17,7 +17,7 @@ Sources (page title, then section):
   Logarithm:  log m = 2 artanh((m - 1)/(m + 1)) = 2 (s + s^3/3 + s^5/5 + ...), s = (m-1)/(m+1)
               (Abramowitz & Stegun 4.1.27), after splitting off the binary exponent.
 
-Readings where the pages are silent (each one is also listed in the design doc):
+Readings where the pages are silent:
   * The tree's proposals are deterministic (top-m children of a drafter, retrieved
     successors), i.e. point masses. Rejection sampling of point-mass proposals tries the
     children of the accepted node u in index order; child c is accepted with the residual

@@ -21,7 +21,7 @@ Sources (page title, then section):
               (non-destructive graft, then one global prune to Bver = 63), §五 (temperature
               0, D=5, W=10, m=10, Bver=63).
 
-Readings where the pages are silent (each one is also listed in the design doc):
+Readings where the pages are silent:
   * node 0 is the root (the current token); it counts among the N verified slots;
   * prune keeps the root plus the best nodes by (score desc, index asc); scores must
     not increase from parent to child (products of probabilities), otherwise the

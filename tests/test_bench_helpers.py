@@ -32,9 +32,16 @@ def test_roofline_bound_follows_the_measured_ridge():
         assert (bench.attn_flops(scn) / bench.attn_bytes(scn) > ridge) == tensor, cid
 
 
-def test_throughput_counts_every_rank():
-    assert bench.job_throughput(1, 200, 0.5) == 400.0
-    assert bench.job_throughput(4, 200, 0.5) == 1600.0
+def test_config_objects_describe_the_workload_only():
+    """Both arms print the same `config` for a workload: sizes and the L2 rotation, no
+    measured value."""
+    scn = make_scenario(3, V=1000, stream_len=5000)
+    c = bench.workload_config(scn, 3, 0.0)
+    assert c["workload"] == scn.name and c["config_id"] == 3 and c["slots"] == 60
+    assert c["step_bytes"] == bench.step_bytes(scn) and c["parallelism"] == "single GPU"
+    per_set, nsets = bench.rotation(scn)
+    assert per_set * nsets >= 4 * bench.L2_BYTES and nsets >= 2
+    assert not any("frac" in k for k in c)
 
 
 def test_reference_arm_line_carries_the_contract_keys():
@@ -49,7 +56,7 @@ def test_reference_arm_line_carries_the_contract_keys():
     assert line["impl"] == "reference"
     assert line["metric"] == bench.METRIC and line["unit"] == "steps/s"
     assert line["higher_is_better"] is True and line["steps"] >= 1 and line["value"] > 0
-    assert line["config"]["workload"] == bench.CONFIGS[1]["name"]
+    assert line["config"] == bench.workload_config(bench.make_scenario(1), 1, 0.0)
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1
     assert line["e2e"] == {"value": line["value"], "unit": "steps/s",

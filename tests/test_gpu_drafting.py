@@ -144,3 +144,37 @@ def test_drafting_errors_are_reported():
     with pytest.raises(gt.GTError):  # both pools given
         gt.gt_frontier_select(g.score, g.n, 2, ds.Nmax, g.first_new, g.visited, ds.W,
                               g.frontier, g.n_frontier, g.err)
+
+
+@pytest.mark.parametrize("mid", [False, True])
+def test_frontier_with_nan_signed_zeros_infinities_and_ties(mid):
+    """gt_frontier_select against the oracle on pools full of the values whose order the
+    rule fixes: NaN last (by index), +0.0 equal to -0.0, +-inf, ties to the smaller index."""
+    rng = np.random.default_rng(17 + mid)
+    B, N, W = 6, 1024, 64
+    specials = np.float32([float("nan"), -float("nan"), 0.0, -0.0, float("inf"),
+                           -float("inf"), 0.5, 0.25, 1e-30])
+    n = np.array([1, 5, 64, 300, 1000, 1024], np.int32)
+    score = np.where(rng.random((B, N)) < 0.5, rng.choice(specials, size=(B, N)),
+                     np.float32(rng.integers(-2, 3, size=(B, N)) / 8)).astype(np.float32)
+    lo = np.array([0, 2, 10, 0, 900, 1023], np.int32)
+    fr = torch.empty((B, W), dtype=torch.int32, device="cuda")
+    nfr = torch.empty(B, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for Wc in (1, 10, W):
+        vis = rng.integers(0, 2, size=(B, N)).astype(np.uint8)  # a fresh unvisited pool
+        dvis = _t(vis)
+        gt.gt_frontier_select(_t(score), _t(n), B, N, None if mid else _t(lo),
+                              dvis if mid else None, Wc, fr, nfr, err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        got, gn = _np(fr), _np(nfr)
+        for b in range(B):
+            if mid:
+                want, new_vis = frontier_select(score[b], int(n[b]), Wc, visited=vis[b].tolist())
+            else:
+                want, new_vis = frontier_select(score[b], int(n[b]), Wc, pool_lo=int(lo[b]))
+            assert gn[b] == len(want) and got[b, :gn[b]].tolist() == want, (b, Wc)
+            assert np.all(got[b, gn[b]:Wc] == -1)
+            if mid:
+                assert _np(dvis)[b].tolist() == new_vis

@@ -71,8 +71,9 @@ def test_step_parity_full_size(cid):
 
 
 def test_step_parity_full_size_batched():
+    """Workload 4 at full size: 16 requests, attention compared on every one of them."""
     scn = make_scenario(4)
-    _full_check(scn, reqs=[0, 7, 15])
+    _full_check(scn)
 
 
 def test_repeated_steps_keep_parity():
@@ -508,3 +509,109 @@ def test_tree_attn_two_cta_cluster_shapes():
                 e = float(np.abs(got[b, :n[b]] - refs[b]).max())
                 assert e <= TOL["bf16"], (B, N, Hq, Hkv, b, e)
                 assert np.all(got[b, n[b]:] == 0.0)
+
+
+def _random_attn_case(rng, B, N, Hq, Hkv, P, nn, dtype):
+    """Random trees and NaN-tailed caches for gt_tree_attn alone; returns the device
+    arguments and the oracle's output per request."""
+    from workload import f32_to_bf16_bits
+    d = 128
+    n = np.array(nn if nn else [N] * B, np.int32)
+    P = np.array(P, np.int32)
+    Lcap = int((P + N).max() + 64) // 64 * 64
+    parent = np.full((B, N), -1, np.int32)
+    for b in range(B):
+        parent[b, 1:n[b]] = [rng.integers(0, v) for v in range(1, n[b])]
+    mask = np.zeros((B, N, 1), np.uint64)
+    for b in range(B):
+        _, _, mask[b] = oracle.tree_mask(parent[b], int(n[b]), int(P[b]), N)
+    Q = rng.standard_normal((B, N, Hq, d), dtype=np.float32)
+    K = rng.standard_normal((B, Hkv, Lcap, d), dtype=np.float32)
+    Vv = rng.standard_normal((B, Hkv, Lcap, d), dtype=np.float32)
+    for b in range(B):
+        K[b, :, P[b] + n[b]:] = np.nan
+        Vv[b, :, P[b] + n[b]:] = np.nan
+    if dtype == "bf16":
+        hq, hk, hv = (f32_to_bf16_bits(x) for x in (Q, K, Vv))
+        dev = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).cuda() for x in (hq, hk, hv)]
+        dec, odt, gdt = oracle.bf16_to_f64, torch.bfloat16, gt.GT_BF16
+    else:
+        hq, hk, hv = Q, K, Vv
+        dev = [_t(x) for x in (Q, K, Vv)]
+        dec, odt, gdt = (lambda a: np.asarray(a, np.float64)), torch.float32, gt.GT_F32
+    scale = 1.0 / np.sqrt(d)
+    refs = []
+    for b in range(B):
+        L = int(P[b] + n[b])
+        refs.append(oracle.tree_attn(dec(hq[b]), dec(hk[b][:, :L]), dec(hv[b][:, :L]), parent[b],
+                                     int(n[b]), int(P[b]), scale))
+    args = dict(Q=dev[0], K=dev[1], V=dev[2], mask=_t(mask), P=_t(P), n=_t(n), B=B, N=N, Hq=Hq,
+                Hkv=Hkv, d=d, Lcap=Lcap, dt=gdt, scale=scale,
+                O=torch.full((B, N, Hq, d), float("nan"), dtype=odt, device="cuda"))
+    return args, refs, n
+
+
+def _check_attn_out(a, refs, n, dtype, tag):
+    got = a["O"].float().cpu().numpy().astype(np.float64)
+    for b in range(a["B"]):
+        e = float(np.abs(got[b, :n[b]] - refs[b]).max())
+        assert e <= TOL[dtype], (tag, b, e)
+        assert np.all(got[b, n[b]:] == 0.0)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_tree_attn_gqa_ratios_not_dividing_128(dtype):
+    """Query heads per KV head of 3, 5, 6, 7 and 12: a node's heads straddle the 128-row
+    M-tiles of the tcgen05 kernel (bf16), in clusters of two, three and four CTAs."""
+    rng = np.random.default_rng(41)
+    cases = [  # B, N, Hq, Hkv, prefixes, nodes per request (None: N)
+        (2, 60, 24, 8, [500, 129], [60, 31]),      # g = 3, 180 rows
+        (2, 50, 40, 8, [128, 1], [50, 9]),         # g = 5, 250 rows
+        (1, 64, 6, 1, [300], None),                # g = 6, 384 rows
+        (1, 64, 7, 1, [700], None),                # g = 7, 448 rows
+        (3, 20, 36, 3, [1000, 2, 64], [20, 1, 13]),  # g = 12, 240 rows
+        (2, 42, 12, 1, [260, 0], [42, 5]),         # g = 12, 504 rows
+    ]
+    for B, N, Hq, Hkv, P, nn in cases:
+        a, refs, n = _random_attn_case(rng, B, N, Hq, Hkv, P, nn, dtype)
+        wsb = gt.gt_tree_attn_workspace(B, N, Hq, Hkv, 128, a["Lcap"])
+        ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        gt.gt_tree_attn(a["Q"], a["K"], a["V"], a["mask"], a["P"], a["n"], B, N, Hq, Hkv, 128,
+                        a["Lcap"], a["dt"], a["scale"], a["O"], ws, wsb, err)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        _check_attn_out(a, refs, n, dtype, (B, N, Hq, Hkv))
+
+
+def test_tree_attn_refuses_memory_of_other_places():
+    """Q, K, V and O must be device memory of the current device: host-pinned and pageable
+    host arrays are refused on the host with GT_ERR_ARG and nothing is launched (the output
+    and the error word keep their contents)."""
+    rng = np.random.default_rng(5)
+    a, refs, n = _random_attn_case(rng, 1, 20, 8, 2, [300], None, "bf16")
+    wsb = gt.gt_tree_attn_workspace(1, 20, 8, 2, 128, a["Lcap"])
+    ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    # host arrays go in as raw addresses (the binding itself takes CUDA tensors only)
+    pinned_K = a["K"].cpu().pin_memory()
+    pageable_V = a["V"].cpu()
+    pinned_O = a["O"].cpu().pin_memory()
+    sentinel = a["O"].clone()
+    for name, q, k, v, o in (("K", a["Q"], pinned_K.data_ptr(), a["V"], a["O"]),
+                             ("V", a["Q"], a["K"], pageable_V.data_ptr(), a["O"]),
+                             ("O", a["Q"], a["K"], a["V"], pinned_O.data_ptr())):
+        with pytest.raises(gt.GTError) as ei:
+            gt.gt_tree_attn(q, k, v, a["mask"], a["P"], a["n"], 1, 20, 8, 2, 128, a["Lcap"],
+                            gt.GT_BF16, a["scale"], o, ws, wsb, err)
+        assert ei.value.status == gt.GT_ERR_ARG
+        assert name in gt.last_error() and "not device memory" in gt.last_error()
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert torch.equal(a["O"].isnan(), sentinel.isnan())  # untouched: still all NaN
+    # the same call on device memory runs and matches the oracle
+    gt.gt_tree_attn(a["Q"], a["K"], a["V"], a["mask"], a["P"], a["n"], 1, 20, 8, 2, 128,
+                    a["Lcap"], gt.GT_BF16, a["scale"], a["O"], ws, wsb, err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    _check_attn_out(a, refs, n, "bf16", "device memory")

@@ -1,11 +1,16 @@
-"""Two-rank host logic of bench.py on CPU (gloo): every rank runs its own replica, ranks
-meet only at barriers and at the max-over-ranks timing, and only rank 0 reports."""
+"""bench.py under a multi-process launch, on CPU: the GPU arm refuses to run on more than one
+GPU before touching CUDA, and the reference arm (the CPU oracle) runs on rank 0 alone while
+the other ranks exit without work."""
 import argparse
 import os
 import socket
+import subprocess
+import sys
 
 import pytest
 import torch.multiprocessing as mp
+
+from conftest import ROOT
 
 
 def _free_port() -> int:
@@ -21,18 +26,17 @@ def _rank_main(rank: int, world: int, port: int, out):
     dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank,
                             world_size=world, timeout=__import__("datetime").timedelta(seconds=60))
     try:
-        mine = 1.5 + 2.0 * rank                      # each rank's own time
-        slowest = bench.max_over_ranks(mine, dist, "cpu")
+        args = argparse.Namespace(config=1, steps=1, warmup=3, ref_budget=0.0, temperature=0.0,
+                                  seed=1)
+        ref = bench.run_reference(args, rank, world)
         dist.barrier()
-        args = argparse.Namespace(config=1, steps=1, warmup=3, ref_budget=0.0)
-        ref = bench.run_reference(args, rank, world) if rank != 0 else "rank0-skipped"
-        out.put((rank, slowest, ref))
+        out.put((rank, None if ref is None else ref["impl"]))
     finally:
         dist.destroy_process_group()
 
 
 @pytest.mark.timeout(120)
-def test_two_ranks_take_the_slowest_time_and_only_rank0_reports():
+def test_reference_arm_runs_on_rank0_only():
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
@@ -43,11 +47,19 @@ def test_two_ranks_take_the_slowest_time_and_only_rank0_reports():
     for p in procs:
         p.join(timeout=60)
         assert p.exitcode == 0
-    assert [r[1] for r in res] == [3.5, 3.5]        # max over ranks on every rank
-    assert res[1][2] is None                        # the reference arm: rank 1 does no work
+    assert res == [(0, "reference"), (1, None)]
 
 
-def test_single_process_helpers():
-    import bench
-    assert bench.max_over_ranks(2.0, None, "cpu") == 2.0
-    assert bench.job_throughput(4, 100, 0.5) == 800.0
+@pytest.mark.timeout(120)
+@pytest.mark.parametrize("env,argv", [({"WORLD_SIZE": "2", "RANK": "0"}, []),
+                                      ({"WORLD_SIZE": "2", "RANK": "1"}, []),
+                                      ({}, ["--gpus", "2"])])
+def test_gpu_arm_refuses_more_than_one_gpu(env, argv):
+    """Exit status 2 and a message, before any CUDA call: a poisoned CUDA_VISIBLE_DEVICES
+    and a missing library would make any later step fail differently."""
+    full = dict(os.environ, **env, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--steps", "1", *argv],
+                       capture_output=True, text=True, env=full, timeout=100)
+    assert r.returncode == 2, (r.returncode, r.stderr[-2000:])
+    assert "exactly one GPU" in r.stderr
+    assert r.stdout.strip() == ""

@@ -2,6 +2,7 @@
 selection routine, an independently written tree generator and a brute-force longest
 match."""
 import heapq
+import math
 
 import numpy as np
 
@@ -48,6 +49,55 @@ def test_frontier_matches_library_selection():
         pool = [v for v in range(n) if not vis[v]]
         assert front == heapq.nsmallest(W, pool, key=lambda v: (-score[v], v))
         assert nv[:n] == [1] * n and nv[n:] == vis[n:]
+
+
+def _better(score, u: int, v: int) -> bool:
+    """The frontier's order rule written out case by case: a number beats NaN; between two
+    numbers the larger wins (+0.0 and -0.0 are equal numbers) and a tie goes to the smaller
+    index; between two NaN the smaller index wins."""
+    a, b = float(np.float32(score[u])), float(np.float32(score[v]))
+    a_nan, b_nan = math.isnan(a), math.isnan(b)
+    if a_nan != b_nan:
+        return b_nan
+    if not a_nan and a != b:
+        return a > b
+    return u < v
+
+
+def _brute_frontier(score, pool, W):
+    """Frontier by counting, for each pool node, the pool nodes that beat it (its rank);
+    the nodes of rank < W, listed by rank."""
+    rank = {v: sum(_better(score, u, v) for u in pool if u != v) for v in pool}
+    return sorted((v for v in pool if rank[v] < W), key=lambda v: rank[v])
+
+
+def test_frontier_order_with_nan_signed_zeros_and_infinities():
+    """Hand example of the rule: +inf, 1.0, the two 0.5 by index, -0.0 and +0.0 by index
+    (equal numbers), then the NaN by index."""
+    nan, inf = float("nan"), float("inf")
+    score = np.float32([1.0, nan, 0.5, -0.0, 0.0, nan, inf, 0.5, -inf])
+    assert frontier_select(score, 9, 5, pool_lo=0)[0] == [6, 0, 2, 7, 3]
+    assert frontier_select(score, 9, 9, pool_lo=0)[0] == [6, 0, 2, 7, 3, 4, 8, 1, 5]
+    assert frontier_select(score, 9, 3, pool_lo=4)[0] == [6, 7, 4]
+    vis = [1, 0, 1, 0, 0, 1, 1, 0, 0]
+    assert frontier_select(score, 9, 4, visited=vis)[0] == [7, 3, 4, 8]
+
+
+def test_frontier_matches_pairwise_brute_force_on_special_values():
+    rng = np.random.default_rng(7)
+    specials = np.float32([float("nan"), -float("nan"), 0.0, -0.0, float("inf"),
+                           -float("inf"), 0.5, 0.5, 1e-30, -1e-30])
+    for _ in range(300):
+        n = int(rng.integers(1, 40))
+        score = np.where(rng.random(n) < 0.6, rng.choice(specials, size=n),
+                         np.float32(rng.integers(-3, 4, size=n) / 4)).astype(np.float32)
+        W = int(rng.integers(1, 12))
+        lo = int(rng.integers(0, n))
+        assert frontier_select(score, n, W, pool_lo=lo)[0] == \
+            _brute_frontier(score, list(range(lo, n)), W)
+        vis = rng.integers(0, 2, size=n).tolist()
+        assert frontier_select(score, n, W, visited=vis)[0] == \
+            _brute_frontier(score, [v for v in range(n) if not vis[v]], W)
 
 
 def test_replays_the_two_drafter_tree_generator():

@@ -1,12 +1,12 @@
 """gt_tree_attn_noalloc (attention with the library's static scratch) against gt_tree_attn
-with a caller workspace, on the same trees and caches: two calls in a row must each match
-within the attention tolerance. The file name sorts last so that the static scratch is also
-exercised after every other GPU test has run in the same process."""
+with a caller workspace and against the oracle, on the same trees and caches: two calls in a
+row must each match within the attention tolerance. The file name sorts last so that the
+static scratch is also exercised after every other GPU test has run in the same process."""
 import numpy as np
 import pytest
 import torch
 
-from parity_util import TOL, device_inputs, np_, oracle_tree, shape_of
+from parity_util import TOL, device_inputs, np_, oracle_attn, oracle_tree, shape_of
 from tree_speculative_decoding_parent_gb300 import gt
 from tree_speculative_decoding_parent_gb300.step import StepBuffers, run_attn, run_tree_build
 from workload import make_scenario
@@ -44,6 +44,7 @@ def test_noalloc_matches_workspace_entry_point(case):
     assert buf.err.item() == 0
     ref = buf.O.float().cpu().numpy()
     n = np_(buf.n_nodes)
+    want = [oracle_attn(scn, tree, b) for b in range(s.B)]
     for _ in range(2):
         O = torch.full_like(buf.O, float("nan"))
         _noalloc(buf, inp, s, scn.scale, O)
@@ -55,6 +56,8 @@ def test_noalloc_matches_workspace_entry_point(case):
             assert np.all(got[b, nb:] == 0.0)
             err = float(np.abs(got[b, :nb].astype(np.float64) - ref[b, :nb]).max())
             assert err <= TOL[scn.dtype], (case, b, err)
+            err = float(np.abs(got[b, :nb].astype(np.float64) - want[b]).max())
+            assert err <= TOL[scn.dtype], (case, "oracle", b, err)
 
 
 def test_noalloc_rejects_shapes_beyond_the_static_scratch():

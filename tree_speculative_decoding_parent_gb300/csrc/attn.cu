@@ -12,6 +12,9 @@
 // of mask[b][i] is set (u an ancestor of i, or i itself).
 #include <cuda_bf16.h>
 #include <math.h>
+#include <stdio.h>
+
+#include <atomic>
 
 #include "attn_common.cuh"
 #include "attn_tc.cuh"
@@ -21,7 +24,8 @@
 namespace gt {
 
 // ------------------------------------------------------------------------------------
-// FP32 SIMT kernel: CTA = (piece, group of 64 query rows); tiles of 64 keys in shared
+// FP32 SIMT kernel (fp32 inputs; bf16 always runs on the tcgen05 kernel): CTA = (piece,
+// group of 64 query rows); tiles of 64 keys in shared
 // memory; S = Q K^T by 4x4 register blocks, masked online softmax (expf), O by 4x8 blocks.
 // ------------------------------------------------------------------------------------
 constexpr int SIMT_ROWS = 64, SIMT_KEYS = 64, SIMT_LD = 68, SIMT_SLD = 65;
@@ -30,18 +34,11 @@ constexpr size_t SIMT_SMEM =
                      (size_t)SIMT_ROWS * SIMT_SLD + 3 * SIMT_ROWS);
 
 
-// Four consecutive elements as fp32 (16-byte fp32 or 8-byte bf16 loads; callers keep the
-// element index a multiple of 4 and the base 16-byte aligned).
+// Four consecutive fp32 elements (a 16-byte load; callers keep the element index a multiple
+// of 4 and the base 16-byte aligned).
 template <typename T> __device__ __forceinline__ float4 load4(const T *p);
 template <> __device__ __forceinline__ float4 load4<float>(const float *p) {
   return *reinterpret_cast<const float4 *>(p);
-}
-template <> __device__ __forceinline__ float4 load4<__nv_bfloat16>(const __nv_bfloat16 *p) {
-  const uint2 u = *reinterpret_cast<const uint2 *>(p);
-  const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&u.x);
-  const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162 *>(&u.y);
-  const float2 fa = __bfloat1622float2(a), fc = __bfloat1622float2(c);
-  return make_float4(fa.x, fa.y, fc.x, fc.y);
 }
 
 template <typename T>
@@ -303,20 +300,55 @@ attn_combine_kernel(const int32_t *__restrict__ n_nodes, int B, int N, int Hq, i
 }
 
 static int device_sms() {
-  static int cache[64] = {0};
+  static std::atomic<int> cache[64];  // per device; an SM count never changes
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     (void)cudaGetLastError();
     return 1024;  // conservative upper bound for the workspace size
   }
-  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  if (dev >= 0 && dev < 64) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
       sms <= 0) {
     (void)cudaGetLastError();
     return 1024;
   }
-  if (dev >= 0 && dev < 64) cache[dev] = sms;
+  if (dev >= 0 && dev < 64) cache[dev].store(sms, std::memory_order_relaxed);
   return sms;
+}
+
+// An array of `bytes` bytes at p must lie in device memory of device `dev` (a cudaMalloc-
+// family allocation made there): the first and the last byte are looked up. The bf16
+// kernel streams K and V through cluster-multicast TMA loads, which this library issues
+// only over the memory of the GPU that runs the kernel, never over host, managed or peer
+// memory; the same rule holds for every array of the call. Returns GT_ERR_ARG, with the
+// detail for gt_last_error, otherwise.
+static int check_own_device(const void *p, size_t bytes, int dev, const char *name) {
+  const char *ends[2] = {static_cast<const char *>(p), static_cast<const char *>(p) + bytes - 1};
+  for (const char *q : ends) {
+    cudaPointerAttributes a{};
+    const cudaError_t e = cudaPointerGetAttributes(&a, q);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();
+      char msg[160];
+      snprintf(msg, sizeof(msg), "gt_tree_attn: %s: cudaPointerGetAttributes: %s", name,
+               cudaGetErrorString(e));
+      note_message(msg);
+      return GT_ERR_ARG;
+    }
+    if (a.type != cudaMemoryTypeDevice || a.device != dev) {
+      char msg[160];
+      snprintf(msg, sizeof(msg),
+               "gt_tree_attn: %s is not device memory of the current device %d (memory type "
+               "%d, device %d)",
+               name, dev, (int)a.type, a.device);
+      note_message(msg);
+      return GT_ERR_ARG;
+    }
+  }
+  return GT_OK;
 }
 
 static bool attn_args_ok(int B, int N, int Hq, int Hkv, int d, int Lcap) {
@@ -351,6 +383,18 @@ GT_API int gt_tree_attn(const void *Q, const void *K, const void *V, const uint6
   if ((uintptr_t)workspace & 255) return GT_ERR_ARG;
   const int S = B * Hkv;
   if (S > 8192) return GT_ERR_SHAPE;
+  {
+    int dev = 0;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return launch_status(e, "cudaGetDevice");
+    const size_t es = dtype == GT_BF16 ? 2 : 4;
+    const size_t qo = (size_t)B * N * Hq * d * es, kv = (size_t)B * Hkv * Lcap * d * es;
+    int rc = check_own_device(Q, qo, dev, "Q");
+    if (rc == GT_OK) rc = check_own_device(K, kv, dev, "K");
+    if (rc == GT_OK) rc = check_own_device(V, kv, dev, "V");
+    if (rc == GT_OK) rc = check_own_device(O, qo, dev, "O");
+    if (rc != GT_OK) return rc;
+  }
   const int g = Hq / Hkv;
   const int rows_pad = ceil_div(g * N, ATTN_ROWS_PAD) * ATTN_ROWS_PAD;
   const int G = device_sms();
@@ -359,7 +403,9 @@ GT_API int gt_tree_attn(const void *Q, const void *K, const void *V, const uint6
   if (ws_bytes < need) return GT_ERR_ARG;
   cudaStream_t s = (cudaStream_t)stream;
 
-  const bool tc = (dtype == GT_BF16) && attn_tc_supported(g, N);
+  // bf16 runs on the tcgen05 kernel for every supported shape, fp32 on the SIMT kernel
+  const bool tc = dtype == GT_BF16;
+  if (tc && !attn_tc_supported(g, N)) return GT_ERR_SHAPE;
   const int TK = tc ? ATTN_TC_KEYS : SIMT_KEYS;
   // the tcgen05 kernel runs one cluster per piece: aim for one wave of clusters
   const int Gs = tc ? attn_tc_pieces(g, N) : G;
@@ -371,7 +417,7 @@ GT_API int gt_tree_attn(const void *Q, const void *K, const void *V, const uint6
   int rc;
   if (tc) {
     rc = attn_tc_launch(Q, K, V, mask, sa, B, N, Hq, Hkv, Lcap, scale, ws, grid_pieces, err, s);
-  } else if (dtype == GT_F32) {
+  } else {
     static SmemAttr attr_f32;
     rc = ensure_smem(attn_simt_kernel<float>, (int)SIMT_SMEM, attr_f32,
                      "cudaFuncSetAttribute(attn_simt_kernel)");
@@ -379,15 +425,6 @@ GT_API int gt_tree_attn(const void *Q, const void *K, const void *V, const uint6
     rc = launch(attn_simt_kernel<float>, dim3(grid_pieces, ceil_div(g * N, SIMT_ROWS)), dim3(256),
                 SIMT_SMEM, s, (const float *)Q, (const float *)K, (const float *)V, mask,
                 prefix_len, n_nodes, N, Hq, Hkv, Lcap, scale, sa, ws, err);
-  } else {
-    static SmemAttr attr_bf16;
-    rc = ensure_smem(attn_simt_kernel<__nv_bfloat16>, (int)SIMT_SMEM, attr_bf16,
-                     "cudaFuncSetAttribute(attn_simt_kernel)");
-    if (rc != GT_OK) return rc;
-    rc = launch(attn_simt_kernel<__nv_bfloat16>, dim3(grid_pieces, ceil_div(g * N, SIMT_ROWS)),
-                dim3(256), SIMT_SMEM, s, (const __nv_bfloat16 *)Q, (const __nv_bfloat16 *)K,
-                (const __nv_bfloat16 *)V, mask, prefix_len, n_nodes, N, Hq, Hkv, Lcap, scale,
-                sa, ws, err);
   }
   if (rc != GT_OK) return rc;
   const int warps = B * N * Hq;

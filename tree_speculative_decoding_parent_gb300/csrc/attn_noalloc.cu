@@ -2,11 +2,17 @@
 // array that this library owns, so that the caller allocates nothing.
 //
 // The scratch is one file-scope device array of GT_ATTN_NOALLOC_SCRATCH_BYTES. Each device
-// gets its own copy of it when the module loads there. Its device address is looked up
-// once per device, with that device current, on the first call made on that device, and
-// cached. The array sits in its own translation unit, so a program that never calls this
-// entry point never references it.
+// gets its own copy of it when the library's module is loaded there. Under lazy module
+// loading (the CUDA default) that happens on the first use of any kernel of this library on
+// the device; under CUDA_MODULE_LOADING=EAGER it happens when a context is created. Either
+// way every device that loads the module holds the 32 MiB until the process exits, whether
+// or not this entry point is ever called.
+//
+// Its device address is looked up with that device current, on the first call made in each
+// context, and cached with the context's id: after cudaDeviceReset the next call sees a new
+// context and looks the address up again instead of passing a dead one.
 #include <atomic>
+#include <mutex>
 #include <stdio.h>
 
 #include "gt_internal.cuh"
@@ -16,9 +22,14 @@ namespace gt {
 static __device__ __align__(256) unsigned char g_attn_scratch[GT_ATTN_NOALLOC_SCRATCH_BYTES];
 
 constexpr int NOALLOC_MAX_DEVICES = 64;
-static std::atomic<uintptr_t> g_scratch_addr[NOALLOC_MAX_DEVICES];
+struct ScratchRecord {
+  uint64_t ctx = 0;  // current_context_id() of the context the address belongs to
+  uintptr_t addr = 0;
+};
+static ScratchRecord g_scratch[NOALLOC_MAX_DEVICES];
+static std::mutex g_scratch_mu;
 
-// Device address of this device's copy of the scratch array (0 on failure, with the
+// Device address of this context's copy of the scratch array (0 on failure, with the
 // detail recorded for gt_last_error).
 static uintptr_t scratch_address() {
   int dev = 0;
@@ -31,8 +42,9 @@ static uintptr_t scratch_address() {
     note_message("gt_tree_attn_noalloc: device ordinal above 63");
     return 0;
   }
-  uintptr_t a = g_scratch_addr[dev].load(std::memory_order_acquire);
-  if (a) return a;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  const uint64_t ctx = current_context_id();
+  if (ctx != 0 && g_scratch[dev].ctx == ctx) return g_scratch[dev].addr;
   void *ptr = nullptr;
   e = cudaGetSymbolAddress(&ptr, g_attn_scratch);
   if (e != cudaSuccess) {
@@ -43,10 +55,10 @@ static uintptr_t scratch_address() {
     note_message("gt_tree_attn_noalloc: cudaGetSymbolAddress(scratch) gave a null address");
     return 0;
   }
-  a = reinterpret_cast<uintptr_t>(ptr);
-  // a racing first call on the same device finds the same address: either store is right
-  g_scratch_addr[dev].store(a, std::memory_order_release);
-  return a;
+  // the look-up creates the context when there was none: key the record on it
+  g_scratch[dev].ctx = current_context_id();
+  g_scratch[dev].addr = reinterpret_cast<uintptr_t>(ptr);
+  return g_scratch[dev].addr;
 }
 
 }  // namespace gt

@@ -48,6 +48,8 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <atomic>
+
 #include "attn_tc.cuh"
 #include "gt_internal.cuh"
 #include "launch.cuh"
@@ -588,14 +590,19 @@ attn_tc_kernel(const __nv_bfloat16 *__restrict__ Qg, const __grid_constant__ CUt
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> cached{nullptr};
+  PFN_cuTensorMapEncodeTiled_v12000 fn = cached.load(std::memory_order_acquire);
   if (!fn) {
     cudaDriverEntryPointQueryResult q;
     void *f = nullptr;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
+        q == cudaDriverEntryPointSuccess) {
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+      cached.store(fn, std::memory_order_release);  // racing callers find the same pointer
+    } else {
+      (void)cudaGetLastError();
+    }
   }
   return fn;
 }
@@ -621,7 +628,9 @@ bool set_attributes() {
 }  // namespace
 
 bool attn_tc_supported(int g, int N) {
-  return g >= 1 && g <= 128 && (128 % g) == 0 && g * N <= 128 * MAX_CLUSTER;
+  // rows are placed one by one (r = node * g + head-in-group), so a node's g heads may
+  // straddle two CTAs of the cluster: any g works up to four 128-row M-tiles
+  return g >= 1 && N >= 1 && g * N <= 128 * MAX_CLUSTER;
 }
 
 int attn_tc_pieces(int g, int N) {
@@ -631,8 +640,9 @@ int attn_tc_pieces(int g, int N) {
     (void)cudaGetLastError();
     return 1;
   }
-  static int cache[64][MAX_CLUSTER + 1] = {};
-  if (cache[dev][C] > 0) return cache[dev][C];
+  static std::atomic<int> cache[64][MAX_CLUSTER + 1];  // zero-initialised (static)
+  const int hit = cache[dev][C].load(std::memory_order_relaxed);
+  if (hit > 0) return hit;
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
     (void)cudaGetLastError();
@@ -657,8 +667,9 @@ int attn_tc_pieces(int g, int N) {
     else
       (void)cudaGetLastError();
   }
-  cache[dev][C] = clusters > 0 ? clusters : 1;
-  return cache[dev][C];
+  if (clusters < 1) clusters = 1;
+  cache[dev][C].store(clusters, std::memory_order_relaxed);
+  return clusters;
 }
 
 int attn_tc_launch(const void *Q, const void *K, const void *V, const uint64_t *mask,

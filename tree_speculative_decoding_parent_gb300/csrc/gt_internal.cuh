@@ -43,11 +43,19 @@ static inline int launch_status(cudaError_t e, const char *what = "kernel launch
   return GT_OK;
 }
 
+// Identity of the calling thread's current CUDA context (cuCtxGetId: unique over the
+// process's lifetime, so the context that replaces one destroyed by cudaDeviceReset gets a
+// new value), or 0 when there is none yet or it cannot be read. Per-device caches of state
+// that lives in a context (function attributes, symbol addresses) are keyed on it.
+uint64_t current_context_id();
+
 // Raises a kernel's dynamic shared-memory limit to at least `bytes` on the current device.
-// The runtime keeps the attribute per device, so each call site remembers, per device, the
-// largest limit it has set (a static SmemAttr); repeated calls then cost no driver call.
+// The runtime keeps the attribute per context, so each call site remembers, per device, the
+// context it set the limit in and the largest limit set there (a static SmemAttr: one word
+// per device, context id in the high 40 bits, bytes in the low 24); repeated calls in the
+// same context then cost no attribute call.
 struct SmemAttr {
-  std::atomic<int> bytes[64];  // zero-initialised when declared static
+  std::atomic<uint64_t> state[64];  // zero-initialised when declared static
 };
 template <typename Kernel>
 static inline int ensure_smem(Kernel kernel, int bytes, SmemAttr &a, const char *what) {
@@ -55,13 +63,23 @@ static inline int ensure_smem(Kernel kernel, int bytes, SmemAttr &a, const char 
   const cudaError_t ge = cudaGetDevice(&dev);
   if (ge != cudaSuccess) return launch_status(ge, "cudaGetDevice");
   const bool cached = dev >= 0 && dev < 64;
-  if (cached && a.bytes[dev].load(std::memory_order_relaxed) >= bytes) return GT_OK;
+  const uint64_t ctx = current_context_id();
+  const bool keyed = ctx != 0 && ctx < (1ull << 40);
+  if (cached && keyed) {
+    const uint64_t st = a.state[dev].load(std::memory_order_relaxed);
+    if ((st >> 24) == ctx && (int)(st & 0xFFFFFFu) >= bytes) return GT_OK;
+  }
   const cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return launch_status(e, what);
-  if (cached) {
-    int cur = a.bytes[dev].load(std::memory_order_relaxed);
-    while (cur < bytes && !a.bytes[dev].compare_exchange_weak(cur, bytes)) {
+  // the attribute call created the context if there was none: key the record on it
+  const uint64_t ctx_now = current_context_id();
+  if (cached && ctx_now != 0 && ctx_now < (1ull << 40) && bytes < (1 << 24)) {
+    const uint64_t want = (ctx_now << 24) | (uint64_t)bytes;
+    uint64_t cur = a.state[dev].load(std::memory_order_relaxed);
+    // keep the larger limit of the same context; a record of another context is replaced
+    while (!((cur >> 24) == ctx_now && (cur & 0xFFFFFFu) >= (uint64_t)bytes) &&
+           !a.state[dev].compare_exchange_weak(cur, want)) {
     }
   }
   return GT_OK;

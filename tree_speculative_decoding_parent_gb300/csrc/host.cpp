@@ -4,9 +4,12 @@
 // Source: "浙江大学、阿里巴巴联手破解AI推理瓶颈" §二 (prune stages 0/1/5 keep 8/24/40 draft nodes
 // and refill 52/36/20 of 60 slots from the successor table; the template is asymmetric:
 // higher-ranked successors get more children and go deeper).
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <stdio.h>
+
+#include <atomic>
 
 #include <queue>
 #include <map>
@@ -94,6 +97,38 @@ GT_API int gt_event_record_external(void *event, gt_stream_t stream) {
 }
 
 namespace gt {
+
+namespace {
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+std::atomic<void *> g_ctx_get_current{nullptr}, g_ctx_get_id{nullptr};
+
+void *driver_entry(const char *name, unsigned version, std::atomic<void *> &slot) {
+  void *f = slot.load(std::memory_order_acquire);
+  if (f) return f;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &f, version, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  slot.store(f, std::memory_order_release);  // every racing caller finds the same pointer
+  return f;
+}
+}  // namespace
+
+uint64_t current_context_id() {
+  auto get_cur = reinterpret_cast<CtxGetCurrentFn>(
+      driver_entry("cuCtxGetCurrent", 4000, g_ctx_get_current));
+  auto get_id = reinterpret_cast<CtxGetIdFn>(driver_entry("cuCtxGetId", 12000, g_ctx_get_id));
+  if (!get_cur || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  if (get_cur(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  unsigned long long id = 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return (uint64_t)id + 1;  // 0 stays "no context"
+}
+
 static thread_local char last_error[256];
 void note_error(const char *what, cudaError_t e) {
   snprintf(last_error, sizeof(last_error), "%s: %s", what,
