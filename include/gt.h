@@ -58,7 +58,11 @@ typedef enum {
   GT_ERR_TREE = -4,         /* device: not a rooted topological tree, id out of range   */
   GT_ERR_NONMONOTONE = -5,  /* device: a node's score exceeds its parent's, or is NaN   */
   GT_ERR_TIMEOUT = -6,      /* device: a bounded wait gave up                           */
-  GT_ERR_RANGE = -7         /* device: a stored count exceeds its buffer                */
+  GT_ERR_RANGE = -7,        /* device: a stored count exceeds its buffer                */
+  GT_ERR_IO = -8,           /* host: a file cannot be opened, read or written, or its    */
+                            /* length differs from what its header states               */
+  GT_ERR_CORRUPT = -9,      /* host: a file's magic, checksum or contents are invalid    */
+  GT_ERR_VALUE = -10        /* device, checked builds only: a NaN where a number belongs */
 } gt_status;
 
 typedef enum { GT_F32 = 0, GT_BF16 = 1 } gt_dtype;
@@ -398,6 +402,30 @@ int gt_tree_attach(int32_t *parent, int32_t *tokens, float *score, int32_t *n_no
                    int Nmax, const int32_t *frontier, const int32_t *n_frontier, int W,
                    const int32_t *child_id, const float *child_p, int m, int V,
                    int32_t *first_new, int32_t *err, gt_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Successor-table files.  [Graft] §六 (the table warmed up in earlier runs is a prior that
+ *     carries over to later ones: 0.37 MB after 5 warm-up rounds, 2.32 MB after 50).
+ *
+ * Host pointers, synchronous, no CUDA calls: copy a device table to the host before saving
+ * and back after loading. File layout (little-endian): magic "GTSUCC" 0x00 0x01; uint32 V;
+ * uint32 k; uint64 payload bytes (4 V k); uint32 CRC-32 of the payload; uint32 CRC-32 of
+ * the 28 header bytes before it; then the table, int32 [V][k] row-major. CRC-32 is the
+ * IEEE 802.3 checksum (reflected polynomial 0xEDB88320, initial value and final XOR
+ * 0xFFFFFFFF).
+ * gt_succ_save: writes table (host i32 [V][k], entries in [-1, V)) to path, through a
+ *   temporary file "<path>.tmp" renamed over path, so path never names a partial file.
+ *   Errors: GT_ERR_ARG (null, V or k < 1, an entry outside [-1, V)), GT_ERR_IO.
+ * gt_succ_file_shape: V and k of the file at path (header checked, payload not read).
+ *   Errors: GT_ERR_ARG, GT_ERR_IO (missing or shorter than a header), GT_ERR_CORRUPT.
+ * gt_succ_load: reads the file into table (host i32 [V][k]). The table changes only when
+ *   every check passes. Errors: GT_ERR_ARG, GT_ERR_IO (missing, shorter or longer than its
+ *   header states), GT_ERR_SHAPE (the file's V or k differ from the arguments),
+ *   GT_ERR_CORRUPT (magic, a checksum, or an entry outside [-1, V)).
+ * ------------------------------------------------------------------------------------- */
+int gt_succ_save(const char *path, const int32_t *table, int V, int k);
+int gt_succ_file_shape(const char *path, int32_t *V, int32_t *k);
+int gt_succ_load(const char *path, int32_t *table, int V, int k);
 
 /* ---------------------------------------------------------------------------------------
  * Host helpers (host pointers, synchronous, no CUDA calls).

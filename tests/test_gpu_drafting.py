@@ -158,10 +158,10 @@ def test_frontier_with_nan_signed_zeros_infinities_and_ties(mid):
     score = np.where(rng.random((B, N)) < 0.5, rng.choice(specials, size=(B, N)),
                      np.float32(rng.integers(-2, 3, size=(B, N)) / 8)).astype(np.float32)
     lo = np.array([0, 2, 10, 0, 900, 1023], np.int32)
-    fr = torch.empty((B, W), dtype=torch.int32, device="cuda")
     nfr = torch.empty(B, dtype=torch.int32, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     for Wc in (1, 10, W):
+        fr = torch.empty((B, Wc), dtype=torch.int32, device="cuda")  # [B][W] of this call
         vis = rng.integers(0, 2, size=(B, N)).astype(np.uint8)  # a fresh unvisited pool
         dvis = _t(vis)
         gt.gt_frontier_select(_t(score), _t(n), B, N, None if mid else _t(lo),

@@ -94,7 +94,12 @@ attn_simt_kernel(const T *__restrict__ Q, const T *__restrict__ K, const T *__re
   }
   if (tid < SIMT_ROWS) {
     const int r = r0 + tid;
-    s_mask[tid] = r < g * n ? mask[(size_t)b * N + r / g] : 0ull;
+    const uint64_t mrow = r < g * n ? mask[(size_t)b * N + r / g] : 0ull;
+    s_mask[tid] = mrow;
+    // checked builds: a tree row's mask holds the root and the node itself, no node past n
+    GT_CHECKED(r >= g * n || (((mrow >> (r / g)) & 1ull) && (mrow & 1ull) &&
+                              (n >= 64 || (mrow >> n) == 0ull)),
+               err, GT_ERR_TREE);
   }
 
   const int ty = tid >> 4, tx = tid & 15;   // S / PV blocking
@@ -373,6 +378,7 @@ GT_API int gt_tree_attn(const void *Q, const void *K, const void *V, const uint6
                         const int32_t *prefix_len, const int32_t *n_nodes, int B, int N, int Hq,
                         int Hkv, int d, int Lcap, int dtype, float scale, void *O,
                         void *workspace, size_t ws_bytes, int32_t *err, gt_stream_t stream) {
+  GT_TRACE("gt_tree_attn");
   if (!attn_args_ok(B, N, Hq, Hkv, d, Lcap)) return GT_ERR_ARG;
   if (dtype != GT_F32 && dtype != GT_BF16) return GT_ERR_ARG;
   if (!(scale > 0.f) || isinf(scale)) return GT_ERR_ARG;

@@ -70,6 +70,7 @@ GT_API int gt_tree_attn_noalloc(const void *Q, const void *K, const void *V,
                                 const int32_t *n_nodes, int B, int N, int Hq, int Hkv, int d,
                                 int Lcap, int dtype, float scale, void *O, int32_t *err,
                                 gt_stream_t stream) {
+  GT_TRACE("gt_tree_attn_noalloc");
   const size_t need = gt_tree_attn_workspace(B, N, Hq, Hkv, d, Lcap);
   if (need == 0) {  // an invalid shape: gt_tree_attn reports which error, launching nothing
     return gt_tree_attn(Q, K, V, mask, prefix_len, n_nodes, B, N, Hq, Hkv, d, Lcap, dtype,

@@ -502,6 +502,10 @@ attn_tc_kernel(const __nv_bfloat16 *__restrict__ Qg, const __grid_constant__ CUt
     const int rl = warp * 32 + lane;                // row within the M-tile = TMEM lane
     const int r = row0 + rl;                        // row within the segment
     const uint64_t mrow = r < g * n ? mask[(size_t)b * N + r / g] : 0ull;
+    // checked builds: a tree row's mask holds the root and the node itself, no node past n
+    GT_CHECKED(r >= g * n || (((mrow >> (r / g)) & 1ull) && (mrow & 1ull) &&
+                              (n >= 64 || (mrow >> n) == 0ull)),
+               err, GT_ERR_TREE);
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const uint32_t tO = tmem + lane_base + O_COL;
     const float sl2 = scale * LOG2E;  // scale > 0: the max of raw scores gives the max

@@ -220,6 +220,7 @@ using namespace gt;
 GT_API int gt_frontier_select(const float *score, const int32_t *n_nodes, int B, int Nmax,
                               const int32_t *pool_lo, uint8_t *visited, int W, int32_t *frontier,
                               int32_t *n_frontier, int32_t *err, gt_stream_t stream) {
+  GT_TRACE("gt_frontier_select");
   if (B < 0 || Nmax < 1 || W < 1) return GT_ERR_ARG;
   if (Nmax > 1024 || W > DRAFT_MAX_W) return GT_ERR_SHAPE;
   if (B == 0) return GT_OK;
@@ -234,6 +235,7 @@ GT_API int gt_ngram_draft(const int32_t *hist, const int32_t *hist_len, int B, i
                           int Nmax, const int32_t *frontier, const int32_t *n_frontier, int W,
                           int q_max, int32_t *child_id, float *child_p, int32_t *match,
                           int32_t *err, gt_stream_t stream) {
+  GT_TRACE("gt_ngram_draft");
   if (B < 0 || Lh < 0 || m < 1 || Nmax < 1 || W < 1 || q_max < 1) return GT_ERR_ARG;
   if (Nmax > 1024 || W > DRAFT_MAX_W || m > DRAFT_MAX_M || q_max > DRAFT_MAX_Q || B > 65535)
     return GT_ERR_SHAPE;
@@ -269,6 +271,7 @@ GT_API int gt_tree_attach(int32_t *parent, int32_t *tokens, float *score, int32_
                           int B, int Nmax, const int32_t *frontier, const int32_t *n_frontier,
                           int W, const int32_t *child_id, const float *child_p, int m, int V,
                           int32_t *first_new, int32_t *err, gt_stream_t stream) {
+  GT_TRACE("gt_tree_attach");
   if (B < 0 || Nmax < 1 || W < 1 || m < 1 || V < 1) return GT_ERR_ARG;
   if (Nmax > 1024 || W > DRAFT_MAX_W || m > DRAFT_MAX_M || W * m > 1024) return GT_ERR_SHAPE;
   if (B == 0) return GT_OK;

@@ -6,16 +6,43 @@
 
 #include <atomic>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "gt.h"
 
 #define GT_API extern "C" __attribute__((visibility("default")))
 
+// Checked builds (compiled with -DGT_CHECK=1 into libgt_check.so) add device-side checks of
+// what the method assumes of its inputs but the kernels do not need for memory safety. A
+// failed check writes its code into *err, as any data error does, and the kernel carries
+// on; nothing traps.
+#ifndef GT_CHECK
+#define GT_CHECK 0
+#endif
+
 namespace gt {
+
+// A named NVTX range over one C-ABI call on the calling host thread, so that profilers
+// attribute the kernels the call launches to it (ncu --nvtx --nvtx-include "gt_tree_attn/").
+// Without a tool attached a push or pop is a call through an unset hook.
+struct NvtxRange {
+  explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange &) = delete;
+  NvtxRange &operator=(const NvtxRange &) = delete;
+};
+#define GT_TRACE(name) ::gt::NvtxRange gt_trace_range_(name)
 
 // First device-side error wins; later ones are dropped.
 __device__ __forceinline__ void set_err(int32_t *err, int code) {
   if (err != nullptr) atomicCAS(reinterpret_cast<int *>(err), 0, code);
 }
+
+// A check of checked builds: reports `code` when cond is false; compiled out otherwise.
+#define GT_CHECKED(cond, err, code)                      \
+  do {                                                   \
+    if (GT_CHECK && !(cond)) ::gt::set_err((err), (code)); \
+  } while (0)
 
 __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 

@@ -1,5 +1,5 @@
-// Host-side helpers of libgt: stage budget, default retrieval template, status strings,
-// and an external event record for timing inside captured CUDA graphs.
+// Host-side helpers of libgt: stage budget, default retrieval template, successor-table
+// files, status strings, and an external event record for timing inside captured CUDA graphs.
 //
 // Source: "浙江大学、阿里巴巴联手破解AI推理瓶颈" §二 (prune stages 0/1/5 keep 8/24/40 draft nodes
 // and refill 52/36/20 of 60 slots from the successor table; the template is asymmetric:
@@ -8,11 +8,12 @@
 #include <cuda_runtime.h>
 
 #include <stdio.h>
+#include <string.h>
 
 #include <atomic>
-
-#include <queue>
 #include <map>
+#include <queue>
+#include <string>
 #include <tuple>
 #include <vector>
 
@@ -72,6 +73,134 @@ GT_API int gt_default_template(int T, int k, int max_depth, int32_t *tpar, int32
   return t == T ? GT_OK : GT_ERR_SHAPE;
 }
 
+// ------------------------------------------------------------------------------------
+// Successor-table persistence ([Graft] §六: the table warmed up in earlier runs is a prior
+// that carries over to later ones). File layout, little-endian:
+//   [0, 8)   magic "GTSUCC" 0x00 0x01 (format 1)
+//   [8, 12)  uint32 V        [12, 16) uint32 k        [16, 24) uint64 payload bytes = 4 V k
+//   [24, 28) uint32 CRC-32 of the payload   [28, 32) uint32 CRC-32 of bytes [0, 28)
+//   [32, ..) the table, int32 [V][k] row-major
+// CRC-32 is the IEEE 802.3 checksum (reflected polynomial 0xEDB88320, initial value and final
+// XOR 0xFFFFFFFF), computed bit by bit from its definition.
+// ------------------------------------------------------------------------------------
+namespace {
+constexpr unsigned char SUCC_MAGIC[8] = {'G', 'T', 'S', 'U', 'C', 'C', 0, 1};
+constexpr size_t SUCC_HDR = 32;
+
+uint32_t crc32_update(uint32_t crc, const unsigned char *p, size_t n) {
+  for (size_t i = 0; i < n; ++i) {
+    crc ^= p[i];
+    for (int b = 0; b < 8; ++b) crc = (crc >> 1) ^ (0xEDB88320u & (0u - (crc & 1u)));
+  }
+  return crc;
+}
+uint32_t crc32_of(const unsigned char *p, size_t n) {
+  return crc32_update(0xFFFFFFFFu, p, n) ^ 0xFFFFFFFFu;
+}
+void put_u32(unsigned char *p, uint32_t v) {
+  for (int i = 0; i < 4; ++i) p[i] = (unsigned char)(v >> (8 * i));
+}
+void put_u64(unsigned char *p, uint64_t v) {
+  for (int i = 0; i < 8; ++i) p[i] = (unsigned char)(v >> (8 * i));
+}
+uint32_t get_u32(const unsigned char *p) {
+  uint32_t v = 0;
+  for (int i = 0; i < 4; ++i) v |= (uint32_t)p[i] << (8 * i);
+  return v;
+}
+uint64_t get_u64(const unsigned char *p) {
+  uint64_t v = 0;
+  for (int i = 0; i < 8; ++i) v |= (uint64_t)p[i] << (8 * i);
+  return v;
+}
+// The table as little-endian bytes (int32 two's complement), independent of the host order.
+std::vector<unsigned char> table_bytes(const int32_t *t, size_t n) {
+  std::vector<unsigned char> out(4 * n);
+  for (size_t i = 0; i < n; ++i) put_u32(&out[4 * i], (uint32_t)t[i]);
+  return out;
+}
+
+// Reads and validates the header; on success *V, *k and *crc hold its fields.
+int read_header(FILE *f, uint32_t *V, uint32_t *k, uint32_t *crc) {
+  unsigned char h[SUCC_HDR];
+  if (fread(h, 1, SUCC_HDR, f) != SUCC_HDR) return GT_ERR_IO;
+  if (memcmp(h, SUCC_MAGIC, 8) != 0 || get_u32(h + 28) != crc32_of(h, 28)) return GT_ERR_CORRUPT;
+  *V = get_u32(h + 8);
+  *k = get_u32(h + 12);
+  if (*V < 1 || *k < 1 || *V > 0x7FFFFFFFu || *k > 0x7FFFFFFFu ||
+      get_u64(h + 16) != 4ull * (uint64_t)*V * (uint64_t)*k)
+    return GT_ERR_CORRUPT;
+  *crc = get_u32(h + 24);
+  return GT_OK;
+}
+}  // namespace
+
+GT_API int gt_succ_save(const char *path, const int32_t *table, int V, int k) {
+  if (!path || !table || V < 1 || k < 1) return GT_ERR_ARG;
+  const size_t n = (size_t)V * (size_t)k;
+  for (size_t i = 0; i < n; ++i)
+    if (table[i] < -1 || table[i] >= V) return GT_ERR_ARG;
+  const std::vector<unsigned char> body = table_bytes(table, n);
+  unsigned char h[SUCC_HDR];
+  memcpy(h, SUCC_MAGIC, 8);
+  put_u32(h + 8, (uint32_t)V);
+  put_u32(h + 12, (uint32_t)k);
+  put_u64(h + 16, 4ull * n);
+  put_u32(h + 24, crc32_of(body.data(), body.size()));
+  put_u32(h + 28, crc32_of(h, 28));
+  // written under a temporary name and renamed, so the path never names a partial file
+  std::string tmp = std::string(path) + ".tmp";
+  FILE *f = fopen(tmp.c_str(), "wb");
+  if (!f) return GT_ERR_IO;
+  bool ok = fwrite(h, 1, SUCC_HDR, f) == SUCC_HDR && fwrite(body.data(), 1, body.size(), f) == body.size();
+  ok = (fclose(f) == 0) && ok;
+  if (!ok || rename(tmp.c_str(), path) != 0) {
+    remove(tmp.c_str());
+    return GT_ERR_IO;
+  }
+  return GT_OK;
+}
+
+GT_API int gt_succ_file_shape(const char *path, int32_t *V, int32_t *k) {
+  if (!path || !V || !k) return GT_ERR_ARG;
+  FILE *f = fopen(path, "rb");
+  if (!f) return GT_ERR_IO;
+  uint32_t v = 0, kk = 0, crc = 0;
+  const int rc = read_header(f, &v, &kk, &crc);
+  fclose(f);
+  if (rc != GT_OK) return rc;
+  *V = (int32_t)v;
+  *k = (int32_t)kk;
+  return GT_OK;
+}
+
+GT_API int gt_succ_load(const char *path, int32_t *table, int V, int k) {
+  if (!path || !table || V < 1 || k < 1) return GT_ERR_ARG;
+  FILE *f = fopen(path, "rb");
+  if (!f) return GT_ERR_IO;
+  uint32_t fv = 0, fk = 0, crc = 0;
+  int rc = read_header(f, &fv, &fk, &crc);
+  if (rc == GT_OK && (fv != (uint32_t)V || fk != (uint32_t)k)) rc = GT_ERR_SHAPE;
+  const size_t n = (size_t)V * (size_t)k;
+  std::vector<unsigned char> body;
+  if (rc == GT_OK) {
+    body.resize(4 * n);
+    unsigned char extra;
+    if (fread(body.data(), 1, body.size(), f) != body.size() || fread(&extra, 1, 1, f) != 0)
+      rc = GT_ERR_IO;  // shorter or longer than the header says
+  }
+  fclose(f);
+  if (rc != GT_OK) return rc;
+  if (crc32_of(body.data(), body.size()) != crc) return GT_ERR_CORRUPT;
+  for (size_t i = 0; i < n; ++i) {
+    const int32_t e = (int32_t)get_u32(&body[4 * i]);
+    if (e < -1 || e >= V) return GT_ERR_CORRUPT;
+  }
+  // the caller's table changes only once the whole file has been checked
+  for (size_t i = 0; i < n; ++i) table[i] = (int32_t)get_u32(&body[4 * i]);
+  return GT_OK;
+}
+
 GT_API const char *gt_status_string(int status) {
   switch (status) {
     case GT_OK: return "ok";
@@ -82,6 +211,9 @@ GT_API const char *gt_status_string(int status) {
     case GT_ERR_NONMONOTONE: return "cumulative score exceeds its parent's (or NaN)";
     case GT_ERR_TIMEOUT: return "bounded device wait timed out";
     case GT_ERR_RANGE: return "device-side count exceeds its buffer";
+    case GT_ERR_IO: return "file cannot be opened, read or written, or has the wrong length";
+    case GT_ERR_CORRUPT: return "file magic, checksum or contents invalid";
+    case GT_ERR_VALUE: return "NaN where a number is required (checked build)";
     default: return "unknown status";
   }
 }

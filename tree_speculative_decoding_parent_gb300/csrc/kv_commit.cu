@@ -79,6 +79,7 @@ using namespace gt;
 GT_API int gt_kv_commit(void *K, void *V, const int32_t *kv_src, const int32_t *kv_dst,
                         const int32_t *acc_len, int B, int N, int Hkv, int d, int Lcap,
                         int dtype, int32_t *err, gt_stream_t stream) {
+  GT_TRACE("gt_kv_commit");
   if (B < 0 || N < 1 || Hkv < 1 || d < 1 || Lcap < 1) return GT_ERR_ARG;
   if (dtype != GT_F32 && dtype != GT_BF16) return GT_ERR_ARG;
   const int es = dtype == GT_F32 ? 4 : 2;

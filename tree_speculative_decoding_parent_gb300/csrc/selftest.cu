@@ -36,6 +36,7 @@ using namespace gt;
 
 GT_API int gt_selftest_wait_timeout(int64_t limit_ns, int32_t *err, int64_t *waited_ns,
                                     gt_stream_t stream) {
+  GT_TRACE("gt_selftest_wait_timeout");
   if (limit_ns < 1 || limit_ns > 1000000000ll) return GT_ERR_ARG;
   if (!err) return GT_ERR_ARG;
   return launch(wait_timeout_kernel, dim3(1), dim3(32), 0, (cudaStream_t)stream,

@@ -232,6 +232,7 @@ GT_API int gt_tree_build(const float *score, const int32_t *parent_in, const int
                          float *out_score, int32_t *out_old_idx, int32_t *n_nodes,
                          int32_t *depth, int32_t *pos, uint64_t *mask, int32_t *err,
                          gt_stream_t stream) {
+  GT_TRACE("gt_tree_build");
   if (B < 0 || Nin < 1 || N < 1 || T < 0 || V < 1 || k < 1) return GT_ERR_ARG;
   if (Nin > 1024 || N > 1024 || T > 1024) return GT_ERR_SHAPE;
   if (B == 0) return GT_OK;

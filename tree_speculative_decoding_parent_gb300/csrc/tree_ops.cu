@@ -259,6 +259,7 @@ GT_API int gt_prune_topB(const float *score, const int32_t *parent, const int32_
                          const float *thresh, int Nout, int32_t *out_parent,
                          int32_t *out_tokens, float *out_score, int32_t *out_old_idx,
                          int32_t *n_out, int32_t *err, gt_stream_t stream) {
+  GT_TRACE("gt_prune_topB");
   if (B < 0 || Nin < 1 || Nout < 1) return GT_ERR_ARG;
   if (Nin > 1024) return GT_ERR_SHAPE;
   if (B == 0) return GT_OK;
@@ -274,6 +275,7 @@ GT_API int gt_graft_expand(int32_t *parent, int32_t *tokens, int32_t *n_nodes, i
                            int Nmax, const int32_t *tpar, const int32_t *trank, int T,
                            const int32_t *R, const int32_t *anchor, const int32_t *table, int V,
                            int k, int32_t *err, gt_stream_t stream) {
+  GT_TRACE("gt_graft_expand");
   if (B < 0 || Nmax < 1 || T < 0 || V < 1 || k < 1) return GT_ERR_ARG;
   if (T > 1024) return GT_ERR_SHAPE;
   if (B == 0) return GT_OK;
@@ -288,6 +290,7 @@ GT_API int gt_graft_expand(int32_t *parent, int32_t *tokens, int32_t *n_nodes, i
 GT_API int gt_tree_mask(const int32_t *parent, const int32_t *n_nodes,
                         const int32_t *prefix_len, int B, int N, int32_t *depth, int32_t *pos,
                         uint64_t *mask, int32_t *err, gt_stream_t stream) {
+  GT_TRACE("gt_tree_mask");
   if (B < 0 || N < 1) return GT_ERR_ARG;
   if (N > 1024) return GT_ERR_SHAPE;
   if (B == 0) return GT_OK;

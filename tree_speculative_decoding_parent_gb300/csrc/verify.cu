@@ -179,8 +179,9 @@ __device__ __forceinline__ void topk_exact(const float *x, int b, int e, uint64_
 template <int KK, int CL>
 __global__ void __launch_bounds__(TOPK_THREADS)
 topk_cluster_kernel(const float *__restrict__ logits, int row0, int V, int k,
-                    int32_t *__restrict__ ids, float *__restrict__ vals) {
+                    int32_t *__restrict__ ids, float *__restrict__ vals, int32_t *err) {
   pdl_enter();
+  bool nan_seen = false;  // checked builds: a NaN logit is reported as GT_ERR_VALUE
   constexpr int NW = TOPK_THREADS / 32;
   constexpr int CH = TOPK_PER * TOPK_THREADS;  // float4 per chunk of the CTA
   __shared__ uint64_t s_cand[TOPK_CAP];        // candidates, then scratch of the merges
@@ -254,11 +255,13 @@ topk_cluster_kernel(const float *__restrict__ logits, int row0, int V, int k,
         const int q = c0 + tid + u * TOPK_THREADS;
         const float e[4] = {a[u].x, a[u].y, a[u].z, a[u].w};
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 4; ++c) {
+          if (GT_CHECK && q < e4) nan_seen |= e[c] != e[c];
           if (q < e4 && !(e[c] < thr)) {
             const int pos = atomicAdd(&s_cnt, 1);
             if (pos < TOPK_CAP) s_cand[pos] = pack_key(order_key(e[c]), 4 * q + c);
           }
+        }
       }
 #pragma unroll
       for (int u = 0; u < TOPK_PER; ++u) a[u] = nx[u];
@@ -292,7 +295,10 @@ topk_cluster_kernel(const float *__restrict__ logits, int row0, int V, int k,
   } else {
     const int b = (int)((long long)V * crank / CL), e = (int)((long long)V * (crank + 1) / CL);
     topk_exact<KK>(x, b, e, s_cand, s_top);
+    if (GT_CHECK)
+      for (int i = b + tid; i < e; i += TOPK_THREADS) nan_seen |= x[i] != x[i];
   }
+  GT_CHECKED(!nan_seen, err, GT_ERR_VALUE);
 
   // CTA -> cluster leader
   asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
@@ -324,23 +330,25 @@ topk_cluster_kernel(const float *__restrict__ logits, int row0, int V, int k,
 
 template <int KK, int CL>
 static int topk_launch_cl(const float *logits, int r0, int nr, int V, int k, int32_t *ids,
-                          float *vals, cudaStream_t s) {
+                          float *vals, int32_t *err, cudaStream_t s) {
   return launch_cluster(topk_cluster_kernel<KK, CL>, dim3(CL, nr), dim3(TOPK_THREADS),
-                        dim3(CL, 1, 1), 0, s, logits, r0, V, k, ids, vals);
+                        dim3(CL, 1, 1), 0, s, logits, r0, V, k, ids, vals, err);
 }
 
 template <int KK>
 static int topk_launch_k(const float *logits, int r0, int nr, int V, int k, int32_t *ids,
-                         float *vals, int cl, cudaStream_t s) {
+                         float *vals, int cl, int32_t *err, cudaStream_t s) {
   switch (cl) {
-    case 2: return topk_launch_cl<KK, 2>(logits, r0, nr, V, k, ids, vals, s);
-    case 4: return topk_launch_cl<KK, 4>(logits, r0, nr, V, k, ids, vals, s);
-    default: return topk_launch_cl<KK, TOPK_CLUSTER>(logits, r0, nr, V, k, ids, vals, s);
+    case 2: return topk_launch_cl<KK, 2>(logits, r0, nr, V, k, ids, vals, err, s);
+    case 4: return topk_launch_cl<KK, 4>(logits, r0, nr, V, k, ids, vals, err, s);
+    default: return topk_launch_cl<KK, TOPK_CLUSTER>(logits, r0, nr, V, k, ids, vals, err, s);
   }
 }
 
+// err: the device error word of the calling entry point (NULL for gt_vocab_topk, which has
+// none); only checked builds write to it.
 static int topk_launch(const float *logits, int rows, int V, int k, int32_t *ids, float *vals,
-                       cudaStream_t s) {
+                       int32_t *err, cudaStream_t s) {
   // CTAs per row: enough that the rows fill the GPU with about four CTAs per SM, and at
   // least two. Each split costs one more merge per row, while a whole-row CTA takes its
   // threshold from too small a first chunk of a long row and overflows its candidate
@@ -355,8 +363,8 @@ static int topk_launch(const float *logits, int rows, int V, int k, int32_t *ids
   while (cl < TOPK_CLUSTER && (long long)rows * cl < 4ll * sms) cl *= 2;
   for (int r0 = 0; r0 < rows; r0 += 65535) {
     const int nr = min(65535, rows - r0);
-    const int rc = k <= 8 ? topk_launch_k<8>(logits, r0, nr, V, k, ids, vals, cl, s)
-                          : topk_launch_k<16>(logits, r0, nr, V, k, ids, vals, cl, s);
+    const int rc = k <= 8 ? topk_launch_k<8>(logits, r0, nr, V, k, ids, vals, cl, err, s)
+                          : topk_launch_k<16>(logits, r0, nr, V, k, ids, vals, cl, err, s);
     if (rc != GT_OK) return rc;
   }
   return GT_OK;
@@ -383,7 +391,7 @@ __device__ __forceinline__ void shadow_duplicates(const int *s_par, int *s_tok, 
 __global__ void __launch_bounds__(1024)
 walk_kernel(const int32_t *__restrict__ tokens, const int32_t *__restrict__ parent,
             const int32_t *__restrict__ n_nodes, const int32_t *__restrict__ prefix_len, int N,
-            int k, const int32_t *__restrict__ topk_id, const int32_t *__restrict__ sample,
+            int V, int k, const int32_t *__restrict__ topk_id, const int32_t *__restrict__ sample,
             int32_t *__restrict__ acc_len, int32_t *__restrict__ path,
             int32_t *__restrict__ out_tok, int32_t *__restrict__ kv_src,
             int32_t *__restrict__ kv_dst, int32_t *err) {
@@ -403,6 +411,8 @@ walk_kernel(const int32_t *__restrict__ tokens, const int32_t *__restrict__ pare
     s_tok[v] = tokens[row0 + v];
     s_am[v] = sample ? sample[row0 + v] : topk_id[(row0 + v) * k];
     if (v == 0 ? (p != -1) : (p < 0 || p >= v)) code = GT_ERR_TREE;
+    // checked builds: every verified token is a vocabulary id (the walk itself only compares)
+    if (GT_CHECK && (s_tok[v] < 0 || s_tok[v] >= V)) code = GT_ERR_TREE;
   }
   __syncthreads();
   if (code) atomicCAS(&s_bad, 0, code);
@@ -551,6 +561,7 @@ walk_update_kernel(const int32_t *__restrict__ tokens, const int32_t *__restrict
     s_tok[v] = tok_v;
     s_am[v] = am_v;
     if (v == 0 ? (p != -1) : (p < 0 || p >= v)) code = GT_ERR_TREE;
+    if (GT_CHECK && (tok_v < 0 || tok_v >= V)) code = GT_ERR_TREE;
   }
   __syncthreads();
   if (code) atomicCAS(&s_bad, 0, code);
@@ -650,11 +661,12 @@ using namespace gt;
 
 GT_API int gt_vocab_topk(const float *logits, int rows, int V, int k, int32_t *ids,
                          float *vals, gt_stream_t stream) {
+  GT_TRACE("gt_vocab_topk");
   if (rows < 0 || V < 1 || k < 1) return GT_ERR_ARG;
   if (k > 16 || k > V) return GT_ERR_SHAPE;
   if (rows == 0) return GT_OK;
   if (!logits || !ids || !vals) return GT_ERR_ARG;
-  return topk_launch(logits, rows, V, k, ids, vals, (cudaStream_t)stream);
+  return topk_launch(logits, rows, V, k, ids, vals, nullptr, (cudaStream_t)stream);
 }
 
 GT_API int gt_verify_greedy(const float *logits, const int32_t *tokens, const int32_t *parent,
@@ -662,6 +674,7 @@ GT_API int gt_verify_greedy(const float *logits, const int32_t *tokens, const in
                             int V, int k, int32_t *topk_id, float *topk_val, int32_t *acc_len,
                             int32_t *path, int32_t *out_tok, int32_t *kv_src, int32_t *kv_dst,
                             int32_t *err, gt_stream_t stream) {
+  GT_TRACE("gt_verify_greedy");
   if (B < 0 || N < 1 || V < 1 || k < 1) return GT_ERR_ARG;
   if (N > 1024 || k > 16 || k > V) return GT_ERR_SHAPE;
   if (B == 0) return GT_OK;
@@ -669,17 +682,18 @@ GT_API int gt_verify_greedy(const float *logits, const int32_t *tokens, const in
       !acc_len || !path || !out_tok || !kv_src || !kv_dst)
     return GT_ERR_ARG;
   cudaStream_t s = (cudaStream_t)stream;
-  int rc = topk_launch(logits, B * N, V, k, topk_id, topk_val, s);
+  int rc = topk_launch(logits, B * N, V, k, topk_id, topk_val, err, s);
   if (rc != GT_OK) return rc;
   const int threads = (N + 31) / 32 * 32;
   return launch(walk_kernel, dim3(B), dim3(threads), 4 * sizeof(int) * (size_t)N, s, tokens,
-                parent, n_nodes, prefix_len, N, k, topk_id, (const int32_t *)nullptr, acc_len, path,
-                out_tok, kv_src, kv_dst, err);
+                parent, n_nodes, prefix_len, N, V, k, topk_id, (const int32_t *)nullptr, acc_len,
+                path, out_tok, kv_src, kv_dst, err);
 }
 
 GT_API int gt_succ_update(int32_t *table, int V, int k, const int32_t *tokens,
                           const int32_t *topk_id, const int32_t *n_nodes, int B, int N,
                           int32_t *err, gt_stream_t stream) {
+  GT_TRACE("gt_succ_update");
   if (B < 0 || N < 1 || V < 1 || k < 1) return GT_ERR_ARG;
   const long long total = (long long)B * N;
   if (total > 16384) return GT_ERR_SHAPE;
@@ -728,6 +742,7 @@ GT_API int gt_verify_commit(const float *logits, const int32_t *tokens, const in
                             int k, int32_t *topk_id, float *topk_val, int32_t *acc_len,
                             int32_t *path, int32_t *out_tok, int32_t *kv_src, int32_t *kv_dst,
                             int32_t *table, int32_t *err, gt_stream_t stream) {
+  GT_TRACE("gt_verify_commit");
   if (B < 0 || N < 1 || V < 1 || k < 1) return GT_ERR_ARG;
   if (N > 1024 || k > 16 || k > V || (long long)B * N > 16384) return GT_ERR_SHAPE;
   if (B == 0) return GT_OK;
@@ -735,7 +750,7 @@ GT_API int gt_verify_commit(const float *logits, const int32_t *tokens, const in
       !acc_len || !path || !out_tok || !kv_src || !kv_dst || !table)
     return GT_ERR_ARG;
   cudaStream_t s = (cudaStream_t)stream;
-  int rc = topk_launch(logits, B * N, V, k, topk_id, topk_val, s);
+  int rc = topk_launch(logits, B * N, V, k, topk_id, topk_val, err, s);
   if (rc != GT_OK) return rc;
   return walk_update_launch(tokens, parent, n_nodes, prefix_len, B, N, V, k, topk_id, nullptr,
                             acc_len, path, out_tok, kv_src, kv_dst, table, err, s);
@@ -743,6 +758,7 @@ GT_API int gt_verify_commit(const float *logits, const int32_t *tokens, const in
 
 GT_API int gt_vocab_sample(const float *logits, int rows, int V, float temperature,
                            uint64_t seed, uint64_t step, int32_t *sample, gt_stream_t stream) {
+  GT_TRACE("gt_vocab_sample");
   if (rows < 0 || V < 1) return GT_ERR_ARG;
   if (rows == 0) return GT_OK;
   if (!logits || !sample) return GT_ERR_ARG;
@@ -754,6 +770,7 @@ GT_API int gt_verify_sample(const float *logits, const int32_t *tokens, const in
                             int V, float temperature, uint64_t seed, uint64_t step,
                             int32_t *sample, int32_t *acc_len, int32_t *path, int32_t *out_tok,
                             int32_t *kv_src, int32_t *kv_dst, int32_t *err, gt_stream_t stream) {
+  GT_TRACE("gt_verify_sample");
   if (B < 0 || N < 1 || V < 1) return GT_ERR_ARG;
   if (N > 1024 || (long long)B * N > 16384) return GT_ERR_SHAPE;
   if (B == 0) return GT_OK;
@@ -765,8 +782,8 @@ GT_API int gt_verify_sample(const float *logits, const int32_t *tokens, const in
   if (rc != GT_OK) return rc;
   const int threads = (N + 31) / 32 * 32;
   return launch(walk_kernel, dim3(B), dim3(threads), 4 * sizeof(int) * (size_t)N, s, tokens,
-                parent, n_nodes, prefix_len, N, 1, (const int32_t *)nullptr, (const int32_t *)sample,
-                acc_len, path, out_tok, kv_src, kv_dst, err);
+                parent, n_nodes, prefix_len, N, V, 1, (const int32_t *)nullptr,
+                (const int32_t *)sample, acc_len, path, out_tok, kv_src, kv_dst, err);
 }
 
 GT_API int gt_verify_sample_commit(const float *logits, const int32_t *tokens,
@@ -777,6 +794,7 @@ GT_API int gt_verify_sample_commit(const float *logits, const int32_t *tokens,
                                    int32_t *acc_len, int32_t *path, int32_t *out_tok,
                                    int32_t *kv_src, int32_t *kv_dst, int32_t *table, int32_t *err,
                                    gt_stream_t stream) {
+  GT_TRACE("gt_verify_sample_commit");
   if (B < 0 || N < 1 || V < 1 || k < 1) return GT_ERR_ARG;
   if (N > 1024 || k > 16 || k > V || (long long)B * N > 16384) return GT_ERR_SHAPE;
   if (B == 0) return GT_OK;
@@ -786,7 +804,7 @@ GT_API int gt_verify_sample_commit(const float *logits, const int32_t *tokens,
   cudaStream_t s = (cudaStream_t)stream;
   int rc = sample_launch(logits, B * N, V, temperature, seed, step, sample, s);
   if (rc != GT_OK) return rc;
-  rc = topk_launch(logits, B * N, V, k, topk_id, topk_val, s);
+  rc = topk_launch(logits, B * N, V, k, topk_id, topk_val, err, s);
   if (rc != GT_OK) return rc;
   return walk_update_launch(tokens, parent, n_nodes, prefix_len, B, N, V, k, topk_id, sample,
                             acc_len, path, out_tok, kv_src, kv_dst, table, err, s);

@@ -15,6 +15,7 @@ LIB_PATH = os.path.join(_HERE, "libgt.so")
 
 GT_OK, GT_ERR_ARG, GT_ERR_SHAPE, GT_ERR_CUDA = 0, -1, -2, -3
 GT_ERR_TREE, GT_ERR_NONMONOTONE, GT_ERR_TIMEOUT, GT_ERR_RANGE = -4, -5, -6, -7
+GT_ERR_IO, GT_ERR_CORRUPT, GT_ERR_VALUE = -8, -9, -10
 GT_F32, GT_BF16 = 0, 1
 GT_ATTN_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024  # size of the static scratch in libgt
 
@@ -51,6 +52,9 @@ _SIGS = {
     "gt_tree_attach": (_i, [_vp, _vp, _vp, _vp, _i, _i, _vp, _vp, _i, _vp, _vp, _i, _i, _vp, _vp,
                             _vp]),
     "gt_selftest_wait_timeout": (_i, [ctypes.c_int64, _vp, _vp, _vp]),
+    "gt_succ_save": (_i, [ctypes.c_char_p, _vp, _i, _i]),
+    "gt_succ_file_shape": (_i, [ctypes.c_char_p, _vp, _vp]),
+    "gt_succ_load": (_i, [ctypes.c_char_p, _vp, _i, _i]),
     "gt_stage_budget": (_i, [_i, _i, _vp, _vp]),
     "gt_default_template": (_i, [_i, _i, _i, _vp, _vp]),
     "gt_status_string": (ctypes.c_char_p, [_i]),
@@ -69,20 +73,37 @@ class GTError(RuntimeError):
         self.status = status
 
 
+def _open(path: str) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with "
+                           "tree_speculative_decoding_parent_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
 def load() -> ctypes.CDLL:
     """Load libgt.so (built in-tree); raises if it has not been built."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
-                               "tree_speculative_decoding_parent_gb300.build.build()")
-        lib = ctypes.CDLL(LIB_PATH)
-        for name, (res, args) in _SIGS.items():
-            fn = getattr(lib, name)
-            fn.restype = res
-            fn.argtypes = args
-        _lib = lib
+        _lib = _open(LIB_PATH)
     return _lib
+
+
+_lib_check = None
+
+
+def load_checked() -> ctypes.CDLL:
+    """Load the checked flavour libgt_check.so (extra device-side input checks reported in
+    the error word; built by ``build.build(check=True)``): the same entry points with the
+    same signatures, called directly on the returned handle."""
+    global _lib_check
+    if _lib_check is None:
+        _lib_check = _open(os.path.join(_HERE, "libgt_check.so"))
+    return _lib_check
 
 
 def exported_symbols():
@@ -253,6 +274,34 @@ def gt_tree_attach(parent, tokens, score, n_nodes, B, Nmax, frontier, n_frontier
 def gt_selftest_wait_timeout(limit_ns, err, waited_ns=None, stream=None):
     _check("gt_selftest_wait_timeout", load().gt_selftest_wait_timeout(
         int(limit_ns), _p(err), _p(waited_ns), _s(stream)))
+
+
+def gt_succ_save(path: str, table) -> None:
+    """Write a successor table (host int32 [V][k]; a torch tensor is copied to the host) to
+    path."""
+    import numpy as np
+    t = table.detach().cpu().numpy() if hasattr(table, "detach") else table
+    t = np.ascontiguousarray(t, dtype=np.int32)
+    V, k = t.shape
+    _check("gt_succ_save", load().gt_succ_save(os.fsencode(path), t.ctypes.data, V, k))
+
+
+def gt_succ_file_shape(path: str):
+    V, k = ctypes.c_int32(), ctypes.c_int32()
+    _check("gt_succ_file_shape", load().gt_succ_file_shape(os.fsencode(path), ctypes.byref(V),
+                                                           ctypes.byref(k)))
+    return V.value, k.value
+
+
+def gt_succ_load(path: str, V: int = None, k: int = None):
+    """Read a successor table file; returns a host int32 [V][k] array (V, k: the expected
+    shape, else the file's)."""
+    import numpy as np
+    if V is None or k is None:
+        V, k = gt_succ_file_shape(path)
+    t = np.empty((V, k), np.int32)
+    _check("gt_succ_load", load().gt_succ_load(os.fsencode(path), t.ctypes.data, V, k))
+    return t
 
 
 def gt_stage_budget(stage: int, slots: int = 60):
