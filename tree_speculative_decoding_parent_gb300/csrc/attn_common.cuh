@@ -89,6 +89,60 @@ __device__ __forceinline__ int4 schedule_piece(const SchedArgs &a, int p, AttnWs
     return ok ? (P + n + a.TK - 1) / a.TK : 0;
   };
   __shared__ int2 s_np;  // (n, P) of the piece's request
+  if (S <= 32) {
+    // up to 32 segments: lane l of warp 0 holds segment l. The same tau and pieces as the
+    // paths below, in the least code: this runs once per CTA, its instructions fetched cold
+    if (warp == 0) {
+      int t = 0, n = 0, P = 0;
+      if (lane < S) {
+        const int b = lane / a.Hkv;
+        n = a.n_nodes[b];
+        P = a.prefix_len[b];
+        const bool ok = n >= 1 && n <= a.N && P >= 0 && (long long)P + n <= (long long)a.Lcap;
+        if (!ok && publisher && (lane % a.Hkv) == 0 && err) atomicCAS(err, 0, GT_ERR_RANGE);
+        t = ok ? (P + n + a.TK - 1) / a.TK : 0;
+      }
+      const int T = (int)__reduce_add_sync(0xffffffffu, (unsigned)t);
+      const int Sn = (int)__reduce_add_sync(0xffffffffu, (unsigned)(t > 0));
+      int tau = max(1, (T + a.G - 1) / a.G);
+      if (Sn > 0 && a.G > Sn) {
+        int lo = tau, hi = max(tau, (T + (a.G - Sn) - 1) / (a.G - Sn));
+        while (lo < hi) {
+          const int mid = lo + (hi - lo) / 2;
+          if ((int)__reduce_add_sync(0xffffffffu, (unsigned)((t + mid - 1) / mid)) <= a.G)
+            hi = mid;
+          else
+            lo = mid + 1;
+        }
+        tau = lo;
+      }
+      const int cnt = (t + tau - 1) / tau;
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int off = incl - cnt;
+      if (lane < S) {
+        if (publisher) ws.seg[lane] = make_int2(off, cnt);
+        if (p >= off && p < off + cnt) {
+          // floor(t * j / cnt) = (t / cnt) * j + floor((t % cnt) * j / cnt), in 32 bits
+          const int j = p - off, q = t / cnt, r = t - q * cnt;
+          s_piece = make_int4(lane, q * j + r * j / cnt, q * (j + 1) + r * (j + 1) / cnt, 0);
+          s_np = make_int2(n, P);
+        }
+      }
+      const int total = __shfl_sync(0xffffffffu, incl, 31);
+      if (lane == 0) {
+        if (publisher) ws.hdr[0] = total;
+        if (p >= total) s_piece = make_int4(-1, 0, 0, 0);
+      }
+    }
+    __syncthreads();
+    if (np_out) *np_out = s_np;
+    return s_piece;
+  }
   if (S <= 32 * CH) {
     // few segments: warp 0 computes the whole schedule with 32-bit shuffles and reductions
     // (lane l holds segments l, l + 32, ...), the same tau and pieces as the block version

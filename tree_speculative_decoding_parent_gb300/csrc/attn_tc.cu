@@ -71,7 +71,6 @@ constexpr uint32_t Q_COL = 384;
 constexpr uint32_t P_COL = 448;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
-constexpr int STAGE_PITCH = ATTN_D * 4 + 16;  // bytes per staged partial row
 static_assert(TK == 128, "the tile shape above assumes 128-key tiles");
 static_assert(KLEAD == NSBUF, "S(t + NSBUF) reuses the buffer of P(t)");
 
@@ -88,9 +87,16 @@ struct Smem {
   static constexpr int END = BAR + NBAR * 8;
   static constexpr size_t BYTES = END + 1024;  // + alignment slack
   static_assert(BYTES + 768 <= 232448, "shared memory of one CTA (dynamic + static)");
-  static_assert(128 * STAGE_PITCH <= SLOTS * SLOT_BYTES, "partial rows are staged in the ring");
+  static_assert(128 * ATTN_D * 4 <= SLOTS * SLOT_BYTES, "partial rows are staged in the ring");
 };
 constexpr int RING_GATE = 3;  // ring items issued before the producer waits for q_full
+// Of every 8 score pairs, this many take their exponentials from a polynomial on the FMA
+// pipe and the rest from the special-function unit, whose rate (16 per SM and cycle) would
+// otherwise bound the softmax of a tile.
+#ifndef GT_ATTN_EX2_POLY_PAIRS
+#define GT_ATTN_EX2_POLY_PAIRS 0
+#endif
+constexpr int EX2_POLY_PAIRS = GT_ATTN_EX2_POLY_PAIRS;
 
 struct Bars {
   uint64_t *q_full, *full, *empty, *s_full, *s_free, *p_full, *o_ready, *o_done, *drain;
@@ -192,11 +198,11 @@ __device__ __forceinline__ void q_row_to_tmem(const __nv_bfloat16 *__restrict__ 
 }
 
 // Softmax of one tile for this thread's row: s holds the row's 128 raw scores of keys
-// kb .. kb+127 (masked in place), P the committed prefix length, keys = P + n, mrow the
-// row's ancestor mask over the tree keys. Produces the P words (bf16 pairs) in pk, the
-// factor alpha by which the running O and sum must be scaled, and updates the reference
-// max m_used (log2 units) and the row sum l. `later` is true for every tile after the
-// piece's first. Warp-collective (its votes keep the paths warp-uniform).
+// kb .. kb+127 (masked in place), P the committed prefix length, mrow the row's ancestor mask
+// over the tree keys (no bit at or past the node count). Produces the P words (bf16 pairs)
+// in pk, the factor alpha by which the running O and sum must be scaled, and updates the
+// reference max m_used (log2 units) and the row sum l. `later` is true for every tile after
+// the piece's first. Warp-collective (its votes keep the paths warp-uniform).
 //
 // p = 2^(s*scale*log2e - m_used) against a lazily moved reference max. A tile wholly inside
 // the committed prefix, once the row has a finite reference, goes straight to the
@@ -204,21 +210,31 @@ __device__ __forceinline__ void q_row_to_tmem(const __nv_bfloat16 *__restrict__ 
 // exceeded the lazy-rescale bound 2^8, so the result is what a max pass first would give
 // (up to summation order). Otherwise (the first tile, a masked tile, or the rare growth of
 // the row's max by more than 8 in log2 units) a max pass moves the reference first. Both
-// cases run the same exponential loop, which keeps the code small.
-__device__ __forceinline__ void softmax_tile(uint32_t (&s)[4][32], int kb, int P, int keys,
-                                             uint64_t mrow, float sl2, bool later,
-                                             float &m_used, float &l, float &alpha,
-                                             uint32_t (&pk)[4][16]) {
+// cases run the same exponential loop, which keeps the code small: code that runs once per
+// piece is fetched cold, at a cost that grows with its size.
+__device__ __forceinline__ void softmax_tile(uint32_t (&s)[4][32], int kb, int P, uint64_t mrow,
+                                             float sl2, bool later, float &m_used, float &l,
+                                             float &alpha, uint32_t (&pk)[4][16]) {
   alpha = 1.f;
-  if (kb + TK > P) {  // keys of the tree: the ancestor mask decides visibility
+  if (kb + TK > P) {
+    // visibility of the tile's keys as one 32-bit word per column of 32 keys: the prefix keys
+    // below P, then the tree keys P + u whose bit u is set in the row's ancestor mask
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
+    for (int c = 0; c < 4; ++c) {
+      const int key0 = kb + c * 32;
+      const int np = min(max(P - key0, 0), 32);
+      const uint32_t pre = np >= 32 ? 0xFFFFFFFFu : ((1u << np) - 1u);
+      const int u0 = key0 - P;
+      uint32_t tree = 0u;
+      if (u0 >= 0 && u0 < 64)
+        tree = (uint32_t)(mrow >> u0);
+      else if (u0 < 0 && u0 > -32)
+        tree = (uint32_t)(mrow << (-u0));
+      const uint32_t vis = pre | tree;
 #pragma unroll
-      for (int q = 0; q < 32; ++q) {
-        const int key = kb + c * 32 + q;
-        const bool vis = key < P || (key < keys && ((mrow >> (unsigned)(key - P)) & 1ull));
-        if (!vis) s[c][q] = __float_as_uint(-INFINITY);
-      }
+      for (int q = 0; q < 32; ++q)
+        if (!((vis >> q) & 1u)) s[c][q] = __float_as_uint(-INFINITY);
+    }
   }
   bool need_max = __any_sync(0xffffffffu, !later || kb + TK > P || m_used == -INFINITY);
   float lt;
@@ -249,8 +265,16 @@ __device__ __forceinline__ void softmax_tile(uint32_t (&s)[4][32], int kb, int P
 #pragma unroll
       for (int q = 0; q < 16; ++q) {
         float p0, p1;
-        tc::ex2_fma_x2(__uint_as_float(s[c][2 * q]), __uint_as_float(s[c][2 * q + 1]), a2, c2,
-                       p0, p1);
+        if ((q & 7) < EX2_POLY_PAIRS) {  // this pair's exponentials on the FMA pipe
+          float x0, x1;
+          tc::fma_x2(__uint_as_float(s[c][2 * q]), __uint_as_float(s[c][2 * q + 1]), a2, c2, x0,
+                     x1);
+          p0 = tc::ex2_poly(x0);
+          p1 = tc::ex2_poly(x1);
+        } else {
+          tc::ex2_fma_x2(__uint_as_float(s[c][2 * q]), __uint_as_float(s[c][2 * q + 1]), a2, c2,
+                         p0, p1);
+        }
         tc::add_x2(acc[q & 3], p0, p1);
         pk[c][q] = tc::pack_bf16x2(p0, p1);
       }
@@ -281,49 +305,52 @@ __device__ __forceinline__ void rescale_o(uint32_t tO, float alpha) {
   }
 }
 
-// The normalised partial rows and their log-sum-exps. They leave through shared memory
-// (`stage`, idle once O is complete) so that every warp store covers a whole 512-byte row;
-// rows are staged at a 528-byte pitch, which keeps the threads' 16-byte writes free of bank
-// conflicts. ok: this thread's waits all succeeded. Called by the 128 softmax threads.
-__device__ __forceinline__ void write_partial(uint8_t *stage, uint32_t tO, bool ok, float l,
-                                              float m_used, int p, int row0, int rows,
-                                              const AttnWs &ws) {
+// The normalised partial rows and their log-sum-exps. The rows are staged in shared memory
+// (`stage`, idle once O is complete) as four boxes of 32 columns x 128 rows in the 128-byte
+// swizzle of the tensor map mapO (16-byte chunk k of row r at chunk k ^ (r % 8), which keeps
+// a warp's 16-byte writes free of bank conflicts), then one thread stores the four boxes with
+// TMA. Rows past the tree are stored too (they lie inside the piece's padded rows and are
+// never read). ok: this thread's waits all succeeded. Called by the 128 softmax threads.
+__device__ __forceinline__ void write_partial(uint8_t *stage, const CUtensorMap *mapO,
+                                              uint32_t tO, bool ok, float l, float m_used, int p,
+                                              int row0, int rows, const AttnWs &ws) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, rl = warp * 32 + lane;
   const int r = row0 + rl;
   const bool wok = __all_sync(0xffffffffu, ok);
   if (wok) {
     tc::tc_fence_after();
     const float inv = l > 0.f ? 1.f / l : 0.f;
-    uint8_t *srow = stage + rl * STAGE_PITCH;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       uint32_t o[32];
       tc::tmem_ld32(tO + c * 32, o);
       tc::tmem_wait_ld();
+      uint8_t *row = stage + c * (128 * 128) + rl * 128;
 #pragma unroll
-      for (int q = 0; q < 32; q += 4)
-        *reinterpret_cast<float4 *>(srow + (c * 32 + q) * 4) =
-            make_float4(__uint_as_float(o[q]) * inv, __uint_as_float(o[q + 1]) * inv,
-                        __uint_as_float(o[q + 2]) * inv, __uint_as_float(o[q + 3]) * inv);
+      for (int k = 0; k < 8; ++k)
+        *reinterpret_cast<float4 *>(row + ((k ^ (rl & 7)) << 4)) =
+            make_float4(__uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
+                        __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
     }
     if (r < rows)
       ws.lse[(size_t)p * ws.rows_pad + r] = l > 0.f ? (m_used + log2f(l)) * LN2 : -INFINITY;
+    tc::fence_proxy_async_smem();  // the staged rows are visible to the TMA engine
   }
-  // the four softmax warps meet (named barrier 1, 128 threads); each then writes 32 rows
+  // the four softmax warps meet (named barrier 1, 128 threads); one thread stores the boxes
   const int wall = __syncthreads_and_named(wok);
-  if (wall) {
-    float *dst0 = ws.opart + ((size_t)p * ws.rows_pad + row0) * ATTN_D;
-    for (int rr = warp * 32; rr < warp * 32 + 32; ++rr) {
-      if (row0 + rr >= rows) break;  // rows past the tree are never read
-      const float4 v = *reinterpret_cast<const float4 *>(stage + rr * STAGE_PITCH + lane * 16);
-      *reinterpret_cast<float4 *>(dst0 + (size_t)rr * ATTN_D + lane * 4) = v;
-    }
+  if (wall && threadIdx.x == 0) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      tc::tma_store_2d(mapO, stage + c * (128 * 128), c * 32, p * ws.rows_pad + row0);
+    tc::bulk_commit();
+    tc::bulk_wait_read_all();  // shared memory may be released once the stores have read it
   }
 }
 
 __global__ void __launch_bounds__(TC_THREADS, 1)
 attn_tc_kernel(const __nv_bfloat16 *__restrict__ Qg, const __grid_constant__ CUtensorMap mapK,
-               const __grid_constant__ CUtensorMap mapV, const uint64_t *__restrict__ mask,
+               const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapO,
+               uint32_t q_slice, uint32_t q_bytes, const uint64_t *__restrict__ mask,
                const int32_t *__restrict__ prefix_len, const int32_t *__restrict__ n_nodes,
                int N, int Hq, int Hkv, float scale, int C, int L, SchedArgs sa, AttnWs ws,
                int32_t *err) {
@@ -375,6 +402,13 @@ attn_tc_kernel(const __nv_bfloat16 *__restrict__ Qg, const __grid_constant__ CUt
   volatile int *abort = &abort_sh;
 
   pdl_enter();
+  // Q is read only after the schedule: each CTA asks L2 for its slice of it now, so that the
+  // rows are on chip when the softmax threads load them
+  if (tid == 0) {
+    const uint32_t q0 = blockIdx.x * q_slice;
+    if (q0 < q_bytes)
+      tc::prefetch_l2_bulk(reinterpret_cast<const uint8_t *>(Qg) + q0, min(q_slice, q_bytes - q0));
+  }
   // every CTA of a cluster gets the same piece, so a cluster leaves here as a whole
   const int p = blockIdx.x / C;
   int2 np;
@@ -501,11 +535,13 @@ attn_tc_kernel(const __nv_bfloat16 *__restrict__ Qg, const __grid_constant__ CUt
     // ------------------------------------------------------------------- softmax
     const int rl = warp * 32 + lane;                // row within the M-tile = TMEM lane
     const int r = row0 + rl;                        // row within the segment
-    const uint64_t mrow = r < g * n ? mask[(size_t)b * N + r / g] : 0ull;
+    const uint64_t mword = r < g * n ? mask[(size_t)b * N + r / g] : 0ull;
     // checked builds: a tree row's mask holds the root and the node itself, no node past n
-    GT_CHECKED(r >= g * n || (((mrow >> (r / g)) & 1ull) && (mrow & 1ull) &&
-                              (n >= 64 || (mrow >> n) == 0ull)),
+    GT_CHECKED(r >= g * n || (((mword >> (r / g)) & 1ull) && (mword & 1ull) &&
+                              (n >= 64 || (mword >> n) == 0ull)),
                err, GT_ERR_TREE);
+    // keys past the request's length stay invisible whatever the word holds past node n - 1
+    const uint64_t mrow = n >= 64 ? mword : (mword & ((1ull << n) - 1ull));
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const uint32_t tO = tmem + lane_base + O_COL;
     const float sl2 = scale * LOG2E;  // scale > 0: the max of raw scores gives the max
@@ -533,7 +569,7 @@ attn_tc_kernel(const __nv_bfloat16 *__restrict__ Qg, const __grid_constant__ CUt
       const int kb = (t0 + j) * TK;
       float alpha;
       uint32_t pk[4][16];  // P(j) as bf16 pairs, stored once the previous P is consumed
-      softmax_tile(s, kb, P, keys, mrow, sl2, j > 0, m_used, l, alpha, pk);
+      softmax_tile(s, kb, P, mrow, sl2, j > 0, m_used, l, alpha, pk);
       // O += P(j-1) V(j-1) must have completed before O is rescaled here and before P(j)
       // overwrites P(j-1)
       if (j > 0 && !__all_sync(0xffffffffu, tc::mbar_wait(bar.o_ready, (uint32_t)((j - 1) & 1), abort))) {
@@ -568,7 +604,7 @@ attn_tc_kernel(const __nv_bfloat16 *__restrict__ Qg, const __grid_constant__ CUt
       tc::mbar_arrive(bar.p_full);
     }
     if (ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(bar.o_done, 0, abort));
-    write_partial(base + Lay::RING, tO, ok, l, m_used, p, row0, g * n, ws);
+    write_partial(base + Lay::RING, &mapO, tO, ok, l, m_used, p, row0, g * n, ws);
   }
 
   tc::tc_fence_before();
@@ -612,12 +648,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 bool encode(CUtensorMap *map, const void *ptr, int rank, const cuuint64_t *dims,
-            const cuuint64_t *strides_bytes, const cuuint32_t *box) {
+            const cuuint64_t *strides_bytes, const cuuint32_t *box,
+            CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint32_t es[4] = {1, 1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(ptr), dims,
-            strides_bytes, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  return fn(map, type, rank, const_cast<void *>(ptr), dims, strides_bytes, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -693,11 +730,24 @@ int attn_tc_launch(const void *Q, const void *K, const void *V, const uint64_t *
     note_error("cuTensorMapEncodeTiled(K/V)", cudaErrorInvalidValue);
     return GT_ERR_CUDA;
   }
+  // the partial rows: fp32 [maxp * rows_pad][d], stored in boxes of 32 columns x 128 rows
+  CUtensorMap mO;
+  const cuuint64_t odims[2] = {(cuuint64_t)ATTN_D, (cuuint64_t)ws.maxp * ws.rows_pad};
+  const cuuint64_t ostr[1] = {(cuuint64_t)ATTN_D * 4};
+  const cuuint32_t obox[2] = {32, 128};
+  if (!encode(&mO, ws.opart, 2, odims, ostr, obox, CU_TENSOR_MAP_DATA_TYPE_FLOAT32)) {
+    note_error("cuTensorMapEncodeTiled(partial O)", cudaErrorInvalidValue);
+    return GT_ERR_CUDA;
+  }
   if (!set_attributes()) return GT_ERR_CUDA;
+  // each CTA asks L2 for a slice of Q (16-byte multiples) before it computes the schedule
+  const uint32_t q_bytes = (uint32_t)((size_t)B * N * Hq * ATTN_D * 2);
+  const int grid = C * pieces;
+  const uint32_t q_slice = max(16u, (q_bytes / grid + 15u) / 16u * 16u);
   // one cluster of C CTAs per piece; the schedule never makes more than `pieces`
-  return launch_cluster(attn_tc_kernel, dim3(C * pieces), dim3(TC_THREADS), dim3(C, 1, 1),
-                        Smem::BYTES, s, (const __nv_bfloat16 *)Q, mK, mV, mask, sa.prefix_len,
-                        sa.n_nodes, N, Hq, Hkv, scale, C, L, sa, ws, err);
+  return launch_cluster(attn_tc_kernel, dim3(grid), dim3(TC_THREADS), dim3(C, 1, 1),
+                        Smem::BYTES, s, (const __nv_bfloat16 *)Q, mK, mV, mO, q_slice, q_bytes,
+                        mask, sa.prefix_len, sa.n_nodes, N, Hq, Hkv, scale, C, L, sa, ws, err);
 }
 
 }  // namespace gt

@@ -133,6 +133,30 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
+// Asks L2 to fetch [p, p + bytes) from global memory (16-byte aligned, size a multiple of
+// 16); nothing waits for it.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)),
+               "r"(bytes)
+               : "memory");
+}
+// 2-D tile store shared -> global through a tensor map (the box of the map at coordinates
+// (c0, c1)), tracked by the issuing thread's bulk async-group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, const void *src, int c0,
+                                             int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Waits until every committed bulk store of this thread has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 // Generic-proxy writes to shared memory become visible to the async proxy (TMA, MMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -289,6 +313,32 @@ __device__ __forceinline__ void ex2_fma_x2(float s0, float s1, uint64_t a, uint6
       "ex2.approx.ftz.f32 %1, x1;\n\t}"
       : "=f"(p0), "=f"(p1)
       : "f"(s0), "f"(s1), "l"(a), "l"(c));
+}
+// x = s * a + c for a pair of scores (one packed FMA, each lane rounded once, as fmaf).
+__device__ __forceinline__ void fma_x2(float s0, float s1, uint64_t a, uint64_t c, float &x0,
+                                       float &x1) {
+  asm("{\n\t.reg .b64 sp, xp;\n\t"
+      "mov.b64 sp, {%2, %3};\n\t"
+      "fma.rn.f32x2 xp, sp, %4, %5;\n\t"
+      "mov.b64 {%0, %1}, xp;\n\t}"
+      : "=f"(x0), "=f"(x1)
+      : "f"(s0), "f"(s1), "l"(a), "l"(c));
+}
+// 2^x on the FMA and integer pipes instead of the special-function unit. Range reduction
+// 2^x = 2^j * 2^f with j = round(x) (x + 1.5 * 2^23 leaves j in the low mantissa bits) and
+// f = x - j in [-1/2, 1/2]; 2^f by a degree-3 polynomial fitted to 2^f on [-1/2, 1/2] by a
+// Remez exchange on the relative error (7.5e-5 for the polynomial, below 1.5e-4 with the
+// float32 evaluation); 2^j is added to the exponent field. x is clamped to [-126, 64] so the
+// exponent field never wraps: values below 2^-126 come out as tiny non-negative numbers (the
+// hardware approximation flushes them to zero) and values above 2^64 as 2^64 or less, which
+// the softmax's overflow test catches like an infinity.
+__device__ __forceinline__ float ex2_poly(float x) {
+  x = fminf(fmaxf(x, -126.f), 64.f);
+  const float t = x + 12582912.f;
+  const float f = x - (t - 12582912.f);
+  const float p = fmaf(fmaf(fmaf(0.0551716685f, f, 0.2426111251f), f, 0.6932609677f), f,
+                       0.9999280572f);
+  return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
 }
 // acc += (p0, p1) with one packed add.
 __device__ __forceinline__ void add_x2(uint64_t &acc, float p0, float p1) {
