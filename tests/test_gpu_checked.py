@@ -89,7 +89,7 @@ def test_checked_build_reports_nan_logit_and_bad_mask_row(chk):
         assert int(err.item()) == want
     mask = buf.mask.clone()
     mask[0, 7] &= ~(1 << 7)  # row 7 without its own node
-    ws = torch.empty(buf.ws_bytes, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(buf.ws_bytes, dtype=torch.uint8, device="cuda")
     for lib, want in ((gt.load(), gt.GT_OK), (chk, gt.GT_ERR_TREE)):
         err = torch.zeros(1, dtype=torch.int32, device="cuda")
         assert _call(lib, "gt_tree_attn", inp["Q"], inp["K"], inp["V"], mask, inp["prefix_len"],
