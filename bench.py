@@ -170,7 +170,7 @@ class ClockSampler:
                 "source": "nvml"}
 
 
-def _traffic_record(kernel_key: str):
+def _traffic_record(kernel_key: str, field: str = "bytes_per_launch"):
     """DRAM bytes per launch from a committed ncu summary, if the kernel's sources are
     unchanged since the capture (sha256 of ATTN_SOURCES), else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
@@ -180,7 +180,7 @@ def _traffic_record(kernel_key: str):
         rec = json.load(f).get(kernel_key)
     if not rec:
         return None
-    return rec["bytes_per_launch"] if rec.get("src_sha256") == _src_hash() else None
+    return rec.get(field) if rec.get("src_sha256") == _src_hash() else None
 
 
 # the sources the attention kernels (tcgen05, SIMT, combine) are compiled from
@@ -532,7 +532,9 @@ def run_gpu(args):
                          "calls": f"{len(attn_ms)} calls, one per {ATTN_EVENT_EVERY} steps of a "
                                   f"{attn_steps}-step graph, events on the launch stream (the "
                                   "call then loses its overlap with the tree build)"},
-                     "traffic": _traffic_record(f"tree_attn/config{args.config}")},
+                     "traffic": _traffic_record(f"tree_attn/config{args.config}"),
+                     "traffic_attn_kernel": _traffic_record(f"tree_attn/config{args.config}",
+                                                            "attn_tc_kernel_bytes")},
         "e2e": {"value": ne / e2e_s, "unit": "steps/s",
                 "eager_value": ne / e2e_eager_s,
                 "how": "pinned host inputs copied in (the logits on a side stream, overlapping "

@@ -96,6 +96,7 @@ def test_verify_sample_commit_matches_oracle(cid):
         want = step_verify_sampled(tree, logits, scn.table, scn.prefix_len, scn.k, T, seed, step)
         assert np.array_equal(np_(buf.sample), want["sample"])
         assert np.array_equal(np_(buf.topk_id), want["topk_id"])
+        assert np.array_equal(np_(buf.topk_val).view(np.uint32), want["topk_val"].view(np.uint32))
         for key in ("acc_len", "path", "out_tok", "kv_src", "kv_dst"):
             assert np.array_equal(np_(getattr(buf, key)), want[key]), key
         assert np.array_equal(np_(inp["table"]), want["table"])
@@ -168,3 +169,42 @@ def test_vocab_sample_long_rows_overflow_the_candidate_queue():
     pick = np.array([0, 1, 150, 304])
     z = dz[torch.from_numpy(pick).cuda()].cpu().numpy()
     assert np.array_equal(np_(out)[pick], vocab_sample(z, pick, 1.3, 31, 2))
+
+
+@pytest.mark.parametrize("V", [37, 4099, 20000])
+def test_sampled_commit_topk_special_values_and_ties(V):
+    """The top-k that gt_verify_sample_commit forms in its sampling pass, against the oracle's
+    top-k on rows of ties, +-0, +-inf, NaN, and rows of one repeated value (every element a
+    candidate: the exact per-thread-list path), on aligned and unaligned rows."""
+    import oracle
+    rng = np.random.default_rng(V)
+    B, N, k = 2, 33, 8
+    pool = np.float32([0.0, -0.0, 1.0, -1.0, 2.5, np.inf, -np.inf, np.nan, 1e-30, -1e-30])
+    logits = pool[rng.integers(0, len(pool), size=(B, N, V))].astype(np.float32)
+    logits[0, 3, :] = 1.5          # one repeated value
+    logits[1, 7, :] = -0.0
+    logits[1, 8, :] = rng.standard_normal(V).astype(np.float32)
+    parent = np.tile(np.arange(-1, N - 1, dtype=np.int32), (B, 1))
+    tokens = rng.integers(0, V, size=(B, N)).astype(np.int32)
+    n = np.full(B, N, np.int32)
+    P = np.zeros(B, np.int32)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    ids = torch.empty((B, N, k), dtype=torch.int32, device="cuda")
+    vals = torch.empty((B, N, k), dtype=torch.float32, device="cuda")
+    outs = [torch.empty((B, N), dtype=torch.int32, device="cuda") for _ in range(4)]
+    out_tok = torch.empty((B, N + 1), dtype=torch.int32, device="cuda")
+    sample = torch.empty((B, N), dtype=torch.int32, device="cuda")
+    acc = torch.empty(B, dtype=torch.int32, device="cuda")
+    table = t(np.full((V, k), -1, np.int32))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gt.gt_verify_sample_commit(t(logits), t(tokens), t(parent), t(n), t(P), B, N, V, k, 0.9, 5, 2,
+                               ids, vals, sample, acc, outs[0], out_tok, outs[1], outs[2], table,
+                               err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    gi, gv = np_(ids), np_(vals)
+    for b in range(B):
+        for v in range(N):
+            wi, wv = oracle.vocab_topk(logits[b, v], k)
+            assert gi[b, v].tolist() == list(wi), (b, v)
+            assert np.array_equal(gv[b, v].view(np.uint32), np.float32(wv).view(np.uint32)), (b, v)

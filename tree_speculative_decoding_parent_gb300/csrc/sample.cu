@@ -21,14 +21,18 @@
 // an exact score in the usual case. The (order key, lowest index) pairs meet in warp
 // shuffles, shared memory and the cluster's distributed shared memory. With one Philox
 // block per 16 logits the pass is close to the bound of reading the logits once.
-#include <cooperative_groups.h>
+//
+// The same pass can also form the row's top-k of the unscaled logits (the table update at
+// T > 0 keeps the target's k most likely tokens): with KK > 0 every thread also filters its
+// units against the top-k threshold of topk_cluster_kernel (the KK-th largest of the CTA's
+// lane maxima, here over each thread's first unit), and the candidates meet through the
+// same warp selection and cluster merge. The logits are then read once for both results.
 #include <math.h>
 
 #include "gt_internal.cuh"
 #include "launch.cuh"
 #include "sample.cuh"
-
-namespace cg = cooperative_groups;
+#include "topk_common.cuh"
 
 namespace gt {
 
@@ -190,11 +194,15 @@ __device__ __forceinline__ uint64_t score_mask(const SmpRow &R, const float (&z)
   return best;
 }
 
-template <int CL>
+// KK > 0: the row's top-k (k <= KK) of the unscaled logits goes to ids / vals as well.
+template <int CL, int KK>
 __global__ void __launch_bounds__(SMP_THREADS, 4)
 sample_cluster_kernel(const float *__restrict__ logits, int row0, int V, float inv_t,
                       uint32_t k0, uint32_t k1, uint32_t step_lo, uint32_t step_hi,
-                      int32_t *__restrict__ sample) {
+                      int32_t *__restrict__ sample, int k, int32_t *__restrict__ ids,
+                      float *__restrict__ vals, int32_t *err) {
+  static_assert(SMP_THREADS == TOPK_THREADS, "the top-k pieces assume 256 threads");
+  constexpr int KS = KK > 0 ? KK : 1;  // array sizes of the top-k state
   pdl_enter();
   __shared__ uint64_t s_warp[SMP_THREADS / 32];
   __shared__ uint32_t s_wz[SMP_THREADS / 32];
@@ -203,7 +211,16 @@ sample_cluster_kernel(const float *__restrict__ logits, int row0, int V, float i
   __shared__ int s_qj[SMP_QCAP];    // candidates found by the streaming pass: index, logit
   __shared__ float s_qz[SMP_QCAP];
   __shared__ int s_qn;
-  if (threadIdx.x == 0) s_qn = 0;
+  __shared__ uint64_t s_tcand[KK > 0 ? TOPK_CAP : 1];  // top-k candidates
+  __shared__ uint64_t s_top[KS];
+  __shared__ uint64_t s_clus[CL * KS];
+  __shared__ uint32_t s_lmax[(SMP_THREADS / 32) * KS];
+  __shared__ uint32_t s_thr;
+  __shared__ int s_tcnt;
+  if (threadIdx.x == 0) {
+    s_qn = 0;
+    s_tcnt = 0;
+  }
   asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
   cg::cluster_group cluster = cg::this_cluster();
   const int crank = (int)cluster.block_rank();
@@ -237,6 +254,35 @@ sample_cluster_kernel(const float *__restrict__ logits, int row0, int V, float i
   int u1 = -1;
   float zn[16];  // the next unit's logits are in flight while this unit is examined
   if (ub + (int)threadIdx.x < ue) load16(ub + (int)threadIdx.x, zn);
+  float tthr = -INFINITY;  // top-k threshold
+  bool nan_seen = false;   // checked builds: a NaN logit is reported as GT_ERR_VALUE
+  if constexpr (KK > 0) {
+    // the KK-th largest of the CTA's lane maxima over each thread's first unit: KK distinct
+    // elements lie at or above it, so nothing below reaches the CTA's top-KK
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t km = 0u;
+    const int u0 = ub + (int)threadIdx.x;
+    if (u0 < ue)
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        if (16 * u0 + e < V) km = max(km, order_key(zn[e]));
+    const uint32_t sorted = warp_sorted_desc(km);
+    if (lane < KK) s_lmax[warp * KK + lane] = sorted;
+    __syncthreads();
+    if (warp == 0) {
+      constexpr int NC = ((SMP_THREADS / 32) * KS + 31) / 32;
+      uint32_t v = 0u;
+#pragma unroll
+      for (int j = 0; j < NC; ++j) {
+        const int q = lane + 32 * j;
+        if (q < (SMP_THREADS / 32) * KK) v = max(v, s_lmax[q]);
+      }
+      const uint32_t kth = __shfl_sync(0xffffffffu, warp_sorted_desc(v), KK - 1);
+      if (lane == 0) s_thr = kth;
+    }
+    __syncthreads();
+    tthr = key_floor(s_thr);
+  }
   for (int u = ub + (int)threadIdx.x; u < ue; u += SMP_THREADS) {
     float z[16];
 #pragma unroll
@@ -252,6 +298,17 @@ sample_cluster_kernel(const float *__restrict__ logits, int row0, int V, float i
       u1 = u;
     } else {
       m2 = fmaxf(m2, um);
+    }
+    if constexpr (KK > 0) {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int j = 16 * u + e;
+        if (GT_CHECK && j < V) nan_seen |= z[e] != z[e];
+        if (j < V && !(z[e] < tthr)) {
+          const int pos = atomicAdd(&s_tcnt, 1);
+          if (pos < TOPK_CAP) s_tcand[pos] = pack_key(order_key(z[e]), j);
+        }
+      }
     }
     uint32_t cand = ff_bytes(a);
     if (u == U16 - 1) cand &= tail_mask;
@@ -270,6 +327,17 @@ sample_cluster_kernel(const float *__restrict__ logits, int row0, int V, float i
     }
   }
   __syncthreads();
+  if constexpr (KK > 0) {
+    // the CTA's top-KK: the candidates, or the exact per-thread lists after an overflow
+    const int tc = s_tcnt;
+    if (tc > TOPK_CAP) {
+      __syncthreads();  // the buffer is reused as scratch
+      topk_exact<KK>(x, 16 * ub, min(16 * ue, V), s_tcand, s_top);
+    } else {
+      select_candidates<KK>(tc, s_tcand, s_top);
+    }
+    GT_CHECKED(!nan_seen, err, GT_ERR_VALUE);
+  }
   const int qn = s_qn;
   for (int i = threadIdx.x; i < min(qn, SMP_QCAP); i += SMP_THREADS)
     best = smp_max(best, smp_pack(R.score(s_qz[i], s_qj[i], 0xFFu), s_qj[i]));
@@ -279,7 +347,10 @@ sample_cluster_kernel(const float *__restrict__ logits, int row0, int V, float i
   uint32_t zk = overflow ? order_key(INFINITY) : order_key(m1);
   // every CTA of the cluster is running after the wait: the first remote write follows it
   asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory");
+  // the top-k lists travel with the first reduction (its cluster barrier publishes them)
+  if constexpr (KK > 0) send_to_leader<KK>(cluster, crank, s_top, s_clus);
   smp_cluster_max<CL>(best, zk, s_warp, s_wz, s_cb[0], s_cz[0], cluster, crank);
+  if constexpr (KK > 0) leader_write<KK, CL>(crank, s_clus, x, R.row, k, ids, vals);
 
   const uint32_t thr = (uint32_t)(best >> 32);
   if (R.can_reach(smp_key_value(zk), thr)) {
@@ -309,16 +380,32 @@ sample_cluster_kernel(const float *__restrict__ logits, int row0, int V, float i
     sample[R.row] = (int32_t)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
 }
 
-template <int CL>
+template <int CL, int KK>
 static int sample_launch_cl(const float *logits, int r0, int nr, int V, float inv_t, uint32_t k0,
-                            uint32_t k1, uint32_t s_lo, uint32_t s_hi, int32_t *sample,
-                            cudaStream_t s) {
-  return launch_cluster(sample_cluster_kernel<CL>, dim3(CL, nr), dim3(SMP_THREADS),
-                        dim3(CL, 1, 1), 0, s, logits, r0, V, inv_t, k0, k1, s_lo, s_hi, sample);
+                            uint32_t k1, uint32_t s_lo, uint32_t s_hi, int32_t *sample, int k,
+                            int32_t *ids, float *vals, int32_t *err, cudaStream_t s) {
+  return launch_cluster(sample_cluster_kernel<CL, KK>, dim3(CL, nr), dim3(SMP_THREADS),
+                        dim3(CL, 1, 1), 0, s, logits, r0, V, inv_t, k0, k1, s_lo, s_hi, sample,
+                        k, ids, vals, err);
+}
+
+template <int KK>
+static int sample_launch_k(const float *logits, int r0, int nr, int V, float inv_t, uint32_t k0,
+                           uint32_t k1, uint32_t s_lo, uint32_t s_hi, int32_t *sample, int k,
+                           int32_t *ids, float *vals, int32_t *err, int cl, cudaStream_t s) {
+  switch (cl) {
+    case 1: return sample_launch_cl<1, KK>(logits, r0, nr, V, inv_t, k0, k1, s_lo, s_hi, sample, k, ids, vals, err, s);
+    case 2: return sample_launch_cl<2, KK>(logits, r0, nr, V, inv_t, k0, k1, s_lo, s_hi, sample, k, ids, vals, err, s);
+    case 4: return sample_launch_cl<4, KK>(logits, r0, nr, V, inv_t, k0, k1, s_lo, s_hi, sample, k, ids, vals, err, s);
+    default:
+      return sample_launch_cl<SMP_CLUSTER, KK>(logits, r0, nr, V, inv_t, k0, k1, s_lo, s_hi, sample, k,
+                                               ids, vals, err, s);
+  }
 }
 
 int sample_launch(const float *logits, int rows, int V, float temperature, uint64_t seed,
-                  uint64_t step, int32_t *sample, cudaStream_t s) {
+                  uint64_t step, int32_t *sample, cudaStream_t s, int k, int32_t *ids,
+                  float *vals, int32_t *err) {
   if (!(temperature > 0.0f) || !isfinite(temperature)) return GT_ERR_ARG;
   const float inv_t = 1.0f / temperature;  // one IEEE float division
   if (!isfinite(inv_t)) return GT_ERR_ARG;
@@ -328,7 +415,8 @@ int sample_launch(const float *logits, int rows, int V, float temperature, uint6
   int dev = 0, sms = 148, per_sm = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sample_cluster_kernel<SMP_CLUSTER>,
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm,
+                                                    sample_cluster_kernel<SMP_CLUSTER, 16>,
                                                     SMP_THREADS, 0) != cudaSuccess) {
     (void)cudaGetLastError();
     sms = 148;
@@ -341,14 +429,10 @@ int sample_launch(const float *logits, int rows, int V, float temperature, uint6
   const uint32_t s_lo = (uint32_t)step, s_hi = (uint32_t)(step >> 32);
   for (int r0 = 0; r0 < rows; r0 += 65535) {
     const int nr = min(65535, rows - r0);
-    int rc;
-    switch (cl) {
-      case 1: rc = sample_launch_cl<1>(logits, r0, nr, V, inv_t, k0, k1, s_lo, s_hi, sample, s); break;
-      case 2: rc = sample_launch_cl<2>(logits, r0, nr, V, inv_t, k0, k1, s_lo, s_hi, sample, s); break;
-      case 4: rc = sample_launch_cl<4>(logits, r0, nr, V, inv_t, k0, k1, s_lo, s_hi, sample, s); break;
-      default:
-        rc = sample_launch_cl<SMP_CLUSTER>(logits, r0, nr, V, inv_t, k0, k1, s_lo, s_hi, sample, s);
-    }
+    const int rc =
+        !ids ? sample_launch_k<0>(logits, r0, nr, V, inv_t, k0, k1, s_lo, s_hi, sample, k, ids, vals, err, cl, s)
+        : k <= 8 ? sample_launch_k<8>(logits, r0, nr, V, inv_t, k0, k1, s_lo, s_hi, sample, k, ids, vals, err, cl, s)
+                 : sample_launch_k<16>(logits, r0, nr, V, inv_t, k0, k1, s_lo, s_hi, sample, k, ids, vals, err, cl, s);
     if (rc != GT_OK) return rc;
   }
   return GT_OK;
