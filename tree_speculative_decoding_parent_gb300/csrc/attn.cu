@@ -243,20 +243,27 @@ template <> __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16 
   *reinterpret_cast<uint2 *>(dst) = u;
 }
 
+// The merged output row w = (b, i, hq): the LSE-weighted sum of its segment's partial
+// rows. Rows of nodes at or past n are zero. Returns false, having written nothing, when
+// the flag *merge_flag (ws.hdr[1]; null: not read) says that no segment needs the combine.
 template <typename T>
-__global__ void __launch_bounds__(256)
-attn_combine_kernel(const int32_t *__restrict__ n_nodes, int B, int N, int Hq, int Hkv,
-                    AttnWs ws, T *__restrict__ O) {
-  pdl_enter();
+__device__ __forceinline__ bool combine_row(int w, int lane, const int32_t *__restrict__ n_nodes,
+                                            int N, int Hq, int Hkv, const AttnWs &ws,
+                                            T *__restrict__ O, bool direct_single,
+                                            const int *merge_flag) {
   constexpr int PRE = 16;  // partials per lane loaded before any arithmetic
-  const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  if (w >= B * N * Hq) return;
   const int hq = w % Hq, i = (w / Hq) % N, b = w / (Hq * N);
   const int g = Hq / Hkv, h = hq / g, r = i * g + (hq - h * g);
   T *dst = O + (size_t)w * ATTN_D + lane * 4;
-  // the node count and the segment's pieces are independent loads: issue them together
+  // the node count, the segment's pieces and (first row) the flag are independent loads:
+  // the empty asm needs all three before the tests below, so they leave together instead
+  // of the tests' branches holding the first two back
   const int n = n_nodes[b];
   int2 sg = ws.seg[b * Hkv + h];
+  const int merge = merge_flag ? *merge_flag : 1;
+  asm volatile("" ::"r"(n), "r"(sg.x), "r"(sg.y), "r"(merge));
+  if (merge == 0) return false;
+  if (direct_single && sg.y == 1) return true;  // written by the attention kernel
   if (i >= n) sg = make_int2(0, 0);  // rows past the tree are zero
   const size_t stride = (size_t)ws.rows_pad * ATTN_D;
   const float *src = ws.opart + ((size_t)sg.x * ws.rows_pad + r) * ATTN_D + lane * 4;
@@ -302,8 +309,26 @@ attn_combine_kernel(const int32_t *__restrict__ n_nodes, int B, int N, int Hq, i
     acc = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
   }
   store4<T>(dst, acc);
+  return true;
 }
 
+// One warp per output row, grid-stride. direct_single: the attention kernel itself wrote
+// the rows of segments that have exactly one piece (the tcgen05 kernel does), so those
+// rows are skipped, and when no segment has another count (ws.hdr[1] == 0) the launch has
+// nothing to do.
+template <typename T>
+__global__ void __launch_bounds__(256, 2)
+attn_combine_kernel(const int32_t *__restrict__ n_nodes, int B, int N, int Hq, int Hkv,
+                    AttnWs ws, T *__restrict__ O, int direct_single) {
+  pdl_enter();
+  const int rows = B * N * Hq, lane = threadIdx.x & 31;
+  const int *flag = direct_single ? ws.hdr + 1 : nullptr;  // read with the first row only
+  for (int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < rows;
+       w += (gridDim.x * blockDim.x) >> 5) {
+    if (!combine_row<T>(w, lane, n_nodes, N, Hq, Hkv, ws, O, direct_single != 0, flag)) return;
+    flag = nullptr;
+  }
+}
 static int device_sms() {
   static std::atomic<int> cache[64];  // per device; an SM count never changes
   int dev = 0, sms = 0;
@@ -422,7 +447,8 @@ GT_API int gt_tree_attn(const void *Q, const void *K, const void *V, const uint6
   const int grid_pieces = S < Gs ? Gs : Gs + S;
   int rc;
   if (tc) {
-    rc = attn_tc_launch(Q, K, V, mask, sa, B, N, Hq, Hkv, Lcap, scale, ws, grid_pieces, err, s);
+    rc = attn_tc_launch(Q, K, V, mask, sa, B, N, Hq, Hkv, Lcap, scale, ws, grid_pieces, O, err,
+                        s);
   } else {
     static SmemAttr attr_f32;
     rc = ensure_smem(attn_simt_kernel<float>, (int)SIMT_SMEM, attr_f32,
@@ -433,11 +459,12 @@ GT_API int gt_tree_attn(const void *Q, const void *K, const void *V, const uint6
                 prefix_len, n_nodes, N, Hq, Hkv, Lcap, scale, sa, ws, err);
   }
   if (rc != GT_OK) return rc;
+  // a warp per output row, at most two CTAs of 8 warps per SM (one resident wave)
   const int warps = B * N * Hq;
-  const dim3 cgrid(ceil_div(warps * 32, 256));
+  const dim3 cgrid(max(1, min(ceil_div(warps, 8), 2 * G)));
   if (dtype == GT_F32)
     return launch(attn_combine_kernel<float>, cgrid, dim3(256), 0, s, n_nodes, B, N, Hq, Hkv, ws,
-                  (float *)O);
+                  (float *)O, 0);
   return launch(attn_combine_kernel<__nv_bfloat16>, cgrid, dim3(256), 0, s, n_nodes, B, N, Hq,
-                Hkv, ws, (__nv_bfloat16 *)O);
+                Hkv, ws, (__nv_bfloat16 *)O, tc ? 1 : 0);
 }

@@ -19,7 +19,7 @@ constexpr int ATTN_MAX_N = 64;     // tree nodes per request (one mask word)
 constexpr int ATTN_ROWS_PAD = 128; // partial rows are padded to a multiple of this
 
 struct AttnWs {
-  int *hdr;          // [0] number of pieces
+  int *hdr;          // [0] number of pieces; [1] 1 if some segment's piece count is not 1
   int2 *seg;         // (first piece, piece count) per segment
   float *lse;        // [maxp][rows_pad] natural-log LSE per partial row
   float *opart;      // [maxp][rows_pad][d] normalised partial O
@@ -66,10 +66,11 @@ struct SchedArgs {
 // of non-empty segments, tau is raised to the smallest value whose pieces all fit in one
 // wave of G (sum_s cnt_s <= G), so that no piece waits for a second wave. Returns piece p
 // as (segment, tile_begin,
-// tile_end, 0), or segment -1 when p is past the last piece, and (when np_out is given)
-// the node count and prefix length of the piece's request. The CTA at blockIdx (0,0)
-// also publishes (first piece, count) of every segment and the piece total into `ws`, and
-// reports invalid requests. Every thread of the CTA must call it (it synchronises).
+// tile_end, piece count of the segment), or segment -1 when p is past the last piece, and
+// (when np_out is given) the node count and prefix length of the piece's request. The CTA
+// at blockIdx (0,0) also publishes (first piece, count) of every segment, the piece total
+// and whether any segment has a piece count other than 1 into `ws`, and reports invalid
+// requests. Every thread of the CTA must call it (it synchronises).
 __device__ __forceinline__ int4 schedule_piece(const SchedArgs &a, int p, AttnWs ws,
                                                int32_t *err, int2 *np_out = nullptr) {
   constexpr int CH = 4;  // segments per thread kept in registers; more are recomputed
@@ -129,13 +130,17 @@ __device__ __forceinline__ int4 schedule_piece(const SchedArgs &a, int p, AttnWs
         if (p >= off && p < off + cnt) {
           // floor(t * j / cnt) = (t / cnt) * j + floor((t % cnt) * j / cnt), in 32 bits
           const int j = p - off, q = t / cnt, r = t - q * cnt;
-          s_piece = make_int4(lane, q * j + r * j / cnt, q * (j + 1) + r * (j + 1) / cnt, 0);
+          s_piece = make_int4(lane, q * j + r * j / cnt, q * (j + 1) + r * (j + 1) / cnt, cnt);
           s_np = make_int2(n, P);
         }
       }
       const int total = __shfl_sync(0xffffffffu, incl, 31);
+      const bool multi = __any_sync(0xffffffffu, lane < S && cnt != 1);
       if (lane == 0) {
-        if (publisher) ws.hdr[0] = total;
+        if (publisher) {
+          ws.hdr[0] = total;
+          ws.hdr[1] = multi ? 1 : 0;
+        }
         if (p >= total) s_piece = make_int4(-1, 0, 0, 0);
       }
     }
@@ -186,6 +191,7 @@ __device__ __forceinline__ int4 schedule_piece(const SchedArgs &a, int p, AttnWs
       }
       // pieces in segment order: segments lane + 32 i for i = 0, 1, ...
       int base = 0;
+      bool multi = false;
 #pragma unroll
       for (int i = 0; i < CH; ++i) {
         const int s = lane + 32 * i;
@@ -199,16 +205,21 @@ __device__ __forceinline__ int4 schedule_piece(const SchedArgs &a, int p, AttnWs
         const int off = base + incl - cnt;
         if (s < S) {
           if (publisher) ws.seg[s] = make_int2(off, cnt);
+          multi = multi || cnt != 1;
           if (p >= off && p < off + cnt) {
             // floor(t * j / cnt) = (t / cnt) * j + floor((t % cnt) * j / cnt), in 32 bits
             const int j = p - off, t = wt[i], q = t / cnt, r = t - q * cnt;
-            s_piece = make_int4(s, q * j + r * j / cnt, q * (j + 1) + r * (j + 1) / cnt, 0);
+            s_piece = make_int4(s, q * j + r * j / cnt, q * (j + 1) + r * (j + 1) / cnt, cnt);
             s_np = make_int2(wn[i], wP[i]);
           }
         }
         base += __shfl_sync(0xffffffffu, incl, 31);
       }
-      if (publisher && lane == 0) ws.hdr[0] = base;
+      multi = __any_sync(0xffffffffu, multi);
+      if (publisher && lane == 0) {
+        ws.hdr[0] = base;
+        ws.hdr[1] = multi ? 1 : 0;
+      }
     }
     __syncthreads();
     if (np_out) *np_out = s_np;
@@ -277,6 +288,7 @@ __device__ __forceinline__ int4 schedule_piece(const SchedArgs &a, int p, AttnWs
     off += (w < warp) ? s_scan[w] : 0;
     total += s_scan[w];
   }
+  bool multi = false;
   for (int s = c0; s < c1; ++s) {
     int t = 0;
 #pragma unroll
@@ -285,16 +297,21 @@ __device__ __forceinline__ int4 schedule_piece(const SchedArgs &a, int p, AttnWs
     if (s >= c0 + CH) t = tiles_of(s);
     const int cnt = (t + tau - 1) / tau;
     if (publisher) ws.seg[s] = make_int2(off, cnt);
+    multi = multi || cnt != 1;
     if (p >= off && p < off + cnt) {
       const int j = p - off;
-      s_piece = make_int4(s, (int)((long long)t * j / cnt), (int)((long long)t * (j + 1) / cnt), 0);
+      s_piece = make_int4(s, (int)((long long)t * j / cnt), (int)((long long)t * (j + 1) / cnt),
+                          cnt);
       const int b = s / a.Hkv;
       s_np = make_int2(a.n_nodes[b], a.prefix_len[b]);
     }
     off += cnt;
   }
-  if (publisher && tid == 0) ws.hdr[0] = total;
-  __syncthreads();
+  const int any_multi = __syncthreads_or(multi);
+  if (publisher && tid == 0) {
+    ws.hdr[0] = total;
+    ws.hdr[1] = any_multi ? 1 : 0;
+  }
   if (np_out) *np_out = s_np;
   return s_piece;
 }

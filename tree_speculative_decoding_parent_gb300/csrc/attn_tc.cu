@@ -347,13 +347,51 @@ __device__ __forceinline__ void write_partial(uint8_t *stage, const CUtensorMap 
   }
 }
 
+// The piece is its segment's only one, so its normalised rows are the output: each
+// softmax thread scales its row by 1 / l, rounds it to bf16 and stores it (zero for nodes at
+// or past n; rows past the segment's g * N are not stored). The combine of a single piece
+// gives the same bits (weight exp(0) = 1, sum 1), so the combine kernel skips these rows.
+// ok: this thread's waits all succeeded. Called by the 128 softmax threads.
+__device__ __forceinline__ void write_final(uint32_t tO, bool ok, float l, int row0, int g,
+                                            int n, int N, int Hq, int h, int b,
+                                            __nv_bfloat16 *__restrict__ O) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = row0 + warp * 32 + lane;
+  if (!__all_sync(0xffffffffu, ok)) return;
+  const int i = r / g, hq = h * g + (r - i * g);
+  const bool exists = r < g * N, live = i < n;
+  const float inv = live && l > 0.f ? 1.f / l : 0.f;
+  uint4 *dst = reinterpret_cast<uint4 *>(O + (((size_t)b * N + i) * Hq + hq) * ATTN_D);
+  tc::tc_fence_after();
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t o[32];
+    tc::tmem_ld32(tO + c * 32, o);  // warp-collective: every lane loads
+    tc::tmem_wait_ld();
+    if (exists) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const __nv_bfloat162 v =
+              __floats2bfloat162_rn(__uint_as_float(o[8 * k + 2 * e]) * inv,
+                                    __uint_as_float(o[8 * k + 2 * e + 1]) * inv);
+          w[e] = *reinterpret_cast<const uint32_t *>(&v);
+        }
+        dst[c * 4 + k] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(TC_THREADS, 1)
 attn_tc_kernel(const __nv_bfloat16 *__restrict__ Qg, const __grid_constant__ CUtensorMap mapK,
                const __grid_constant__ CUtensorMap mapV, const __grid_constant__ CUtensorMap mapO,
                uint32_t q_slice, uint32_t q_bytes, const uint64_t *__restrict__ mask,
                const int32_t *__restrict__ prefix_len, const int32_t *__restrict__ n_nodes,
                int N, int Hq, int Hkv, float scale, int C, int L, SchedArgs sa, AttnWs ws,
-               int32_t *err) {
+               __nv_bfloat16 *__restrict__ O, int32_t *err) {
   using Lay = Smem;
   constexpr int SLOTS = Lay::SLOTS, SLOT_BYTES = Lay::SLOT_BYTES;
   extern __shared__ uint8_t smem_raw[];
@@ -604,7 +642,10 @@ attn_tc_kernel(const __nv_bfloat16 *__restrict__ Qg, const __grid_constant__ CUt
       tc::mbar_arrive(bar.p_full);
     }
     if (ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(bar.o_done, 0, abort));
-    write_partial(base + Lay::RING, &mapO, tO, ok, l, m_used, p, row0, g * n, ws);
+    if (pc.w == 1)
+      write_final(tO, ok, l, row0, g, n, N, Hq, h, b, O);
+    else
+      write_partial(base + Lay::RING, &mapO, tO, ok, l, m_used, p, row0, g * n, ws);
   }
 
   tc::tc_fence_before();
@@ -715,7 +756,7 @@ int attn_tc_pieces(int g, int N) {
 
 int attn_tc_launch(const void *Q, const void *K, const void *V, const uint64_t *mask,
                    const SchedArgs &sa, int B, int N, int Hq, int Hkv, int Lcap, float scale,
-                   const AttnWs &ws, int pieces, int32_t *err, cudaStream_t s) {
+                   const AttnWs &ws, int pieces, void *O, int32_t *err, cudaStream_t s) {
   const int g = Hq / Hkv;
   const int C = cluster_of(g, N), L = loaders_of(C);
   CUtensorMap mK, mV;
@@ -747,7 +788,8 @@ int attn_tc_launch(const void *Q, const void *K, const void *V, const uint64_t *
   // one cluster of C CTAs per piece; the schedule never makes more than `pieces`
   return launch_cluster(attn_tc_kernel, dim3(grid), dim3(TC_THREADS), dim3(C, 1, 1),
                         Smem::BYTES, s, (const __nv_bfloat16 *)Q, mK, mV, mO, q_slice, q_bytes,
-                        mask, sa.prefix_len, sa.n_nodes, N, Hq, Hkv, scale, C, L, sa, ws, err);
+                        mask, sa.prefix_len, sa.n_nodes, N, Hq, Hkv, scale, C, L, sa, ws,
+                        (__nv_bfloat16 *)O, err);
 }
 
 }  // namespace gt

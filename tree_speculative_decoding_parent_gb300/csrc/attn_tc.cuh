@@ -22,6 +22,6 @@ int attn_tc_pieces(int g, int N);
 // schedule's piece count (one cluster is launched per possible piece).
 int attn_tc_launch(const void *Q, const void *K, const void *V, const uint64_t *mask,
                    const SchedArgs &sa, int B, int N, int Hq, int Hkv, int Lcap, float scale,
-                   const AttnWs &ws, int pieces, int32_t *err, cudaStream_t s);
+                   const AttnWs &ws, int pieces, void *O, int32_t *err, cudaStream_t s);
 
 }  // namespace gt
