@@ -189,7 +189,31 @@ __device__ __forceinline__ int4 schedule_piece(const SchedArgs &a, int p, AttnWs
         }
         tau = lo;
       }
-      // pieces in segment order: segments lane + 32 i for i = 0, 1, ...
+      // Piece order. With at most 32 requests, requests are taken by decreasing piece
+      // length (ties: lower index), each request's KV heads in order: a launch of more
+      // pieces than one wave holds then starts its longest pieces first, and the shorter
+      // ones fill in behind them (largest-first list scheduling). Lane b handles request b:
+      // its pieces start after those of every request whose key is larger.
+      const bool by_length = a.B <= 32;
+      int r_off = 0, r_cnt = 0;
+      if (by_length) {
+        int tb = 0;
+        if (lane < a.B) {
+          const int n = a.n_nodes[lane], P = a.prefix_len[lane];
+          const bool ok = n >= 1 && n <= a.N && P >= 0 && (long long)P + n <= (long long)a.Lcap;
+          tb = ok ? (P + n + a.TK - 1) / a.TK : 0;
+        }
+        r_cnt = (tb + tau - 1) / tau;
+        const uint32_t len = r_cnt > 0 ? (uint32_t)((tb + r_cnt - 1) / r_cnt) : 0u;
+        const uint32_t key = lane < a.B ? ((len << 5) | (uint32_t)(31 - lane)) : 0u;
+        const int np = lane < a.B ? r_cnt * a.Hkv : 0;
+        for (int c = 0; c < 32; ++c) {
+          const uint32_t kc = __shfl_sync(0xffffffffu, key, c);
+          const int nc = __shfl_sync(0xffffffffu, np, c);
+          if (kc > key) r_off += nc;
+        }
+      }
+      // pieces in segment order (segments lane + 32 i for i = 0, 1, ...) or by length
       int base = 0;
       bool multi = false;
 #pragma unroll
@@ -202,7 +226,11 @@ __device__ __forceinline__ int4 schedule_piece(const SchedArgs &a, int p, AttnWs
           const int y = __shfl_up_sync(0xffffffffu, incl, o);
           if (lane >= o) incl += y;
         }
-        const int off = base + incl - cnt;
+        int off = base + incl - cnt;
+        if (by_length) {  // request b = s / Hkv: its offset, then h pieces of cnt each
+          const int b = min(s / a.Hkv, 31), h = s - (s / a.Hkv) * a.Hkv;
+          off = __shfl_sync(0xffffffffu, r_off, b) + h * cnt;
+        }
         if (s < S) {
           if (publisher) ws.seg[s] = make_int2(off, cnt);
           multi = multi || cnt != 1;
