@@ -511,6 +511,41 @@ def test_tree_attn_two_cta_cluster_shapes():
                 assert np.all(got[b, n[b]:] == 0.0)
 
 
+def test_tree_attn_more_segments_than_clusters():
+    """Launches with as many segments as resident clusters or more (pieces in several
+    waves, longest first): requests of very unequal length (the long one's segments cut
+    into several pieces, merged by the combine, the short ones' single pieces stored
+    directly), and invalid requests among valid ones (their rows zero, GT_ERR_RANGE
+    reported)."""
+    rng = np.random.default_rng(57)
+    cases = [  # B, N, Hq, Hkv, prefixes, nodes per request, expected error
+        (5, 60, 64, 8, [8000, 100, 100, 100, 100], [60, 7, 1, 30, 60], 0),
+        (6, 60, 64, 8, [300, 300, 4000, 300, 0, 2000], [60, 0, 60, 61, 5, 60], gt.GT_ERR_RANGE),
+        (40, 20, 16, 4, rng.integers(0, 3000, size=40).tolist(),
+         rng.integers(1, 21, size=40).tolist(), 0),
+    ]
+    for B, N, Hq, Hkv, P, nn, want in cases:
+        valid = [1 <= v <= N for v in nn]
+        a, refs, n = _random_attn_case(rng, B, N, Hq, Hkv, P,
+                                        [v if ok else 1 for v, ok in zip(nn, valid)], "bf16")
+        a["n"] = _t(np.array(nn, np.int32))
+        wsb = gt.gt_tree_attn_workspace(B, N, Hq, Hkv, 128, a["Lcap"])
+        ws = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        gt.gt_tree_attn(a["Q"], a["K"], a["V"], a["mask"], a["P"], a["n"], B, N, Hq, Hkv, 128,
+                        a["Lcap"], a["dt"], a["scale"], a["O"], ws, wsb, err)
+        torch.cuda.synchronize()
+        assert err.item() == want, (B, N, Hq, Hkv, err.item())
+        got = a["O"].float().cpu().numpy().astype(np.float64)
+        for b in range(B):
+            if not valid[b]:
+                assert np.all(got[b] == 0.0), (B, b)
+                continue
+            e = float(np.abs(got[b, :n[b]] - refs[b]).max())
+            assert e <= TOL["bf16"], (B, N, Hq, Hkv, b, e)
+            assert np.all(got[b, n[b]:] == 0.0)
+
+
 def _random_attn_case(rng, B, N, Hq, Hkv, P, nn, dtype):
     """Random trees and NaN-tailed caches for gt_tree_attn alone; returns the device
     arguments and the oracle's output per request."""
