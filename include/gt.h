@@ -155,8 +155,8 @@ int gt_tree_mask(const int32_t *parent, const int32_t *n_nodes, const int32_t *p
  * kernel streams K and V through cluster-multicast TMA loads, which this library issues
  * only over the memory of the GPU that runs them.
  * Limits: d = 128, 1 <= N <= 64, Hq % Hkv == 0, (Hq/Hkv)*N <= 512, Lcap >= 1, scale a
- * finite value > 0 (else GT_ERR_ARG); Q, K, V, O 16-byte aligned. Device errors: GT_ERR_RANGE (prefix_len + n_nodes > Lcap,
- * n_nodes outside [1, N], prefix_len < 0). Keys past a request's length are never read
+ * finite value > 0 (else GT_ERR_ARG); Q, K, V, O 16-byte aligned. Device errors:
+ * GT_ERR_RANGE (prefix_len + n_nodes > Lcap, n_nodes outside [1, N], prefix_len < 0). Keys past a request's length are never read
  * into the result (cache rows there may hold anything, NaN included).
  * ------------------------------------------------------------------------------------- */
 size_t gt_tree_attn_workspace(int B, int N, int Hq, int Hkv, int d, int Lcap);
