@@ -523,6 +523,12 @@ def test_tree_attn_more_segments_than_clusters():
         (6, 60, 64, 8, [300, 300, 4000, 300, 0, 2000], [60, 0, 60, 61, 5, 60], gt.GT_ERR_RANGE),
         (40, 20, 16, 4, rng.integers(0, 3000, size=40).tolist(),
          rng.integers(1, 21, size=40).tolist(), 0),
+        # two-CTA clusters, one-warp schedule: 32 requests (pieces ordered by length) and
+        # 40 requests (more than 32: pieces in segment order)
+        (32, 40, 16, 4, rng.integers(0, 4000, size=32).tolist(),
+         rng.integers(1, 41, size=32).tolist(), 0),
+        (40, 20, 16, 2, rng.integers(0, 3000, size=40).tolist(),
+         rng.integers(1, 21, size=40).tolist(), 0),
     ]
     for B, N, Hq, Hkv, P, nn, want in cases:
         valid = [1 <= v <= N for v in nn]
