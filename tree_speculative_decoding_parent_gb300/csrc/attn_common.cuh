@@ -128,9 +128,12 @@ __device__ __forceinline__ int4 schedule_piece(const SchedArgs &a, int p, AttnWs
       if (lane < S) {
         if (publisher) ws.seg[lane] = make_int2(off, cnt);
         if (p >= off && p < off + cnt) {
-          // floor(t * j / cnt) = (t / cnt) * j + floor((t % cnt) * j / cnt), in 32 bits
+          // piece j: tiles [ceil(t j / cnt), ceil(t (j+1) / cnt)), with
+          // ceil(t j / cnt) = (t / cnt) j + ceil((t % cnt) j / cnt) in 32 bits; the longer
+          // pieces come first, so the last one, which holds the masked tail tile, is short
           const int j = p - off, q = t / cnt, r = t - q * cnt;
-          s_piece = make_int4(lane, q * j + r * j / cnt, q * (j + 1) + r * (j + 1) / cnt, cnt);
+          s_piece = make_int4(lane, q * j + (r * j + cnt - 1) / cnt,
+                              q * (j + 1) + (r * (j + 1) + cnt - 1) / cnt, cnt);
           s_np = make_int2(n, P);
         }
       }
@@ -235,9 +238,10 @@ __device__ __forceinline__ int4 schedule_piece(const SchedArgs &a, int p, AttnWs
           if (publisher) ws.seg[s] = make_int2(off, cnt);
           multi = multi || cnt != 1;
           if (p >= off && p < off + cnt) {
-            // floor(t * j / cnt) = (t / cnt) * j + floor((t % cnt) * j / cnt), in 32 bits
+            // tiles [ceil(t j / cnt), ceil(t (j+1) / cnt)), as above
             const int j = p - off, t = wt[i], q = t / cnt, r = t - q * cnt;
-            s_piece = make_int4(s, q * j + r * j / cnt, q * (j + 1) + r * (j + 1) / cnt, cnt);
+            s_piece = make_int4(s, q * j + (r * j + cnt - 1) / cnt,
+                                q * (j + 1) + (r * (j + 1) + cnt - 1) / cnt, cnt);
             s_np = make_int2(wn[i], wP[i]);
           }
         }
@@ -328,8 +332,8 @@ __device__ __forceinline__ int4 schedule_piece(const SchedArgs &a, int p, AttnWs
     multi = multi || cnt != 1;
     if (p >= off && p < off + cnt) {
       const int j = p - off;
-      s_piece = make_int4(s, (int)((long long)t * j / cnt), (int)((long long)t * (j + 1) / cnt),
-                          cnt);
+      s_piece = make_int4(s, (int)(((long long)t * j + cnt - 1) / cnt),
+                          (int)(((long long)t * (j + 1) + cnt - 1) / cnt), cnt);
       const int b = s / a.Hkv;
       s_np = make_int2(a.n_nodes[b], a.prefix_len[b]);
     }
