@@ -112,22 +112,33 @@ static inline int ensure_smem(Kernel kernel, int bytes, SmemAttr &a, const char 
   return GT_OK;
 }
 
-// Exclusive prefix count of `flag` over the threads of a block (flags by thread index).
-// `warp_tot` is shared scratch of 32 ints. Returns the prefix; *total receives the sum.
-__device__ __forceinline__ int block_excl_count(bool flag, int *warp_tot, int *total) {
+// Barrier over the first nthreads threads of the block (named barrier 1; nthreads a
+// multiple of 32), or over the whole block when nthreads is 0.
+__device__ __forceinline__ void sync_threads_n(int nthreads) {
+  if (nthreads == 0)
+    __syncthreads();
+  else
+    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+// Exclusive prefix count of `flag` over the threads of a block (flags by thread index), or
+// over its first nthreads threads (see sync_threads_n). `warp_tot` is shared scratch of 32
+// ints. Returns the prefix; *total receives the sum.
+__device__ __forceinline__ int block_excl_count(bool flag, int *warp_tot, int *total,
+                                                int nthreads = 0) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nwarps = (blockDim.x + 31) >> 5;
+  const int nwarps = ((nthreads ? nthreads : (int)blockDim.x) + 31) >> 5;
   unsigned bal = __ballot_sync(0xffffffffu, flag);
   int in_warp = __popc(bal & ((1u << lane) - 1u));
   if (lane == 0) warp_tot[warp] = __popc(bal);
-  __syncthreads();
+  sync_threads_n(nthreads);
   int off = 0, tot = 0;
   for (int w = 0; w < nwarps; ++w) {
     int c = warp_tot[w];
     off += (w < warp) ? c : 0;
     tot += c;
   }
-  __syncthreads();
+  sync_threads_n(nthreads);
   *total = tot;
   return off + in_warp;
 }

@@ -15,23 +15,25 @@ namespace gt {
 // exact radix select of the K-th largest key (four passes of 8-bit digits through a
 // shared-memory histogram) and a block scan over the nodes that tie with it.
 // s_hist: 256 ints, s_sel: 2 ints, warp_tot: 32 ints of shared scratch. Every thread of
-// the CTA must call it (it synchronises).
+// the CTA must call it (it synchronises), or, with nthreads > 0, every one of the first
+// nthreads threads (named barrier 1; the others hold no node).
 __device__ __forceinline__ bool topk_keys_keep(uint32_t key, int K, int *s_hist, int *s_sel,
-                                               int *warp_tot) {
+                                               int *warp_tot, int nthreads = 0) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int stride = nthreads ? nthreads : (int)blockDim.x;
   int total;
-  (void)block_excl_count(key != 0u, warp_tot, &total);
+  (void)block_excl_count(key != 0u, warp_tot, &total, nthreads);
   if (K <= 0) return false;
   if (total <= K) return key != 0u;
   uint32_t prefix = 0u;  // top bits of the K-th largest key fixed so far
   int kr = K;            // its rank among the keys that share those bits
   for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = tid; i < 256; i += blockDim.x) s_hist[i] = 0;
-    __syncthreads();
+    for (int i = tid; i < 256; i += stride) s_hist[i] = 0;
+    sync_threads_n(nthreads);
     const bool match =
         key != 0u && (shift == 24 || (key >> (shift + 8)) == (prefix >> (shift + 8)));
     if (match) atomicAdd(&s_hist[(key >> shift) & 255u], 1);
-    __syncthreads();
+    sync_threads_n(nthreads);
     if (warp == 0) {
       // lane L holds the digits 255 - 8L down to 248 - 8L: lanes run from high to low
       int c[8], sum = 0;
@@ -60,13 +62,13 @@ __device__ __forceinline__ bool topk_keys_keep(uint32_t key, int K, int *s_hist,
         }
       }
     }
-    __syncthreads();
+    sync_threads_n(nthreads);
     prefix |= (uint32_t)s_sel[0] << shift;
     kr = s_sel[1];
   }
   // prefix is now the K-th largest key; kr of the keys equal to it are kept
   int neq;
-  const int eq_rank = block_excl_count(key != 0u && key == prefix, warp_tot, &neq);
+  const int eq_rank = block_excl_count(key != 0u && key == prefix, warp_tot, &neq, nthreads);
   return key > prefix || (key == prefix && eq_rank < kr);
 }
 

@@ -17,7 +17,7 @@
 
 namespace gt {
 
-__global__ void __launch_bounds__(1024)
+__global__ void __launch_bounds__(1024, 1)
 tree_build_kernel(const float *__restrict__ score, const int32_t *__restrict__ parent_in,
                   const int32_t *__restrict__ tokens_in, const int32_t *__restrict__ n_in,
                   int Nin, const int32_t *__restrict__ keep, const float *__restrict__ thresh,
@@ -28,7 +28,8 @@ tree_build_kernel(const float *__restrict__ score, const int32_t *__restrict__ p
                   int32_t *__restrict__ parent, int32_t *__restrict__ tokens,
                   float *__restrict__ out_score, int32_t *__restrict__ out_old,
                   int32_t *__restrict__ n_nodes, int32_t *__restrict__ depth,
-                  int32_t *__restrict__ pos, uint64_t *__restrict__ mask, int32_t *err) {
+                  int32_t *__restrict__ pos, uint64_t *__restrict__ mask, int32_t *err,
+                  int gw) {
   pdl_enter();
   extern __shared__ int s_dyn[];
   const int Nin4 = (Nin + 3) & ~3;
@@ -40,10 +41,16 @@ tree_build_kernel(const float *__restrict__ score, const int32_t *__restrict__ p
   int *s_tpar = s_tok + N;                            // [Tb]
   int *s_ttok = s_tpar + Tb;                          // [Tb]
   int *s_tnew = s_ttok + Tb;                          // [Tb]
+  int *s_tflag = s_tnew + Tb;                         // [Tb] graft warp: bad template / entry
+  int *s_tdep = s_tflag + Tb;                         // [Tb] graft warp: template depth
   __shared__ int warp_tot[32];
   __shared__ int s_hist[256], s_sel[2];
   __shared__ int s_bad, s_maxd, s_n;
   const int b = blockIdx.x, t = threadIdx.x;
+  // gw: the block's last warp retrieves the graft (one dependent table read per template
+  // level) while the others prune; the prune then synchronises only its own np threads
+  const int np = gw ? (int)blockDim.x - 32 : 0;
+  const bool graft_warp = gw && t >= np;
   const size_t in0 = (size_t)b * Nin, row0 = (size_t)b * N;
   const int n = n_in ? n_in[b] : Nin;
   const int kb = keep[b];
@@ -57,6 +64,7 @@ tree_build_kernel(const float *__restrict__ score, const int32_t *__restrict__ p
   int code = (n < 1 || n > Nin) ? GT_ERR_RANGE : 0;
   int p = -1, tok = -1;
   float s = 0.f;
+  int nk = 0;
   // every global read of the prune and of the graft set-up is issued here, before the
   // first barrier, so that none of them waits for a phase before it
   const float th = thresh ? thresh[b] : -INFINITY;
@@ -64,13 +72,67 @@ tree_build_kernel(const float *__restrict__ score, const int32_t *__restrict__ p
   const int R_b = R[b];
   const int tpar_t = t < T ? tpar[t] : -1;
   const int trank_t = t < T ? trank[t] : 0;
+  if (graft_warp) {
+    // --------------------------------------------- concurrent graft retrieval (one warp)
+    // Template nodes t' < min(R, T, N - nk) fit, nk the kept count. Without a threshold
+    // the prune keeps exactly min(keep, n) nodes (every non-root node competes: a NaN
+    // score fails the monotonicity check); with one, at least the root. Every node up to
+    // that bound is retrieved now, and only the nodes that fit count (errors included).
+    const int lane = t - np;
+    const int nk_min = thresh ? 1 : max(1, min(kb, n));
+    const int rmax = max(0, min(min(R_b, T), N - nk_min));
+    const int rt = tokens_in[in0];  // the root's token: the graft hangs from the root
+    const int rtok = (rt >= 0 && rt < V) ? rt : -1;
+    for (int u = lane; u < rmax; u += 32) {
+      const int tp = tpar[u], rk = trank[u];
+      s_tpar[u] = tp;
+      s_tnew[u] = rk;  // the rank, until the placement reuses the array
+      s_tflag[u] = (tp < -1 || tp >= u || rk < 0 || rk >= k) ? 1 : 0;
+      s_ttok[u] = -1;
+    }
+    __syncwarp();
+    int maxd = 0;
+    for (int u = lane; u < rmax; u += 32) {
+      // parents precede children, so a chain of valid nodes ends at the root; a node with
+      // a bad entry on its chain is never retrieved
+      int d = 0;
+      for (int v = u; v != -1; v = s_tpar[v]) {
+        if (s_tflag[v] & 1) {
+          d = 0;
+          break;
+        }
+        ++d;
+      }
+      s_tdep[u] = d;
+      maxd = max(maxd, d);
+    }
+    maxd = (int)__reduce_max_sync(0xffffffffu, (unsigned)maxd);
+    __syncwarp();
+    for (int L = 1; L <= maxd; ++L) {
+      for (int u = lane; u < rmax; u += 32) {
+        if (s_tdep[u] != L) continue;
+        const int tp = s_tpar[u];
+        const int ptok = tp == -1 ? rtok : s_ttok[tp];
+        int tk = -1;
+        if (ptok >= 0) {
+          tk = table[(size_t)ptok * k + s_tnew[u]];
+          if (tk < -1 || tk >= V) {
+            s_tflag[u] |= 2;  // reported after the prune if the node fits
+            tk = -1;
+          }
+        }
+        s_ttok[u] = tk;
+      }
+      __syncwarp();
+    }
+  } else {
   if (!code && t < n) {
     p = parent_in[in0 + t];
     s = score[in0 + t];
     tok = tokens_in[in0 + t];
     s_score[t] = s;
   }
-  __syncthreads();
+  sync_threads_n(np);
   if (!code && t < n) {
     if (t == 0) {
       if (p != -1) code = GT_ERR_TREE;
@@ -84,7 +146,32 @@ tree_build_kernel(const float *__restrict__ score, const int32_t *__restrict__ p
   const int ke = min(kb, n);
   if (!code && (kb < 1 || ke > N)) code = GT_ERR_RANGE;
   if (code) atomicCAS(&s_bad, 0, code);
+  sync_threads_n(np);
+  if (!s_bad) {
+  // the root is always kept; the other nodes compete for the remaining ke - 1 slots
+  const bool cand = t > 0 && t < n && s >= th;
+  const bool sel = topk_keys_keep(cand ? order_key(s) : 0u, ke - 1, s_hist, s_sel, warp_tot,
+                                  np);
+  const bool kept = (t == 0) || sel;
+  const int newi = block_excl_count(kept, warp_tot, &nk, np);
+  if (t < n) s_new[t] = kept ? newi : -1;
+  sync_threads_n(np);
+  if (kept) {
+    s_par[newi] = (t == 0) ? -1 : s_new[p];
+    s_tok[newi] = tok;
+    if (out_score) out_score[row0 + newi] = s;
+    if (out_old) out_old[row0 + newi] = t;
+  }
+  for (int j = nk + t; j < N; j += (gw ? np : (int)blockDim.x)) {
+    if (out_score) out_score[row0 + j] = 0.f;
+    if (out_old) out_old[row0 + j] = -1;
+  }
+  if (gw && t == 0) s_n = nk;  // for the graft warp, which did not count the kept nodes
+  }
+  }
+  // the prune's tree and (gw) the retrieved tokens are complete for every thread here
   __syncthreads();
+  if (gw) nk = s_n;
   const int bad = s_bad;
   if (bad) {  // as the separate calls: nothing kept, every row padded
     if (t == 0) {
@@ -100,25 +187,6 @@ tree_build_kernel(const float *__restrict__ score, const int32_t *__restrict__ p
     }
     return;
   }
-  // the root is always kept; the other nodes compete for the remaining ke - 1 slots
-  const bool cand = t > 0 && t < n && s >= th;
-  const bool sel = topk_keys_keep(cand ? order_key(s) : 0u, ke - 1, s_hist, s_sel, warp_tot);
-  const bool kept = (t == 0) || sel;
-  int nk;
-  const int newi = block_excl_count(kept, warp_tot, &nk);
-  if (t < n) s_new[t] = kept ? newi : -1;
-  __syncthreads();
-  if (kept) {
-    s_par[newi] = (t == 0) ? -1 : s_new[p];
-    s_tok[newi] = tok;
-    if (out_score) out_score[row0 + newi] = s;
-    if (out_old) out_old[row0 + newi] = t;
-  }
-  for (int j = nk + t; j < N; j += blockDim.x) {
-    if (out_score) out_score[row0 + j] = 0.f;
-    if (out_old) out_old[row0 + j] = -1;
-  }
-  __syncthreads();
 
   // ---------------------------------------------------------------- phase B: graft
   // the retrieved tree hangs from the anchor: the root, or (Graft-TAIL) the last kept node
@@ -147,6 +215,9 @@ tree_build_kernel(const float *__restrict__ score, const int32_t *__restrict__ p
   int n_final = nk;
   if (s_bad) {  // the kept tree stays; no graft
     if (t == 0) set_err(err, s_bad);
+  } else if (gw) {
+    // the graft warp retrieved every node that fits; a bad table entry among them counts
+    if (active && (s_tflag[t] & 2)) set_err(err, GT_ERR_TREE);
   } else {
     int dep = 0;
     if (active) {
@@ -170,6 +241,8 @@ tree_build_kernel(const float *__restrict__ score, const int32_t *__restrict__ p
       }
       __syncthreads();
     }
+  }
+  if (!s_bad) {
     const bool alive = active && s_ttok[t] >= 0;
     int cnt;
     const int gi = block_excl_count(alive, warp_tot, &cnt);
@@ -241,10 +314,14 @@ GT_API int gt_tree_build(const float *score, const int32_t *parent_in, const int
     return GT_ERR_ARG;
   const int W = (N + 63) / 64;
   const int Tb = T > 0 ? T : 1;
-  const int threads = (max(max(Nin, N), Tb) + 31) / 32 * 32;
-  const size_t smem = sizeof(int) * ((size_t)((Nin + 3) & ~3) + Nin + 2 * (size_t)N + 3 * (size_t)Tb);
+  int threads = (max(max(Nin, N), Tb) + 31) / 32 * 32;
+  // a graft hung from the root does not depend on the prune: one more warp retrieves it
+  // meanwhile (a Graft-TAIL anchor is only known once the prune is done)
+  const int gw = (T > 0 && !anchor && threads + 32 <= 1024) ? 1 : 0;
+  threads += 32 * gw;
+  const size_t smem = sizeof(int) * ((size_t)((Nin + 3) & ~3) + Nin + 2 * (size_t)N + 5 * (size_t)Tb);
   return launch(tree_build_kernel, dim3(B), dim3(threads), smem, (cudaStream_t)stream, score,
                 parent_in, tokens_in, n_in, Nin, keep, thresh, tpar, trank, T, R, anchor, table, V, k,
                 prefix_len, N, W, parent, tokens, out_score, out_old_idx, n_nodes, depth, pos,
-                mask, err);
+                mask, err, gw);
 }
