@@ -193,14 +193,15 @@ static int topk_launch(const float *logits, int rows, int V, int k, int32_t *ids
 // With one target draw per node (T > 0) the walk enters only the first child carrying the
 // draw: a later sibling with the same token as an earlier one can never be entered, so its
 // token is replaced by -1 (draws are never negative). Every thread of the block calls this.
-__device__ __forceinline__ void shadow_duplicates(const int *s_par, int *s_tok, int n, int v) {
+__device__ __forceinline__ void shadow_duplicates(const int *s_par, int *s_tok, int n, int v,
+                                                  int nthreads = 0) {
   bool shadowed = false;
   if (v < n && v > 0)
     for (int w = 1; w < v && !shadowed; ++w)
       shadowed = s_par[w] == s_par[v] && s_tok[w] == s_tok[v];
-  __syncthreads();
+  sync_threads_n(nthreads);
   if (shadowed) s_tok[v] = -1;
-  __syncthreads();
+  sync_threads_n(nthreads);
 }
 
 __global__ void __launch_bounds__(1024)
@@ -470,6 +471,168 @@ walk_update_kernel(const int32_t *__restrict__ tokens, const int32_t *__restrict
   }
 }
 
+// walk_update_kernel with the two halves of its work on separate warps, concurrently: the
+// first nw threads (a thread per node) walk the tree and write the path, the tokens and the
+// commit indices, synchronising on named barrier 1; the next nu threads stage every
+// request's verified tokens, hash them and write this request's table rows, on named
+// barrier 2. The table rows depend on every node's tokens and top-k, not on the walk, so
+// neither half waits for the other. Same results and error codes as walk_update_kernel.
+__global__ void __launch_bounds__(1024, 1)
+walk_update_split_kernel(const int32_t *__restrict__ tokens, const int32_t *__restrict__ parent,
+                         const int32_t *__restrict__ n_nodes,
+                         const int32_t *__restrict__ prefix_len, int B, int N, int k,
+                         const int32_t *__restrict__ topk_id, const int32_t *__restrict__ sample,
+                         int32_t *__restrict__ acc_len, int32_t *__restrict__ path,
+                         int32_t *__restrict__ out_tok, int32_t *__restrict__ kv_src,
+                         int32_t *__restrict__ kv_dst, int32_t *__restrict__ table, int V, int hs,
+                         int nw, int32_t *err) {
+  pdl_enter();
+  extern __shared__ int s_w[];
+  int *s_par = s_w, *s_tok = s_w + N, *s_am = s_w + 2 * N, *s_path = s_w + 3 * N;
+  int *s_all = s_w + 4 * N;  // [B*N] verified tokens of every request (-1: none)
+  int *s_hk = s_all + B * N, *s_hv = s_hk + hs;  // [hs] hash keys (tokens) and last indices
+  __shared__ uint32_t s_best[32];
+  __shared__ int s_bad;
+  const int b = blockIdx.x, total = B * N;
+  const size_t row0 = (size_t)b * N;
+  if ((int)threadIdx.x < nw) {
+    // ----------------------------------------------------------------------- the walk
+    const int v = threadIdx.x;
+    int p_v = -1, tok_v = -1, am_v = -1;
+    if (v < N) {
+      p_v = parent[row0 + v];
+      tok_v = tokens[row0 + v];
+      am_v = sample ? sample[row0 + v] : topk_id[(row0 + v) * k];
+    }
+    const int n = n_nodes[b], P = prefix_len[b];
+    if (v == 0) s_bad = 0;
+    int code = (n < 1 || n > N) ? GT_ERR_RANGE : 0;
+    if (!code && v < n) {
+      const int p = p_v;
+      s_par[v] = p;
+      s_tok[v] = tok_v;
+      s_am[v] = am_v;
+      if (v == 0 ? (p != -1) : (p < 0 || p >= v)) code = GT_ERR_TREE;
+      if (GT_CHECK && (tok_v < 0 || tok_v >= V)) code = GT_ERR_TREE;
+    }
+    sync_threads_n(nw);
+    if (code) atomicCAS(&s_bad, 0, code);
+    sync_threads_n(nw);
+    const int bad = s_bad;
+    int L = 0, vstar = 0;
+    if (!bad) {
+      if (sample) shadow_duplicates(s_par, s_tok, n, v, nw);
+      uint32_t key = 0u;
+      if (v < n) {
+        bool acc = true;
+        int d = 0;
+        for (int u = v; u != 0; u = s_par[u]) {
+          acc = acc && (s_tok[u] == s_am[s_par[u]]);
+          ++d;
+        }
+        if (acc) key = ((uint32_t)d << 16) | (0xFFFFu - (uint32_t)v);
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) key = max(key, __shfl_xor_sync(0xffffffffu, key, o));
+      if ((v & 31) == 0) s_best[v >> 5] = key;
+      sync_threads_n(nw);
+      uint32_t best = 0u;
+      for (int w = 0; w < (nw >> 5); ++w) best = max(best, s_best[w]);
+      L = (int)(best >> 16);
+      vstar = (int)(0xFFFFu - (best & 0xFFFFu));
+      if (v <= L) {
+        int u = vstar;
+        for (int s = 0; s < L - v; ++s) u = s_par[u];
+        s_path[v] = u;
+      }
+      sync_threads_n(nw);
+    } else if (v == 0) {
+      set_err(err, bad);
+    }
+    if (v < N) {
+      const bool on = !bad && v <= L;
+      path[row0 + v] = on ? s_path[v] : -1;
+      kv_src[row0 + v] = on ? P + s_path[v] : -1;
+      kv_dst[row0 + v] = on ? P + v : -1;
+    }
+    for (int j = v; j < N + 1; j += nw) {
+      int t = -1;
+      if (!bad && j < L) t = s_tok[s_path[j + 1]];
+      else if (!bad && j == L) t = s_am[vstar];
+      out_tok[(size_t)b * (N + 1) + j] = t;
+    }
+    if (v == 0) acc_len[b] = bad ? 0 : L;
+    return;
+  }
+  // ------------------------------------------------------------ the successor-table rows
+  const int u = threadIdx.x - nw, nu = (int)blockDim.x - nw;
+  // this thread's node's top-k row waits in registers for its table row
+  int krow[16];
+  if (u < N) {
+#pragma unroll
+    for (int c = 0; c < 16; ++c) krow[c] = c < k ? topk_id[(row0 + u) * k + c] : -1;
+  }
+  for (int i = u; i < hs; i += nu) s_hk[i] = s_hv[i] = -1;
+  for (int i = u; i < total; i += nu) {
+    const int bb = i / N, vv = i - bb * N;
+    const int nn = n_nodes[bb];
+    int t = -1;
+    if (nn >= 0 && nn <= N && vv < nn) {
+      t = tokens[i];
+      if (t < 0 || t >= V) {
+        if (bb == b) set_err(err, GT_ERR_TREE);
+        t = -1;
+      }
+    } else if ((nn < 0 || nn > N) && vv == 0 && bb == b) {
+      set_err(err, GT_ERR_RANGE);
+    }
+    s_all[i] = t;
+  }
+  asm volatile("bar.sync 2, %0;" ::"r"(nu) : "memory");
+  auto slot0 = [&](int t) { return (int)(((uint32_t)t * 2654435761u) & (uint32_t)(hs - 1)); };
+  if (hs > 0) {  // hs is a power of two above B*N, so every probe sequence ends
+    for (int i = u; i < total; i += nu) {
+      const int t = s_all[i];
+      if (t < 0) continue;
+      for (int h = slot0(t);; h = (h + 1) & (hs - 1)) {
+        const int prev = atomicCAS(&s_hk[h], -1, t);
+        if (prev == -1 || prev == t) {
+          atomicMax(&s_hv[h], i);
+          break;
+        }
+      }
+    }
+    asm volatile("bar.sync 2, %0;" ::"r"(nu) : "memory");
+  }
+  for (int vv = u; vv < N; vv += nu) {
+    const int i = b * N + vv;
+    const int t = s_all[i];
+    if (t < 0) continue;
+    bool last = true;
+    if (hs > 0) {
+      int h = slot0(t);
+      while (s_hk[h] != t) h = (h + 1) & (hs - 1);
+      last = s_hv[h] == i;
+    } else {
+      for (int j = i + 1; j < total; ++j)
+        if (s_all[j] == t) {
+          last = false;
+          break;
+        }
+    }
+    if (!last) continue;
+    int32_t *dst = table + (size_t)t * k;
+    if (vv == u) {
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        if (c < k) dst[c] = krow[c];
+    } else {
+      const int32_t *src = topk_id + (size_t)i * k;
+      for (int c = 0; c < k; ++c) dst[c] = src[c];
+    }
+  }
+}
+
 }  // namespace gt
 
 using namespace gt;
@@ -534,6 +697,8 @@ static int walk_update_launch(const int32_t *tokens, const int32_t *parent,
   // a thread per node for the walk; up to 512 threads so that the B*N verified tokens every
   // CTA stages and hashes take a few load rounds instead of B rounds
   const int threads = (max(N, min(B * N, 512)) + 31) / 32 * 32;
+  // the walk and the table rows on separate warps when both fit in one block
+  const int nw = (N + 31) / 32 * 32, nu = (min(B * N, 512) + 31) / 32 * 32;
   size_t smem = sizeof(int) * (4 * (size_t)N + (size_t)B * N);
   // the token hash: a power of two at least twice B*N, when it fits (else the scan)
   int hs = 1;
@@ -541,6 +706,17 @@ static int walk_update_launch(const int32_t *tokens, const int32_t *parent,
   if (smem + 2 * sizeof(int) * (size_t)hs > 160 * 1024)
     hs = 0;
   smem += 2 * sizeof(int) * (size_t)hs;
+  if (nw + nu <= 1024) {
+    if (smem > 48 * 1024) {
+      static SmemAttr attr;
+      const int rc = ensure_smem(walk_update_split_kernel, (int)smem, attr,
+                                 "cudaFuncSetAttribute(walk_update_split_kernel)");
+      if (rc != GT_OK) return rc;
+    }
+    return launch(walk_update_split_kernel, dim3(B), dim3(nw + nu), smem, s, tokens, parent,
+                  n_nodes, prefix_len, B, N, k, topk_id, sample, acc_len, path, out_tok, kv_src,
+                  kv_dst, table, V, hs, nw, err);
+  }
   if (smem > 48 * 1024) {
     static SmemAttr attr;
     const int rc = ensure_smem(walk_update_kernel, (int)smem, attr,
