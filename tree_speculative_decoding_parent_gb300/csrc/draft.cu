@@ -33,7 +33,7 @@ frontier_kernel(const float *__restrict__ score, const int32_t *__restrict__ n_n
                 const int32_t *__restrict__ pool_lo, uint8_t *__restrict__ visited, int W,
                 int32_t *__restrict__ frontier, int32_t *__restrict__ n_frontier, int32_t *err) {
   pdl_enter();
-  __shared__ int s_hist[256], s_sel[2], warp_tot[32];
+  __shared__ int s_hist[256], s_sel[3], warp_tot[32];
   __shared__ uint32_t s_key[DRAFT_MAX_W];
   __shared__ int s_idx[DRAFT_MAX_W];
   const int b = blockIdx.x, v = threadIdx.x;

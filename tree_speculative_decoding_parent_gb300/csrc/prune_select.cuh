@@ -12,9 +12,13 @@ namespace gt {
 // candidate, larger key = better, see order_key), keeps the K with the largest keys, equal
 // keys going to the smaller thread index. Node v is kept iff fewer than K candidates have a
 // larger key, or an equal key and a smaller index: the rank rule, found in O(n) by an
-// exact radix select of the K-th largest key (four passes of 8-bit digits through a
-// shared-memory histogram) and a block scan over the nodes that tie with it.
-// s_hist: 256 ints, s_sel: 2 ints, warp_tot: 32 ints of shared scratch. Every thread of
+// exact radix select of the K-th largest key (up to four passes of 8-bit digits through a
+// shared-memory histogram) and a block scan over the nodes that tie with it. The select
+// stops after the first pass whose chosen digit bucket is taken whole (its count equals
+// the rank still to fill): then exactly K candidates have top bits at or above the
+// bucket's, every one of them has fewer than K better keys, and every other candidate
+// has at least K, so the rank rule keeps exactly those and no tie is left to break.
+// s_hist: 256 ints, s_sel: 3 ints, warp_tot: 32 ints of shared scratch. Every thread of
 // the CTA must call it (it synchronises), or, with nthreads > 0, every one of the first
 // nthreads threads (named barrier 1; the others hold no node).
 __device__ __forceinline__ bool topk_keys_keep(uint32_t key, int K, int *s_hist, int *s_sel,
@@ -56,6 +60,7 @@ __device__ __forceinline__ bool topk_keys_keep(uint32_t key, int K, int *s_hist,
           if (acc + c[i] >= kr) {
             s_sel[0] = 255 - 8 * lane - i;
             s_sel[1] = kr - acc;
+            s_sel[2] = c[i];
             break;
           }
           acc += c[i];
@@ -65,6 +70,8 @@ __device__ __forceinline__ bool topk_keys_keep(uint32_t key, int K, int *s_hist,
     sync_threads_n(nthreads);
     prefix |= (uint32_t)s_sel[0] << shift;
     kr = s_sel[1];
+    if (s_sel[2] == kr)  // the bucket is taken whole (the same decision in every thread)
+      return key != 0u && (key >> shift) >= (prefix >> shift);
   }
   // prefix is now the K-th largest key; kr of the keys equal to it are kept
   int neq;

@@ -44,7 +44,7 @@ tree_build_kernel(const float *__restrict__ score, const int32_t *__restrict__ p
   int *s_tflag = s_tnew + Tb;                         // [Tb] graft warp: bad template / entry
   int *s_tdep = s_tflag + Tb;                         // [Tb] graft warp: template depth
   __shared__ int warp_tot[32];
-  __shared__ int s_hist[256], s_sel[2];
+  __shared__ int s_hist[256], s_sel[3];
   __shared__ int s_bad, s_maxd, s_n;
   const int b = blockIdx.x, t = threadIdx.x;
   // gw: the block's last warp retrieves the graft (one dependent table read per template

@@ -35,7 +35,7 @@ prune_kernel(const float *__restrict__ score, const int32_t *__restrict__ parent
   const int Nin4 = (Nin + 3) & ~3;
   int *s_new = reinterpret_cast<int *>(s_score + Nin4);  // [Nin]
   __shared__ int warp_tot[32];
-  __shared__ int s_hist[256], s_sel[2];
+  __shared__ int s_hist[256], s_sel[3];
   __shared__ int s_bad;
   const int b = blockIdx.x, v = threadIdx.x;
   const size_t in0 = (size_t)b * Nin, out0 = (size_t)b * Nout;
