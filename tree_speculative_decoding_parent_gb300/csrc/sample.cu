@@ -300,14 +300,22 @@ sample_cluster_kernel(const float *__restrict__ logits, int row0, int V, float i
       m2 = fmaxf(m2, um);
     }
     if constexpr (KK > 0) {
+      // the unit's elements not below tthr (NaN included) as a bit mask, then the rare set bits
+      uint32_t tm = 0u;
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
-        const int j = 16 * u + e;
-        if (GT_CHECK && j < V) nan_seen |= z[e] != z[e];
-        if (j < V && !(z[e] < tthr)) {
-          const int pos = atomicAdd(&s_tcnt, 1);
-          if (pos < TOPK_CAP) s_tcand[pos] = pack_key(order_key(z[e]), j);
-        }
+        if (GT_CHECK && 16 * u + e < V) nan_seen |= z[e] != z[e];
+        tm |= !(z[e] < tthr) ? 1u << e : 0u;
+      }
+      if (u == U16 - 1) tm &= tail_mask;
+      while (tm) {
+        const int e = __ffs(tm) - 1;
+        tm &= tm - 1u;
+        float v = 0.0f;
+#pragma unroll
+        for (int c = 0; c < 16; ++c) v = c == e ? z[c] : v;
+        const int pos = atomicAdd(&s_tcnt, 1);
+        if (pos < TOPK_CAP) s_tcand[pos] = pack_key(order_key(v), 16 * u + e);
       }
     }
     uint32_t cand = ff_bytes(a);
@@ -357,8 +365,10 @@ sample_cluster_kernel(const float *__restrict__ logits, int row0, int V, float i
     // pass 2 (the same decision in every CTA): the elements that can still reach thr. When
     // no other unit's maximum can, only the unit of the part's largest logit is scored.
     const bool one = thr > 1u && !overflow && !R.can_reach(m2, thr);
-    for (int u = one ? u1 : ub + (int)threadIdx.x; u >= 0 && u < ue;
-         u = one ? -1 : u + SMP_THREADS) {
+    // can_reach is monotone in z: when the part's largest logit m1 cannot reach thr, no
+    // element of its unit can (and with `one`, no element of the other units either)
+    const int ustart = one ? (R.can_reach(m1, thr) ? u1 : -1) : ub + (int)threadIdx.x;
+    for (int u = ustart; u >= 0 && u < ue; u = one ? -1 : u + SMP_THREADS) {
       float z[16];
       load16(u, z);
       // the bound SMP_GB holds for non-candidates only: after an overflow the candidates
