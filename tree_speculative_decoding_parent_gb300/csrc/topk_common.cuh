@@ -162,18 +162,42 @@ __device__ __forceinline__ void topk_exact(const float *x, int b, int e, uint64_
   __syncthreads();
 }
 
-// The CTA's top-KK of cnt <= TOPK_CAP candidates, by warp 0, into s_top. Every thread of
-// the CTA calls it (it synchronises).
+// The CTA's top-KK of cnt <= TOPK_CAP candidates into s_top (s_top[r] = the r-th best, 0 past
+// the last candidate). Up to TOPK_RANKED candidates (the usual few dozen): packed words are
+// unique, so a candidate's rank is the number of candidates above it, and every thread ranks
+// candidates t, t + blockDim.x, ... against all of them (broadcast shared-memory reads, no
+// dependent rounds); the top KK place themselves. The ranking work grows with the square of
+// the count, so larger counts go to warp 0's KK selection rounds over 8 or 16 candidates per
+// lane. Every thread of the CTA calls it (it synchronises).
+constexpr int TOPK_RANKED = 128;
 template <int KK>
 __device__ __forceinline__ void select_candidates(int cnt, const uint64_t *s_cand,
                                                   uint64_t *s_top) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (warp == 0) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (cnt <= TOPK_RANKED) {
+    for (int t = tid; t < cnt; t += blockDim.x) {
+      const uint64_t c = s_cand[t];
+      int r0 = 0, r1 = 0;
+      int j = 0;
+      for (; j + 1 < cnt; j += 2) {
+        r0 += s_cand[j] > c;
+        r1 += s_cand[j + 1] > c;
+      }
+      if (j < cnt) r0 += s_cand[j] > c;
+      const int r = r0 + r1;
+      if (r < KK) s_top[r] = c;
+    }
+    if (tid < KK && tid >= cnt) s_top[tid] = 0ull;
+  } else if (warp == 0) {
     uint64_t bb;
-    if (cnt <= 64) {  // the usual case: a few dozen candidates
-      uint64_t c[2] = {lane < cnt ? s_cand[lane] : 0ull,
-                       lane + 32 < cnt ? s_cand[lane + 32] : 0ull};
-      bb = warp_select<KK, 2>(c);
+    if (cnt <= 256) {
+      uint64_t c[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int q = lane + 32 * j;
+        c[j] = q < cnt ? s_cand[q] : 0ull;
+      }
+      bb = warp_select<KK, 8>(c);
     } else {
       constexpr int NC = TOPK_CAP / 32;
       uint64_t c[NC];
