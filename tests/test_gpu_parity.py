@@ -656,3 +656,66 @@ def test_tree_attn_refuses_memory_of_other_places():
     torch.cuda.synchronize()
     assert err.item() == 0
     _check_attn_out(a, refs, n, "bf16", "device memory")
+
+
+@pytest.mark.parametrize("R", [60, 180])
+def test_tree_build_grafts_large_templates(R):
+    """The fused tree build retrieves the graft on its extra warp while the prune runs; with
+    60 template nodes a lane holds up to two of them in registers, with 180 the warp loops
+    over them.
+    Random draft trees (monotone scores), empty table entries, a root-only request; the
+    result against the oracle's prune -> graft -> mask. Then out-of-range table entries
+    report GT_ERR_TREE and are retrieved as empty."""
+    from workload import default_template
+    rng = np.random.default_rng(R)
+    V, k, B, Nin, N = 300, 8, 3, 256, 200
+    tpar, trank = default_template(R, k)
+    table = rng.integers(0, V, size=(V, k)).astype(np.int32)
+    table[rng.random((V, k)) < 0.25] = -1
+    parent_in = np.full((B, Nin), -1, np.int32)
+    tokens_in = rng.integers(0, V, size=(B, Nin)).astype(np.int32)
+    score_in = np.ones((B, Nin), np.float32)
+    for b in range(B):
+        for v in range(1, Nin):
+            p = int(rng.integers(0, v))
+            parent_in[b, v] = p
+            score_in[b, v] = np.float32(score_in[b, p] * rng.uniform(0.3, 0.99))
+    keep = np.array([10, 20, 1], np.int32)
+    Rv = np.array([R, R - 7, R], np.int32)
+    prefix = np.array([100, 0, 5000], np.int32)
+    W = (N + 63) // 64
+
+    def run(tab):
+        outs = dict(parent=torch.empty((B, N), dtype=torch.int32, device="cuda"),
+                    tokens=torch.empty((B, N), dtype=torch.int32, device="cuda"),
+                    score=torch.empty((B, N), dtype=torch.float32, device="cuda"),
+                    old_idx=torch.empty((B, N), dtype=torch.int32, device="cuda"),
+                    n_nodes=torch.empty((B,), dtype=torch.int32, device="cuda"),
+                    depth=torch.empty((B, N), dtype=torch.int32, device="cuda"),
+                    pos=torch.empty((B, N), dtype=torch.int32, device="cuda"),
+                    mask=torch.empty((B, N, W), dtype=torch.int64, device="cuda"))
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        gt.gt_tree_build(_t(score_in), _t(parent_in), _t(tokens_in), None, B, Nin, _t(keep), None,
+                         _t(tpar), _t(trank), R, _t(Rv), None, _t(tab), V, k, _t(prefix), N,
+                         outs["parent"], outs["tokens"], outs["score"], outs["old_idx"],
+                         outs["n_nodes"], outs["depth"], outs["pos"], outs["mask"], err)
+        torch.cuda.synchronize()
+        return type("Out", (), outs), int(err.item())
+
+    got, err = run(table)
+    assert err == 0
+    want = oracle.step_tree_phase(parent_in, tokens_in, score_in, [Nin] * B, keep, None, tpar,
+                                  trank, Rv, table, prefix, N)
+    compare_tree(got, want)
+    assert int(np_(got.n_nodes)[0]) > 10 + R // 4  # the graft did fill slots
+    # out-of-range entries: reported, and retrieved as empty (the oracle's -1)
+    bad = table.copy()
+    hit = rng.random((V, k)) < 0.05
+    bad[hit] = V + 3
+    got, err = run(bad)
+    assert err == gt.GT_ERR_TREE
+    clean = bad.copy()
+    clean[hit] = -1
+    want = oracle.step_tree_phase(parent_in, tokens_in, score_in, [Nin] * B, keep, None, tpar,
+                                  trank, Rv, clean, prefix, N)
+    compare_tree(got, want)

@@ -83,47 +83,113 @@ tree_build_kernel(const float *__restrict__ score, const int32_t *__restrict__ p
     const int rmax = max(0, min(min(R_b, T), N - nk_min));
     const int rt = tokens_in[in0];  // the root's token: the graft hangs from the root
     const int rtok = (rt >= 0 && rt < V) ? rt : -1;
-    for (int u = lane; u < rmax; u += 32) {
-      const int tp = tpar[u], rk = trank[u];
-      s_tpar[u] = tp;
-      s_tnew[u] = rk;  // the rank, until the placement reuses the array
-      s_tflag[u] = (tp < -1 || tp >= u || rk < 0 || rk >= k) ? 1 : 0;
-      s_ttok[u] = -1;
-    }
-    __syncwarp();
-    int maxd = 0;
-    for (int u = lane; u < rmax; u += 32) {
-      // parents precede children, so a chain of valid nodes ends at the root; a node with
-      // a bad entry on its chain is never retrieved
-      int d = 0;
-      for (int v = u; v != -1; v = s_tpar[v]) {
-        if (s_tflag[v] & 1) {
-          d = 0;
-          break;
-        }
-        ++d;
+    // a retrieved entry outside [-1, V) is bad: flagged (reported after the prune if the node
+    // fits) and retrieved as -1
+    auto publish = [&](int u, int tk) {
+      if (tk < -1 || tk >= V) {
+        s_tflag[u] |= 2;
+        tk = -1;
       }
-      s_tdep[u] = d;
-      maxd = max(maxd, d);
-    }
-    maxd = (int)__reduce_max_sync(0xffffffffu, (unsigned)maxd);
-    __syncwarp();
-    for (int L = 1; L <= maxd; ++L) {
-      for (int u = lane; u < rmax; u += 32) {
-        if (s_tdep[u] != L) continue;
-        const int tp = s_tpar[u];
-        const int ptok = tp == -1 ? rtok : s_ttok[tp];
-        int tk = -1;
-        if (ptok >= 0) {
-          tk = table[(size_t)ptok * k + s_tnew[u]];
-          if (tk < -1 || tk >= V) {
-            s_tflag[u] |= 2;  // reported after the prune if the node fits
-            tk = -1;
-          }
+      s_ttok[u] = tk;
+    };
+    constexpr int GPL = 2;  // template nodes per lane held in registers (rmax <= 64)
+    if (rmax <= 32 * GPL) {
+      // lane holds nodes u = lane + 32 j; every read of a level leaves at once, and level 1
+      // (children of the root, which need only the root's row) as soon as the template
+      // entries are in, before the depths are known
+      int tpv[GPL], rkv[GPL], tkv[GPL], dv[GPL];
+#pragma unroll
+      for (int j = 0; j < GPL; ++j) {
+        const int u = lane + 32 * j;
+        tpv[j] = u < rmax ? tpar[u] : -1;
+        rkv[j] = u < rmax ? trank[u] : 0;
+      }
+#pragma unroll
+      for (int j = 0; j < GPL; ++j) {
+        const int u = lane + 32 * j;
+        tkv[j] = -1;
+        if (u < rmax) {
+          const int tp = tpv[j], rk = rkv[j];
+          const bool badt = tp < -1 || tp >= u || rk < 0 || rk >= k;
+          s_tpar[u] = tp;
+          s_tflag[u] = badt ? 1 : 0;
+          if (!badt && tp == -1 && rtok >= 0) tkv[j] = table[(size_t)rtok * k + rk];
         }
-        s_ttok[u] = tk;
+      }
+#pragma unroll
+      for (int j = 0; j < GPL; ++j) {
+        const int u = lane + 32 * j;
+        if (u < rmax) publish(u, tkv[j]);
       }
       __syncwarp();
+      // parents precede children, so a chain of valid nodes ends at the root; a node with a
+      // bad entry on its chain is never retrieved
+      int maxd = 0;
+#pragma unroll
+      for (int j = 0; j < GPL; ++j) {
+        const int u = lane + 32 * j;
+        int d = 0;
+        if (u < rmax)
+          for (int v = u; v != -1; v = s_tpar[v]) {
+            if (s_tflag[v] & 1) {
+              d = 0;
+              break;
+            }
+            ++d;
+          }
+        dv[j] = d;
+        maxd = max(maxd, d);
+      }
+      maxd = (int)__reduce_max_sync(0xffffffffu, (unsigned)maxd);
+      for (int L = 2; L <= maxd; ++L) {
+        bool at[GPL];
+#pragma unroll
+        for (int j = 0; j < GPL; ++j) {
+          at[j] = dv[j] == L;
+          tkv[j] = -1;
+          if (at[j]) {
+            const int ptok = s_ttok[tpv[j]];
+            if (ptok >= 0) tkv[j] = table[(size_t)ptok * k + rkv[j]];
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < GPL; ++j)
+          if (at[j]) publish(lane + 32 * j, tkv[j]);
+        __syncwarp();
+      }
+    } else {
+      for (int u = lane; u < rmax; u += 32) {
+        const int tp = tpar[u], rk = trank[u];
+        s_tpar[u] = tp;
+        s_tnew[u] = rk;  // the rank, until the placement reuses the array
+        s_tflag[u] = (tp < -1 || tp >= u || rk < 0 || rk >= k) ? 1 : 0;
+        s_ttok[u] = -1;
+      }
+      __syncwarp();
+      int maxd = 0;
+      for (int u = lane; u < rmax; u += 32) {
+        int d = 0;
+        for (int v = u; v != -1; v = s_tpar[v]) {
+          if (s_tflag[v] & 1) {
+            d = 0;
+            break;
+          }
+          ++d;
+        }
+        s_tdep[u] = d;
+        maxd = max(maxd, d);
+      }
+      maxd = (int)__reduce_max_sync(0xffffffffu, (unsigned)maxd);
+      __syncwarp();
+      for (int L = 1; L <= maxd; ++L) {
+        for (int u = lane; u < rmax; u += 32) {
+          if (s_tdep[u] != L) continue;
+          const int tp = s_tpar[u];
+          const int ptok = tp == -1 ? rtok : s_ttok[tp];
+          publish(u, ptok >= 0 ? table[(size_t)ptok * k + s_tnew[u]] : -1);
+        }
+        __syncwarp();
+      }
     }
   } else {
   if (!code && t < n) {
