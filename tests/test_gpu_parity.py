@@ -665,7 +665,9 @@ def test_tree_build_grafts_large_templates(R):
     over them.
     Random draft trees (monotone scores), empty table entries, a root-only request; the
     result against the oracle's prune -> graft -> mask. Then out-of-range table entries
-    report GT_ERR_TREE and are retrieved as empty."""
+    report GT_ERR_TREE and are retrieved as empty; a bad template entry among a request's
+    fitting nodes, or a bad root token, reports GT_ERR_TREE and keeps that request's pruned
+    tree alone, while a bad entry past a request's fitting nodes leaves its graft as it is."""
     from workload import default_template
     rng = np.random.default_rng(R)
     V, k, B, Nin, N = 300, 8, 3, 256, 200
@@ -685,7 +687,7 @@ def test_tree_build_grafts_large_templates(R):
     prefix = np.array([100, 0, 5000], np.int32)
     W = (N + 63) // 64
 
-    def run(tab):
+    def run(tab, trk=trank, toks=tokens_in):
         outs = dict(parent=torch.empty((B, N), dtype=torch.int32, device="cuda"),
                     tokens=torch.empty((B, N), dtype=torch.int32, device="cuda"),
                     score=torch.empty((B, N), dtype=torch.float32, device="cuda"),
@@ -695,8 +697,8 @@ def test_tree_build_grafts_large_templates(R):
                     pos=torch.empty((B, N), dtype=torch.int32, device="cuda"),
                     mask=torch.empty((B, N, W), dtype=torch.int64, device="cuda"))
         err = torch.zeros(1, dtype=torch.int32, device="cuda")
-        gt.gt_tree_build(_t(score_in), _t(parent_in), _t(tokens_in), None, B, Nin, _t(keep), None,
-                         _t(tpar), _t(trank), R, _t(Rv), None, _t(tab), V, k, _t(prefix), N,
+        gt.gt_tree_build(_t(score_in), _t(parent_in), _t(toks), None, B, Nin, _t(keep), None,
+                         _t(tpar), _t(trk), R, _t(Rv), None, _t(tab), V, k, _t(prefix), N,
                          outs["parent"], outs["tokens"], outs["score"], outs["old_idx"],
                          outs["n_nodes"], outs["depth"], outs["pos"], outs["mask"], err)
         torch.cuda.synchronize()
@@ -718,4 +720,24 @@ def test_tree_build_grafts_large_templates(R):
     clean[hit] = -1
     want = oracle.step_tree_phase(parent_in, tokens_in, score_in, [Nin] * B, keep, None, tpar,
                                   trank, Rv, clean, prefix, N)
+    compare_tree(got, want)
+    # bad template entries: inside every request's fitting nodes, then past request 1's
+    for u_bad, graft in ((5, [0, 0, 0]), (R - 1, [0, R - 7, 0])):
+        trk = np.array(trank, np.int32).copy()
+        trk[u_bad] = k  # a rank outside the table row
+        got, err = run(table, trk=trk)
+        assert err == gt.GT_ERR_TREE, u_bad
+        want = oracle.step_tree_phase(parent_in, tokens_in, score_in, [Nin] * B, keep, None, tpar,
+                                      trank, np.array(graft, np.int32), table, prefix, N)
+        compare_tree(got, want)
+    # a root token outside the vocabulary: request 1 keeps its pruned tree alone
+    toks = tokens_in.copy()
+    toks[1, 0] = V + 1
+    got, err = run(table, toks=toks)
+    assert err == gt.GT_ERR_TREE
+    # (the oracle refuses the bad token outright: its trees with the clean token and no graft
+    # for request 1, whose root token is copied as given)
+    want = oracle.step_tree_phase(parent_in, tokens_in, score_in, [Nin] * B, keep, None, tpar,
+                                  trank, np.array([R, 0, R], np.int32), table, prefix, N)
+    want["tokens"][1, 0] = V + 1
     compare_tree(got, want)

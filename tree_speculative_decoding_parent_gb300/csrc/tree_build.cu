@@ -9,6 +9,7 @@
 // (cumulative path score, global prune to Bver); "浙江大学、阿里巴巴联手破解AI推理瓶颈" §二
 // (successor-table retrieval by a template into the freed slots; flatten, tree position ids
 // and mask) and §四 (static slot count per request in batched serving).
+#include <limits.h>
 #include <math.h>
 
 #include "gt_internal.cuh"
@@ -46,6 +47,7 @@ tree_build_kernel(const float *__restrict__ score, const int32_t *__restrict__ p
   __shared__ int warp_tot[32];
   __shared__ int s_hist[256], s_sel[3];
   __shared__ int s_bad, s_maxd, s_n;
+  __shared__ int s_gtot, s_fbad, s_grmax;  // graft warp: retrieved count, first bad template node
   const int b = blockIdx.x, t = threadIdx.x;
   // gw: the block's last warp retrieves the graft (one dependent table read per template
   // level) while the others prune; the prune then synchronises only its own np threads
@@ -191,6 +193,24 @@ tree_build_kernel(const float *__restrict__ score, const int32_t *__restrict__ p
         __syncwarp();
       }
     }
+    // for the placement after the join: the exclusive prefix counts of the retrieved nodes
+    // (s_tnew, no longer the ranks), their total, and the first node with a bad template
+    // entry; the fitting count r <= rmax, so prefixes up to r are the ones the join needs
+    int base = 0, fb = INT_MAX;
+    for (int u0 = 0; u0 < rmax; u0 += 32) {
+      const int u = u0 + lane;
+      const bool got = u < rmax && s_ttok[u] >= 0;
+      const unsigned ba = __ballot_sync(0xffffffffu, got);
+      const unsigned bb = __ballot_sync(0xffffffffu, u < rmax && (s_tflag[u] & 1));
+      if (u < rmax) s_tnew[u] = base + __popc(ba & ((1u << lane) - 1u));
+      base += __popc(ba);
+      if (bb && fb == INT_MAX) fb = u0 + __ffs(bb) - 1;
+    }
+    if (lane == 0) {
+      s_gtot = base;
+      s_fbad = fb;
+      s_grmax = rmax;
+    }
   } else {
   if (!code && t < n) {
     p = parent_in[in0 + t];
@@ -255,6 +275,29 @@ tree_build_kernel(const float *__restrict__ score, const int32_t *__restrict__ p
   }
 
   // ---------------------------------------------------------------- phase B: graft
+  int nf_gw = 0;  // graft warp mode: the final count, the same in every thread
+  if (gw) {
+    // The graft warp retrieved, flagged and counted every template node that can fit; the
+    // r = min(R, N - nk, T) that do fit hang from the root. A bad root token, or a bad
+    // template entry among them, keeps the pruned tree alone (as the separate calls do);
+    // otherwise a bad table entry among them is reported. Every thread decides alike.
+    const int root_tok = s_tok[0];
+    const int r = max(0, min(min(R_b, N - nk), T));
+    int n_final = nk;
+    if (root_tok < 0 || root_tok >= V || s_fbad < r) {
+      if (t == 0) set_err(err, GT_ERR_TREE);
+    } else {
+      if (t < r && (s_tflag[t] & 2)) set_err(err, GT_ERR_TREE);
+      if (t < r && s_ttok[t] >= 0) {
+        const int gi = s_tnew[t];
+        s_par[nk + gi] = (tpar_t == -1) ? 0 : nk + s_tnew[tpar_t];
+        s_tok[nk + gi] = s_ttok[t];
+      }
+      n_final = nk + (r < s_grmax ? s_tnew[r] : s_gtot);
+    }
+    // kept in a register: a slower thread may still be reading the kept count from s_n
+    nf_gw = n_final;
+  } else {
   // the retrieved tree hangs from the anchor: the root, or (Graft-TAIL) the last kept node
   int a = 0;
   code = 0;
@@ -281,9 +324,6 @@ tree_build_kernel(const float *__restrict__ score, const int32_t *__restrict__ p
   int n_final = nk;
   if (s_bad) {  // the kept tree stays; no graft
     if (t == 0) set_err(err, s_bad);
-  } else if (gw) {
-    // the graft warp retrieved every node that fits; a bad table entry among them counts
-    if (active && (s_tflag[t] & 2)) set_err(err, GT_ERR_TREE);
   } else {
     int dep = 0;
     if (active) {
@@ -321,10 +361,11 @@ tree_build_kernel(const float *__restrict__ score, const int32_t *__restrict__ p
     n_final = nk + cnt;
   }
   if (t == 0) s_n = n_final;
+  }
   __syncthreads();
 
   // ---------------------------------------------------------------- phase C: mask
-  const int nf = s_n;
+  const int nf = gw ? nf_gw : s_n;
   for (int v = t; v < N; v += blockDim.x) {
     const size_t o = row0 + v;
     uint64_t *mrow = mask + o * W;
