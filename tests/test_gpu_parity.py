@@ -741,3 +741,91 @@ def test_tree_build_grafts_large_templates(R):
                                   trank, np.array([R, 0, R], np.int32), table, prefix, N)
     want["tokens"][1, 0] = V + 1
     compare_tree(got, want)
+
+
+def _select_stop(scores, K):
+    """Where the radix select of the prune settles for the given candidate scores (host model
+    of its stop rule, used only to check that the cases below reach every stop): the pass
+    (1-4) after which the K-th largest key's digit bucket is taken whole, 5 when the final
+    tie count decides, 0 when no selection is needed."""
+    b = np.asarray(scores, np.float32).view(np.uint32).astype(np.uint64)
+    b = np.where(b == 0x80000000, 0, b)
+    key = np.where(b & 0x80000000, ~b & 0xFFFFFFFF, b | 0x80000000)
+    if K <= 0 or len(key) <= K:
+        return 0
+    prefix, kr = 0, K
+    for p, shift in enumerate((24, 16, 8, 0), 1):
+        sel = key if p == 1 else key[(key >> (shift + 8)) == (prefix >> (shift + 8))]
+        digits = (sel >> shift) & 255
+        acc = 0
+        for d in range(255, -1, -1):
+            c = int((digits == d).sum())
+            if acc + c >= kr:
+                prefix |= d << shift
+                kr -= acc
+                if c == kr:
+                    return p
+                break
+            acc += c
+    return 5
+
+
+def test_prune_select_stops_at_every_pass():
+    """Keys built so that the prune's radix select settles after each of its four passes or
+    only through the final tie count, for K from 1 to 200: star trees (every node a child of
+    the root, so any scores are monotone), gt_prune_topB and the fused gt_tree_build against
+    the oracle's best-first prune."""
+    rng = np.random.default_rng(21)
+    Nin, Nout = 400, 256
+    n = Nin - 1
+    families = {
+        "spread": lambda: np.float32(10.0 ** rng.uniform(-30, 30, n)),
+        "one_octave": lambda: np.float32(1.0 + rng.random(n)),
+        "shared_16_bits": lambda: np.float32(1.0 + rng.integers(0, 4096, n) * 2.0 ** -20),
+        "shared_24_bits": lambda: np.float32(1.0 + rng.integers(0, 128, n) * 2.0 ** -23),
+        "ties": lambda: np.float32(rng.choice([0.5, 0.25, 0.125], n)),
+    }
+    cases = []
+    for name, gen in families.items():
+        for K in (1, 7, 23, 62, 200):
+            cases.append((name, K, gen()))
+    stops = {_select_stop(s, K - 1) for _, K, s in cases}
+    assert {1, 2, 3, 4, 5} <= stops, stops
+    B = len(cases)
+    parent = np.zeros((B, Nin), np.int32)
+    parent[:, 0] = -1
+    score = np.ones((B, Nin), np.float32)
+    for b, (_, _, s) in enumerate(cases):
+        score[b, 1:] = s
+    tokens = rng.integers(0, 1000, size=(B, Nin)).astype(np.int32)
+    keep = np.array([K for _, K, _ in cases], np.int32)
+    outs = [torch.empty((B, Nout), dtype=dt, device="cuda")
+            for dt in (torch.int32, torch.int32, torch.float32, torch.int32)]
+    n_out = torch.empty(B, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gt.gt_prune_topB(_t(score), _t(parent), _t(tokens), None, B, Nin, _t(keep), None, Nout, *outs,
+                     n_out, err)
+    # the fused build with no template: prune, then mask
+    W = (Nout + 63) // 64
+    f = dict(parent=torch.empty((B, Nout), dtype=torch.int32, device="cuda"),
+             tokens=torch.empty((B, Nout), dtype=torch.int32, device="cuda"),
+             score=torch.empty((B, Nout), dtype=torch.float32, device="cuda"),
+             old_idx=torch.empty((B, Nout), dtype=torch.int32, device="cuda"),
+             n_nodes=torch.empty((B,), dtype=torch.int32, device="cuda"),
+             depth=torch.empty((B, Nout), dtype=torch.int32, device="cuda"),
+             pos=torch.empty((B, Nout), dtype=torch.int32, device="cuda"),
+             mask=torch.empty((B, Nout, W), dtype=torch.int64, device="cuda"))
+    table = np.zeros((1000, 8), np.int32)
+    gt.gt_tree_build(_t(score), _t(parent), _t(tokens), None, B, Nin, _t(keep), None, None, None, 0,
+                     _t(np.zeros(B, np.int32)), None, _t(table), 1000, 8,
+                     _t(np.zeros(B, np.int32)), Nout, f["parent"], f["tokens"], f["score"],
+                     f["old_idx"], f["n_nodes"], f["depth"], f["pos"], f["mask"], err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    for b, (name, K, _) in enumerate(cases):
+        p, t, s, o = oracle.prune_topB(score[b], parent[b], tokens[b], Nin, K)
+        m = len(p)
+        for got_n, got_p, got_o in ((n_out, outs[0], outs[3]), (f["n_nodes"], f["parent"], f["old_idx"])):
+            assert np_(got_n)[b] == m, (name, K)
+            assert np_(got_o)[b, :m].tolist() == o, (name, K)
+            assert np_(got_p)[b, :m].tolist() == p, (name, K)
