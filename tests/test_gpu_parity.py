@@ -829,3 +829,47 @@ def test_prune_select_stops_at_every_pass():
             assert np_(got_n)[b] == m, (name, K)
             assert np_(got_o)[b, :m].tolist() == o, (name, K)
             assert np_(got_p)[b, :m].tolist() == p, (name, K)
+
+
+@pytest.mark.parametrize("fused_sampler", [False, True], ids=["topk", "draws+topk"])
+def test_vocab_topk_candidate_counts_of_every_selection_tier(fused_sampler):
+    """Rows of 151,936 logits, each CTA's part (8 per row) holding c copies of 5.0, a value no
+    other element reaches: the CTA's threshold is 5.0 and its candidates are those c copies,
+    so c picks the selection tier (ranked up to 128, warp rounds over 8 or 16 candidates per
+    lane up to 256 or 512, the exact per-thread lists beyond). The top-k (the 8 lowest
+    indices holding 5.0) against the oracle, from gt_vocab_topk and from the sampler's pass
+    of gt_verify_sample_commit."""
+    rng = np.random.default_rng(31)
+    V, k, CL = 151936, 8, 8
+    counts = [40, 100, 128, 129, 200, 256, 257, 400, 512, 513, 700]
+    rows = len(counts)
+    x = (rng.standard_normal((rows, V)) * 0.5).astype(np.float32)
+    V4 = V // 4
+    for r, c in enumerate(counts):
+        for part in range(CL):
+            b, e = 4 * (V4 * part // CL), 4 * (V4 * (part + 1) // CL)
+            x[r, rng.choice(np.arange(b, e), size=c, replace=False)] = 5.0
+    ids = torch.full((rows, k), -7, dtype=torch.int32, device="cuda")
+    vals = torch.empty((rows, k), dtype=torch.float32, device="cuda")
+    if not fused_sampler:
+        gt.gt_vocab_topk(_t(x), rows, V, k, ids, vals)
+    else:
+        # one request of `rows` nodes (a chain), the draws at T = 1.0 beside the top-k
+        B, N = 1, rows
+        parent = np.arange(-1, N - 1, dtype=np.int32)[None]
+        tokens = rng.integers(0, V, size=(B, N)).astype(np.int32)
+        outs = [torch.empty((B, N), dtype=torch.int32, device="cuda") for _ in range(4)]
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        gt.gt_verify_sample_commit(_t(x[None]), _t(tokens), _t(parent),
+                                   _t(np.array([N], np.int32)), _t(np.zeros(1, np.int32)), B, N,
+                                   V, k, 1.0, 3, 1, ids, vals,
+                                   torch.empty((B, N), dtype=torch.int32, device="cuda"),
+                                   torch.empty((B,), dtype=torch.int32, device="cuda"), outs[0],
+                                   torch.empty((B, N + 1), dtype=torch.int32, device="cuda"),
+                                   outs[1], outs[2], _t(np.full((V, k), -1, np.int32)), err)
+    torch.cuda.synchronize()
+    gi, gv = np_(ids), np_(vals)
+    for r in range(rows):
+        wi, wv = oracle.vocab_topk(x[r], k)
+        assert gi[r].tolist() == wi.tolist(), counts[r]
+        assert np.array_equal(gv[r].view(np.uint32), wv.view(np.uint32)), counts[r]
