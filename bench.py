@@ -541,9 +541,13 @@ def run_gpu(args):
                          "calls": f"{len(attn_ms)} calls, one per {ATTN_EVENT_EVERY} steps of a "
                                   f"{attn_steps}-step graph, events on the launch stream (the "
                                   "call then loses its overlap with the tree build)"},
-                     "traffic": _traffic_record(f"tree_attn/config{args.config}"),
+                     # DRAM bytes of one call (both kernels) recorded by ncu with the caches
+                     # as the step leaves them; the flushed figure re-reads the partial rows
+                     "traffic": _traffic_record(f"tree_attn/config{args.config}",
+                                                "live_bytes_per_launch"),
                      "traffic_attn_kernel": _traffic_record(f"tree_attn/config{args.config}",
-                                                            "attn_tc_kernel_bytes")},
+                                                            "live_attn_tc_kernel_bytes"),
+                     "traffic_flushed": _traffic_record(f"tree_attn/config{args.config}")},
         "e2e": {"value": ne / e2e_s, "unit": "steps/s",
                 "eager_value": ne / e2e_eager_s,
                 "how": "pinned host inputs copied in (the logits on a side stream, overlapping "
